@@ -1,0 +1,324 @@
+#!/usr/bin/env python3
+"""Throughput of the PowerSGD compression step on one GB300 (per rank), as gradient GB/s
+and as a fraction of the HBM roofline.
+
+Workload: one d_model = 3968 resblock shard. The four 1/8-column weight-gradient
+matrices qkv 3968x1488, attn-out 3968x496, mlp-in 3968x1984 and mlp-out 15872x496 in
+fp16, W = 8 simulated workers, rank 112, fp16 error buffers and fp32 Q state.
+Gradients are synthetic N(0, 2^-2) fp16 (sigma 2^-12 at scale s_b = 2^10), drawn once
+on the device into two gradient sets used on alternate steps. Every step reads 378 MB
+of gradient and 378 MB of error buffer, more than the 129 MB L2, so L2 is not flushed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank compresses its own resblock shard.
+The ranks are independent blocks with no data exchange (weak scaling). The value is the
+gradient bytes of all ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+SHAPES = ((3968, 1488), (3968, 496), (3968, 1984), (15872, 496))
+W, RANK, DTYPE = 8, 112, "f16"
+WORKLOAD = "resblock_shard_3968_fp16_w8_r112"
+METRIC = "PowerSGD step gradient GB/s and % of HBM roofline (rank 112, 1 GB300)"
+UNIT = "GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}
+SMS, FP32_LANES = 152, 128  # GB300: SMs, FP32 lanes per SM
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0: max(3, steps // 10)")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def numel_per_worker():
+    return sum(m * n for m, n in SHAPES)
+
+
+# ------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1])); smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle (CPU) leg
+def oracle_sample(matrices, seconds_note=""):
+    """Time the fp64 oracle on one step of the given matrices of this workload (W = 8).
+    Returns (gradient bytes processed, seconds)."""
+    import numpy as np
+    import oracle
+    import synth
+    wl = synth.with_shapes(synth.resblock_shard(steps=1), matrices)
+    grads = [[synth.grad(wl, 0, 0, j, w).double().numpy() for w in range(W)] for j in range(len(matrices))]
+    st = oracle.BlockState(e=[[np.zeros(s) for _ in range(W)] for s in matrices],
+                           q=[synth.q0(wl, 0, j).double().numpy() for j in range(len(matrices))])
+    t0 = time.perf_counter()
+    oracle.block_step(grads, st, wl.scale(0), "f16")
+    dt = time.perf_counter() - t0
+    return W * sum(m * n for m, n in matrices) * 2, dt
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    sample = ((3968, 496),)  # attn-out, all 8 workers: about a second of fp64 work per step
+    for _ in range(args.warmup):
+        oracle_sample(sample)
+    tot_b, tot_s = 0, 0.0
+    for _ in range(args.steps):
+        b, s = oracle_sample(sample)
+        tot_b += b
+        tot_s += s
+    val = tot_b / tot_s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "attn_out 3968x496 x 8 workers"},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": "one step of the attn-out matrix (3968x496, W=8) per timed step"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------- our leg
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from rank_gradient_compression_gb300 import psgd
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234 + rank)
+    sets = []
+    for _ in range(2):
+        sets.append([[[(torch.randn((m, n), generator=g, device=dev) * 0.25).half() for _ in range(W)]
+                      for (m, n) in SHAPES]])
+    errs = [[[torch.zeros((m, n), dtype=torch.float16, device=dev) for _ in range(W)] for (m, n) in SHAPES]]
+    q = [[torch.randn((n, RANK), generator=g, device=dev) for (m, n) in SHAPES]]
+    ghat = [[torch.empty((m, n), dtype=torch.float32, device=dev) for (m, n) in SHAPES]]
+    scales = [1024.0]
+    ps = psgd.PowerSGD(SHAPES, 1, W, RANK, DTYPE, device=dev)
+
+    for i in range(args.warmup):
+        ps.step(sets[i % 2], errs, q, scales, ghat)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    psgd.psgd_profile_begin(ps.handle, args.steps)
+    launches0 = psgd.psgd_launch_count(ps.handle)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    start.record(stream)
+    for i in range(args.steps):
+        ps.step(sets[i % 2], errs, q, scales, ghat)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    launches = psgd.psgd_launch_count(ps.handle) - launches0
+    phase_ms, nprof = psgd.psgd_profile_end(ps.handle)
+    ms = start.elapsed_time(end) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---------------- end to end: pinned host gradients in, G-hat out, every step
+    e2e_steps = args.e2e_steps or max(3, args.steps // 10)
+    host_g = [[[t.cpu().pin_memory() for t in row] for row in sets[0][0]]]
+    host_gh = [[torch.empty((m, n), dtype=torch.float32).pin_memory() for (m, n) in SHAPES]]
+    dev_g = sets[1]
+    h2d = sum(t.numel() * t.element_size() for row in host_g[0] for t in row)
+    d2h = sum(t.numel() * t.element_size() for t in host_gh[0])
+    for i in range(2):
+        for j in range(len(SHAPES)):
+            for w_ in range(W):
+                dev_g[0][j][w_].copy_(host_g[0][j][w_], non_blocking=True)
+        ps.step(dev_g, errs, q, scales, ghat)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        for j in range(len(SHAPES)):
+            for w_ in range(W):
+                dev_g[0][j][w_].copy_(host_g[0][j][w_], non_blocking=True)
+        ps.step(dev_g, errs, q, scales, ghat)
+        for j in range(len(SHAPES)):
+            host_gh[0][j].copy_(ghat[0][j], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    barrier()
+
+    grad_bytes = W * numel_per_worker() * 2  # per rank per step
+    value = world * grad_bytes / (ms * 1e-3) / 1e9
+    e2e_val = world * grad_bytes / (e2e_ms * 1e-3) / 1e9
+
+    pk, pk_kind = peaks()
+    hbm = float(pk["hbm_gbs"])
+    nel = numel_per_worker()
+    we = W * nel  # worker-elements per step
+    # algorithmic bytes per launch and flops per launch, per phase (per rank)
+    alg_bytes = {"ingest": 6 * we, "pgemm": 2 * we, "qgemm": 2 * we, "decomp": 4 * we + 4 * nel,
+                 "skip_unc": 0, "orth": 0, "qreduce": 0}
+    flops = {"pgemm": 2 * we * RANK, "qgemm": 2 * we * RANK, "decomp": 2 * nel * RANK}
+    per_launch = {k: v / max(nprof, 1) for k, v in phase_ms.items()}
+    total_ms = sum(per_launch.values()) or 1.0
+    share = {k: v / total_ms for k, v in per_launch.items()}
+    dom = max(per_launch, key=per_launch.get)
+    if ps.engine == "tcgen05" and dom == "pgemm":
+        alg_bytes["pgemm"] = 0
+    d_ms = per_launch[dom]
+    sm_clock = clk.get("sm_mhz") or float(pk.get("sm_max_mhz", 2070.0))
+    if alg_bytes.get(dom, 0) and (ps.engine == "tcgen05" or dom in ("ingest", "decomp")):
+        ach = alg_bytes[dom] / (d_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": None, "kernel": dom, "peak_kind": pk_kind}
+    else:
+        ach = flops.get(dom, 0) / (d_ms * 1e-3) / 1e12
+        peak = SMS * FP32_LANES * 2 * float(pk.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak if peak else None, "traffic": None, "kernel": dom,
+                "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"}
+    step_bytes = 12 * we + 4 * nel
+    step_gbs = world * step_bytes / (ms * 1e-3) / 1e9
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "shapes": [list(s) for s in SHAPES], "workers": W,
+                       "rank": RANK, "grad_dtype": DTYPE, "engine": ps.engine,
+                       "blocks_per_rank": 1, "l2": "inputs larger than L2 (756 MB read per step), no flush",
+                       "parallelism": f"independent resblock shard per rank x{world}"},
+            "roofline": roof,
+            "step_roofline": {"alg_bytes_per_step": step_bytes, "achieved": step_gbs, "unit": "GB/s",
+                              "frac_of_measured_hbm": step_gbs / hbm / world,
+                              "frac_of_8TBs": step_gbs / 8000.0 / world},
+            "phases_ms_per_step": {k: round(v, 4) for k, v in per_launch.items()},
+            "phase_share": {k: round(v, 4) for k, v in share.items()},
+            "clocks": clk, "gpu_launches": launches,
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        b, s = oracle_sample(SHAPES)
+        line["cpu_baseline"] = {"value": b / s / 1e9, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                                "sample": "one full step of the workload (all 4 matrices, W=8) in fp64 numpy",
+                                "seconds": s}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ps.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

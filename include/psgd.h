@@ -1,0 +1,162 @@
+/*
+ * psgd.h — C ABI of the GB300 PowerSGD gradient-compression step (libpsgd.so).
+ *
+ * One call of psgd_step runs, for every weight-gradient matrix j of every resblock b
+ * and every simulated data-parallel worker w held on this GPU:
+ *
+ *   g_w   = G_w * (1/s_b); nonfinite entries of g_w set to 0 and counted
+ *   M_w   = round_E(g_w + E_w)                       (E_w: the error buffer)
+ *   skip_b = (nonfinite count of block b over all workers >= threshold_b)
+ *   P     = (1/W) sum_w M_w Q                        (first exchange point)
+ *   P^    = orthonormal basis of span(P)             (fp32, shifted CholeskyQR)
+ *   Q     = (1/W) sum_w M_w^T P^                     (second exchange point; new Q state)
+ *   G^    = P^ Q^T                                   (fp32-accurate products)
+ *   E_w   = round_E(M_w - G^)
+ *   gains/biases: u = (1/W) sum_w zero_nonfinite(U_w * (1/s_b)) in fp32
+ *
+ * Sources for what each step computes:
+ *   "Zero-Shot Text-to-Image Generation - 中文验证版" (reading card), §方法适配: per-
+ *     resblock gradient scales; PowerSGD all-reduces low-rank factors; total rank 896
+ *     = 112 per GPU shard; embedding/unembedding/gains/biases reduced in 32-bit.
+ *     §证据: error buffer, finiteness checks, grouped all-reduce, 32-bit products for
+ *     the decompressed gradient.
+ *   "[논문 정리] Zero-Shot Text-to-Image Generation", §Mixed-Precision Training: unscale
+ *     when the block ends, and Inf/NaN are set to 0. PowerSGD list: the gradient is
+ *     accumulated into the error buffer, and gains/biases stay uncompressed in 32-bit.
+ *   "AIGC 基本功|混合精度与数值稳定性", §6.2: every data-parallel rank takes the same
+ *     skip decision.
+ *
+ * Conventions (all entry points):
+ *   - Every device pointer is owned by the caller. The library allocates no device
+ *     memory. Its scratch lives in the caller's workspace (psgd_workspace_size). The
+ *     handle owns only host-side plans and one pinned host staging buffer.
+ *   - Matrices are row-major and dense: leading dimension = n. Device pointers to
+ *     gradients, error buffers and G^ must be 16-byte aligned, and n * element size
+ *     must be a multiple of 16 bytes.
+ *   - Nothing throws or exits across the ABI. Argument errors return PSGD_EINVAL or
+ *     PSGD_EUNSUPPORTED before any launch. CUDA launch/runtime errors return
+ *     PSGD_ECUDA. psgd_last_error() returns a per-thread message for the last failure.
+ *   - psgd_step is asynchronous on `stream` (a cudaStream_t, or NULL for the legacy
+ *     default stream). It never synchronises the host, except when the pointer or
+ *     scale tables differ from the previous call. Then it waits for that call's table
+ *     upload to finish before it reuses the staging buffer.
+ */
+#ifndef PSGD_H_
+#define PSGD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PSGD_F32 = 0, PSGD_F16 = 1, PSGD_BF16 = 2 } psgd_dtype;
+
+typedef enum {
+  PSGD_OK = 0,
+  PSGD_EINVAL = 1,        /* bad argument: null pointer, bad shape, misalignment, ... */
+  PSGD_ECUDA = 2,         /* a CUDA runtime or launch error */
+  PSGD_EUNSUPPORTED = 3,  /* valid but not supported by this build (e.g. dtype mix) */
+  PSGD_ETIMEOUT = 4       /* a bounded device-side wait expired (see psgd_check) */
+} psgd_status;
+
+typedef struct {
+  int64_t m, n; /* rows, columns of one weight-gradient matrix */
+} psgd_shape;
+
+/* Flags (psgd_config.flags). */
+#define PSGD_FLAG_SIMT 0x1u          /* use the FFMA GEMM engine for 16-bit too (debug) */
+#define PSGD_FLAG_MASK 0x2u          /* write the nonfinite mask bitmap (debug output) */
+#define PSGD_FLAG_STOP_AFTER_INGEST 0x4u /* only unscale/mask/count/M and skip (debug) */
+
+typedef struct {
+  int32_t num_blocks;       /* B >= 1 resblocks */
+  int32_t mats_per_block;   /* J >= 1 matrices per resblock */
+  int32_t num_workers;      /* W >= 1 simulated data-parallel workers */
+  int32_t rank;             /* r, 1 <= r <= min(m, n) for every matrix */
+  const psgd_shape* shapes; /* [J] host array: every block has the same J shapes */
+  int32_t grad_dtype;       /* psgd_dtype of G */
+  int32_t err_dtype;        /* psgd_dtype of E (and of M). 16-bit G needs the same
+                               16-bit E; fp32 G needs fp32 E. */
+  int64_t unc_len;          /* fp32 gains+biases per block per worker (0 = none) */
+  double skip_fraction;     /* T in (0, 1]: skip block b when its nonfinite count over
+                               all workers is >= ceil(T * W * numel_b) (IEEE double) */
+  uint32_t flags;           /* PSGD_FLAG_* */
+} psgd_config;
+
+typedef struct psgd_handle psgd_handle;
+
+/* Arguments of one step. Host arrays of device pointers, indexed as stated. */
+typedef struct {
+  const void* const* grads;     /* [B*J*W] G_{b,j,w} at ((b*J)+j)*W+w, grad_dtype m x n */
+  void* const* errs;            /* [B*J*W] E_{b,j,w}, err_dtype m x n, read and updated */
+  float* const* q_state;        /* [B*J] Q_{b,j}, fp32 n x r row-major; the caller
+                                   writes Q0 before the first step; updated in place */
+  const float* scales;          /* [B] host: s_b, finite and >= 1 (powers of two give
+                                   a bit-exact M) */
+  float* const* ghat;           /* [B*J] G^_{b,j}, fp32 m x n (written; 0 when skipped) */
+  const float* const* unc_in;   /* [B*W] raw gains/biases, fp32 unc_len (NULL if none) */
+  float* const* unc_out;        /* [B] mean gains/biases, fp32 unc_len (NULL if none) */
+  int64_t* counts;              /* device [B*W]: nonfinite entries of block b, worker w
+                                   (matrices and gains/biases); overwritten each step */
+  uint8_t* skip;                /* device [B]: 1 when block b was skipped */
+  uint32_t* mask_bits;          /* device, only with PSGD_FLAG_MASK (else ignored): one
+                                   bit per matrix entry, LSB-first in 32-bit words,
+                                   row-major; matrix (b,j,w) starts at word
+                                   psgd_mask_offset(cfg, b, j, w) */
+} psgd_step_args;
+
+/* Bytes of device workspace psgd_init needs for this configuration (0 on error). */
+size_t psgd_workspace_size(const psgd_config* cfg);
+
+/* Word offset of matrix (b, j, w) in the mask bitmap, and the bitmap's total words. */
+int64_t psgd_mask_offset(const psgd_config* cfg, int32_t b, int32_t j, int32_t w);
+int64_t psgd_mask_words(const psgd_config* cfg);
+
+/* Validate cfg and plan the step into `workspace` (device, >= psgd_workspace_size
+ * bytes, 256-byte aligned, owned by the caller, alive until psgd_finalize). On
+ * PSGD_OK *out holds a handle. Work is enqueued on `stream` (workspace clearing). */
+psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes,
+                      void* stream, psgd_handle** out);
+
+/* Enqueue one PowerSGD step on `stream` (see the top of this file). */
+psgd_status psgd_step(psgd_handle* h, const psgd_step_args* args, void* stream);
+
+/* Wait for `stream`, then report a device-side error raised by an earlier step
+ * (PSGD_ETIMEOUT for an expired bounded wait), and clear it. */
+psgd_status psgd_check(psgd_handle* h, void* stream);
+
+/* Release the handle's host resources. The workspace stays the caller's. NULL is a no-op. */
+psgd_status psgd_finalize(psgd_handle* h);
+
+const char* psgd_strerror(psgd_status s);
+const char* psgd_last_error(void);
+
+/* Profiling. psgd_profile_begin creates events for up to `max_steps` later steps. Each of
+ * those psgd_step calls records PSGD_NUM_PHASES + 1 events on its stream, at the phase
+ * boundaries (ingest | skip and gains/biases | P GEMM | orthonormalisation | Q GEMM |
+ * Q reduction | decompress + error update). psgd_profile_end waits for the events. It
+ * writes the summed milliseconds of each phase into phase_ms[PSGD_NUM_PHASES] and the
+ * number of profiled steps into *steps, then destroys the events. The events are host
+ * resources; no device memory is allocated. */
+#define PSGD_NUM_PHASES 7
+psgd_status psgd_profile_begin(psgd_handle* h, int32_t max_steps);
+psgd_status psgd_profile_end(psgd_handle* h, double* phase_ms, int32_t* steps);
+
+/* Total kernel launches this handle has enqueued (all steps so far). */
+int64_t psgd_launch_count(psgd_handle* h);
+
+/* Debug: device pointer to M_{b,j,w} (the error-dtype scratch written by the last step),
+ * or NULL on a bad index. */
+const void* psgd_debug_m(psgd_handle* h, int32_t b, int32_t j, int32_t w);
+/* Debug: device pointer to P^_{b,j} of the last step, fp32 m x rp row-major with
+ * rp = r rounded up to a multiple of 16 (columns r..rp-1 are 0), or NULL. */
+const float* psgd_debug_phat(psgd_handle* h, int32_t b, int32_t j);
+/* Name of the GEMM engine this handle uses: "tcgen05" or "simt". */
+const char* psgd_engine(psgd_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PSGD_H_ */

@@ -51,18 +51,22 @@ def round_to_format(x, fmt: str) -> np.ndarray:
     if fmt == "f64":
         return np.array(x, dtype=np.float64, copy=True)
     x = np.asarray(x, dtype=np.float64)
+    shape = x.shape
+    x = x.reshape(-1)
     p, emin, _, _, _ = FORMATS[fmt]
-    out = np.array(x, dtype=np.float64, copy=True)
-    fin = np.isfinite(x) & (x != 0.0)
-    xf = x[fin]
-    _, ex = np.frexp(xf)  # xf = f * 2**ex with 0.5 <= |f| < 1
-    e = np.maximum(ex - 1, emin)  # 2**e <= |xf| < 2**(e+1), clamped to the subnormal binade
-    qexp = e - (p - 1)
-    y = np.ldexp(np.rint(np.ldexp(xf, -qexp)), qexp)  # np.rint rounds half to even
-    big = np.abs(y) > max_finite(fmt)
-    y[big] = np.copysign(np.inf, xf[big])
-    out[fin] = y
-    return out
+    with np.errstate(invalid="ignore", over="ignore"):
+        _, ex = np.frexp(x)  # x = f * 2**ex with 0.5 <= |f| < 1 (ex = 0 for 0, inf, nan)
+        np.subtract(ex, p, out=ex)  # quantum exponent e - (p - 1) with e = ex - 1
+        np.maximum(ex, emin - (p - 1), out=ex)  # subnormals share the smallest binade
+        q = np.ldexp(1.0, ex)
+        y = np.divide(x, q)  # exact: q is a power of two
+        np.rint(y, out=y)  # ties to even
+        np.multiply(y, q, out=y)
+        big = np.abs(y) > max_finite(fmt)
+        y[big] = np.copysign(np.inf, x[big])
+        nf = ~np.isfinite(x)
+        y[nf] = x[nf]
+    return y.reshape(shape)
 
 
 def decode_bits(bits, fmt: str) -> np.ndarray:

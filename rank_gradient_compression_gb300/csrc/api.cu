@@ -1,0 +1,496 @@
+// Host side of the C ABI declared in psgd.h: validation, workspace planning, the
+// per-step pointer table, and the launch sequence of one PowerSGD step.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "handle.h"
+
+namespace psgd {
+namespace {
+
+thread_local std::string g_last_error;
+
+psgd_status fail(psgd_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+psgd_status cuda_fail(cudaError_t e, const char* where) {
+  g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
+  return PSGD_ECUDA;
+}
+
+size_t esize(int dt) { return dt == DT_F32 ? 4 : 2; }
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Rows of the Q-GEMM slices and Gram chunks of the FFMA engine.
+constexpr int64_t kSliceRows = 512;
+constexpr int64_t kGramRows = 256;
+
+struct Layout {
+  size_t total = 0;
+  size_t meta = 0, threshold = 0, mask_off = 0, segs = 0, table = 0, err = 0, scal = 0;
+  std::vector<size_t> mscr, P, Xa, Xb, Phat, ostate, Qpart, Gpart, Rinv;
+  size_t tc = 0;
+  size_t table_bytes = 0;
+  int64_t nseg = 0;
+};
+
+bool valid_dtype(int d) { return d == DT_F32 || d == DT_F16 || d == DT_BF16; }
+
+psgd_status validate_config(const psgd_config* c) {
+  if (!c) return fail(PSGD_EINVAL, "config is NULL");
+  if (c->num_blocks < 1 || c->mats_per_block < 1 || c->num_workers < 1)
+    return fail(PSGD_EINVAL, "num_blocks, mats_per_block and num_workers must be >= 1");
+  if (!c->shapes) return fail(PSGD_EINVAL, "shapes is NULL");
+  if (!valid_dtype(c->grad_dtype) || !valid_dtype(c->err_dtype))
+    return fail(PSGD_EINVAL, "unknown dtype");
+  if (c->grad_dtype != c->err_dtype)
+    return fail(PSGD_EUNSUPPORTED, "grad_dtype and err_dtype must be equal in this build");
+  if (c->rank < 1) return fail(PSGD_EINVAL, "rank must be >= 1");
+  if (c->rank > kMaxRank)
+    return fail(PSGD_EUNSUPPORTED, "rank above 128 is not supported by this build");
+  if (c->unc_len < 0) return fail(PSGD_EINVAL, "unc_len must be >= 0");
+  if (!(c->skip_fraction > 0.0 && c->skip_fraction <= 1.0))
+    return fail(PSGD_EINVAL, "skip_fraction must be in (0, 1]");
+  const size_t es = esize(c->grad_dtype);
+  for (int j = 0; j < c->mats_per_block; ++j) {
+    const psgd_shape s = c->shapes[j];
+    if (s.m < 1 || s.n < 1) return fail(PSGD_EINVAL, "matrix shapes must be positive");
+    if ((s.n * (int64_t)es) % 16 != 0)
+      return fail(PSGD_EINVAL, "n * element size must be a multiple of 16 bytes");
+    if (c->rank > s.m || c->rank > s.n) return fail(PSGD_EINVAL, "rank must be <= min(m, n)");
+    if (s.m > (1ll << 31) || s.n > (1ll << 31)) return fail(PSGD_EINVAL, "matrix too large");
+  }
+  return PSGD_OK;
+}
+
+Layout plan_layout(const psgd_config* c) {
+  Layout L;
+  const int B = c->num_blocks, J = c->mats_per_block, W = c->num_workers;
+  const int rp = (c->rank + 15) / 16 * 16;
+  const size_t es = esize(c->err_dtype);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = up256(off + bytes); return o; };
+  L.meta = take(sizeof(MatMeta) * B * J);
+  L.threshold = take(8 * (size_t)B);
+  L.mask_off = take(8 * (size_t)B * J * W);
+  L.nseg = (int64_t)B * J * W + (c->unc_len > 0 ? (int64_t)B * W : 0);
+  L.segs = take(sizeof(IngestSeg) * L.nseg);
+  L.table_bytes = 8 * ((size_t)2 * B * J * W + 2 * (size_t)B * J + (size_t)B * W + B) + 4 * (size_t)B;
+  L.table = take(L.table_bytes);
+  L.err = take(16);
+  L.scal = take(16 * (size_t)B * J);
+  for (int t = 0; t < B * J; ++t) {
+    const psgd_shape s = c->shapes[t % J];
+    const int64_t mpad = ceil_div(s.m, 128) * 128;
+    const int64_t S = std::max<int64_t>(1, ceil_div(s.m, kSliceRows));
+    const int64_t C = std::max<int64_t>(1, ceil_div(s.m, kGramRows));
+    L.mscr.push_back(take(es * (size_t)W * s.m * s.n));
+    L.P.push_back(take(4 * (size_t)mpad * rp));
+    L.Xa.push_back(take(4 * (size_t)mpad * rp));
+    L.Xb.push_back(take(4 * (size_t)mpad * rp));
+    L.Phat.push_back(take(4 * (size_t)mpad * rp));
+    L.ostate.push_back(take(4 * 4 * kMaxPasses));
+    L.Qpart.push_back(take(4 * (size_t)S * s.n * rp));
+    L.Gpart.push_back(take(4 * (size_t)C * rp * rp));
+    L.Rinv.push_back(take(4 * (size_t)rp * rp));
+  }
+  L.tc = take(tc_workspace_bytes(c));
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+}  // namespace psgd
+
+using namespace psgd;
+
+struct psgd_handle {
+  Handle h;
+};
+
+extern "C" {
+
+const char* psgd_strerror(psgd_status s) {
+  switch (s) {
+    case PSGD_OK: return "ok";
+    case PSGD_EINVAL: return "invalid argument";
+    case PSGD_ECUDA: return "CUDA error";
+    case PSGD_EUNSUPPORTED: return "unsupported configuration";
+    case PSGD_ETIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* psgd_last_error(void) { return g_last_error.c_str(); }
+
+size_t psgd_workspace_size(const psgd_config* cfg) {
+  if (validate_config(cfg) != PSGD_OK) return 0;
+  return plan_layout(cfg).total;
+}
+
+int64_t psgd_mask_words(const psgd_config* c) {
+  if (validate_config(c) != PSGD_OK) return -1;
+  int64_t tot = 0;
+  for (int j = 0; j < c->mats_per_block; ++j)
+    tot += ceil_div(c->shapes[j].m * c->shapes[j].n, 32);
+  return tot * c->num_blocks * c->num_workers;
+}
+
+int64_t psgd_mask_offset(const psgd_config* c, int32_t b, int32_t j, int32_t w) {
+  if (validate_config(c) != PSGD_OK) return -1;
+  if (b < 0 || b >= c->num_blocks || j < 0 || j >= c->mats_per_block || w < 0 ||
+      w >= c->num_workers)
+    return -1;
+  int64_t per_block = 0, before_j = 0;
+  for (int k = 0; k < c->mats_per_block; ++k) {
+    const int64_t words = ceil_div(c->shapes[k].m * c->shapes[k].n, 32);
+    if (k < j) before_j += words;
+    per_block += words;
+  }
+  const int64_t wj = ceil_div(c->shapes[j].m * c->shapes[j].n, 32);
+  return (int64_t)b * c->num_workers * per_block + before_j * c->num_workers + (int64_t)w * wj;
+}
+
+psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, void* stream,
+                      psgd_handle** out) {
+  if (!out) return fail(PSGD_EINVAL, "out is NULL");
+  *out = nullptr;
+  psgd_status st = validate_config(cfg);
+  if (st != PSGD_OK) return st;
+  if (!workspace) return fail(PSGD_EINVAL, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(PSGD_EINVAL, "workspace must be 256-byte aligned");
+  const Layout L = plan_layout(cfg);
+  if (ws_bytes < L.total)
+    return fail(PSGD_EINVAL, "workspace too small: need " + std::to_string(L.total) + " bytes");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  psgd_handle* ph = new (std::nothrow) psgd_handle();
+  if (!ph) return fail(PSGD_EINVAL, "out of host memory");
+  Handle& h = ph->h;
+  h.cfg = *cfg;
+  h.shapes.assign(cfg->shapes, cfg->shapes + cfg->mats_per_block);
+  h.cfg.shapes = h.shapes.data();
+  h.B = cfg->num_blocks; h.J = cfg->mats_per_block; h.W = cfg->num_workers;
+  h.r = cfg->rank; h.rp = (cfg->rank + 15) / 16 * 16;
+  h.gdt = cfg->grad_dtype; h.edt = cfg->err_dtype;
+  h.ws = static_cast<char*>(workspace);
+  h.ws_bytes = ws_bytes;
+  std::string why;
+  h.tc = h.edt != DT_F32 && !(cfg->flags & PSGD_FLAG_SIMT) && tc_supported(cfg, &why);
+
+  const int BJ = h.B * h.J;
+  h.d_meta = reinterpret_cast<MatMeta*>(h.ws + L.meta);
+  h.d_threshold = reinterpret_cast<int64_t*>(h.ws + L.threshold);
+  h.d_mask_off = reinterpret_cast<int64_t*>(h.ws + L.mask_off);
+  h.d_segs = reinterpret_cast<IngestSeg*>(h.ws + L.segs);
+  h.d_table = h.ws + L.table;
+  h.table_bytes = L.table_bytes;
+  h.d_err = reinterpret_cast<int*>(h.ws + L.err);
+  h.d_scal_all = reinterpret_cast<float*>(h.ws + L.scal);
+
+  h.meta.resize(BJ);
+  for (int t = 0; t < BJ; ++t) {
+    const psgd_shape sh = h.shapes[t % h.J];
+    MatMeta& mt = h.meta[t];
+    std::memset(&mt, 0, sizeof(mt));
+    mt.m = sh.m; mt.n = sh.n; mt.b = t / h.J; mt.j = t % h.J;
+    mt.S = (int)std::max<int64_t>(1, ceil_div(sh.m, kSliceRows));
+    mt.C = (int)std::max<int64_t>(1, ceil_div(sh.m, kGramRows));
+    mt.mtiles = (int)ceil_div(sh.m, 128);
+    mt.mscr = h.ws + L.mscr[t];
+    mt.P = reinterpret_cast<float*>(h.ws + L.P[t]);
+    mt.Xa = reinterpret_cast<float*>(h.ws + L.Xa[t]);
+    mt.Xb = reinterpret_cast<float*>(h.ws + L.Xb[t]);
+    mt.Phat = reinterpret_cast<float*>(h.ws + L.Phat[t]);
+    mt.ostate = reinterpret_cast<int*>(h.ws + L.ostate[t]);
+    mt.Qpart = reinterpret_cast<float*>(h.ws + L.Qpart[t]);
+    mt.Gpart = reinterpret_cast<float*>(h.ws + L.Gpart[t]);
+    mt.Rinv = reinterpret_cast<float*>(h.ws + L.Rinv[t]);
+    mt.scal = h.d_scal_all + 4 * t;
+    h.max_mtiles = std::max(h.max_mtiles, mt.mtiles);
+    h.max_S = std::max(h.max_S, mt.S);
+    h.max_C = std::max(h.max_C, mt.C);
+    h.max_ntiles64 = std::max<int>(h.max_ntiles64, (int)ceil_div(sh.n, 64));
+    h.max_mtiles64 = std::max<int>(h.max_mtiles64, (int)ceil_div(sh.m, 64));
+    h.max_ntiles128 = std::max<int>(h.max_ntiles128, (int)ceil_div(sh.n, 128));
+  }
+  // thresholds: ceil(T * W * numel_b) in IEEE double
+  int64_t numel_b = cfg->unc_len;
+  for (int j = 0; j < h.J; ++j) numel_b += h.shapes[j].m * h.shapes[j].n;
+  std::vector<int64_t> thr(h.B, (int64_t)std::ceil(cfg->skip_fraction * (double)(h.W * numel_b)));
+  std::vector<int64_t> moff((size_t)BJ * h.W);
+  for (int b = 0; b < h.B; ++b)
+    for (int j = 0; j < h.J; ++j)
+      for (int w = 0; w < h.W; ++w) moff[((size_t)b * h.J + j) * h.W + w] = psgd_mask_offset(cfg, b, j, w);
+  // ingest segments
+  int64_t cta = 0;
+  for (int t = 0; t < BJ; ++t)
+    for (int w = 0; w < h.W; ++w) {
+      IngestSeg sg{};
+      sg.numel = h.meta[t].m * h.meta[t].n;
+      sg.cta_start = cta;
+      sg.kind = 0; sg.t = t; sg.b = h.meta[t].b; sg.w = w;
+      h.segs.push_back(sg);
+      cta += ceil_div(sg.numel, kIngestChunk);
+    }
+  if (cfg->unc_len > 0)
+    for (int b = 0; b < h.B; ++b)
+      for (int w = 0; w < h.W; ++w) {
+        IngestSeg sg{};
+        sg.numel = cfg->unc_len;
+        sg.cta_start = cta;
+        sg.kind = 1; sg.t = -1; sg.b = b; sg.w = w;
+        h.segs.push_back(sg);
+        cta += ceil_div(sg.numel, kIngestChunk);
+      }
+  h.ingest_ctas = cta;
+
+  cudaError_t e;
+  if (h.tc && (e = tc_plan(h, h.ws + L.tc, s)) != cudaSuccess) {
+    tc_free(h);
+    delete ph;
+    return cuda_fail(e, "tensor-engine plan");
+  }
+  // Upload the static tables (synchronously: init is not on the hot path).
+  e = cudaMemcpyAsync(h.d_meta, h.meta.data(), sizeof(MatMeta) * BJ, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h.d_threshold, thr.data(), 8 * thr.size(), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h.d_mask_off, moff.data(), 8 * moff.size(), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h.d_segs, h.segs.data(), sizeof(IngestSeg) * h.segs.size(), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h.d_err, 0, 16, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&h.h_stage), h.table_bytes, cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.upload_ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    if (h.h_stage) cudaFreeHost(h.h_stage);
+    tc_free(h);
+    delete ph;
+    return cuda_fail(e, "psgd_init");
+  }
+  const size_t B = h.B, J = h.J, W = h.W;
+  char* base = h.d_table;
+  h.tab.g = reinterpret_cast<const void* const*>(base);
+  h.tab.e = reinterpret_cast<void* const*>(base + 8 * B * J * W);
+  h.tab.q = reinterpret_cast<float* const*>(base + 16 * B * J * W);
+  h.tab.ghat = reinterpret_cast<float* const*>(base + 16 * B * J * W + 8 * B * J);
+  h.tab.unc_in = reinterpret_cast<const float* const*>(base + 16 * B * J * W + 16 * B * J);
+  h.tab.unc_out = reinterpret_cast<float* const*>(base + 16 * B * J * W + 16 * B * J + 8 * B * W);
+  h.tab.inv_scale = reinterpret_cast<const float*>(base + 16 * B * J * W + 16 * B * J + 8 * B * W + 8 * B);
+  *out = ph;
+  return PSGD_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
+  if (!ph || !a) return fail(PSGD_EINVAL, "handle or args is NULL");
+  Handle& h = ph->h;
+  const size_t B = h.B, J = h.J, W = h.W;
+  if (!a->grads || !a->errs || !a->q_state || !a->scales || !a->ghat || !a->counts || !a->skip)
+    return fail(PSGD_EINVAL, "a required argument array is NULL");
+  if (h.cfg.unc_len > 0 && (!a->unc_in || !a->unc_out))
+    return fail(PSGD_EINVAL, "unc_in/unc_out are required when unc_len > 0");
+  if ((h.cfg.flags & PSGD_FLAG_MASK) && !a->mask_bits)
+    return fail(PSGD_EINVAL, "mask_bits is required with PSGD_FLAG_MASK");
+  for (size_t i = 0; i < B * J * W; ++i) {
+    if (!a->grads[i] || !a->errs[i]) return fail(PSGD_EINVAL, "NULL gradient or error pointer");
+    if (!aligned16(a->grads[i]) || !aligned16(a->errs[i]))
+      return fail(PSGD_EINVAL, "gradient and error pointers must be 16-byte aligned");
+  }
+  for (size_t i = 0; i < B * J; ++i) {
+    if (!a->q_state[i] || !a->ghat[i]) return fail(PSGD_EINVAL, "NULL Q or G-hat pointer");
+    if (!aligned16(a->ghat[i])) return fail(PSGD_EINVAL, "G-hat pointers must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(a->q_state[i]) & 3u) return fail(PSGD_EINVAL, "Q must be 4-byte aligned");
+  }
+  for (size_t b = 0; b < B; ++b) {
+    const float s = a->scales[b];
+    if (!std::isfinite(s) || !(s >= 1.0f)) return fail(PSGD_EINVAL, "scales must be finite and >= 1");
+  }
+  if (h.cfg.unc_len > 0) {
+    for (size_t i = 0; i < B * W; ++i)
+      if (!a->unc_in[i] || (reinterpret_cast<uintptr_t>(a->unc_in[i]) & 3u))
+        return fail(PSGD_EINVAL, "unc_in pointers must be non-NULL and 4-byte aligned");
+    for (size_t b = 0; b < B; ++b)
+      if (!a->unc_out[b] || (reinterpret_cast<uintptr_t>(a->unc_out[b]) & 3u))
+        return fail(PSGD_EINVAL, "unc_out pointers must be non-NULL and 4-byte aligned");
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+
+  // Pointer table: upload only when it differs from the previous step's.
+  std::vector<char> tab(h.table_bytes, 0);
+  char* o = tab.data();
+  std::memcpy(o, a->grads, 8 * B * J * W); o += 8 * B * J * W;
+  std::memcpy(o, a->errs, 8 * B * J * W); o += 8 * B * J * W;
+  std::memcpy(o, a->q_state, 8 * B * J); o += 8 * B * J;
+  std::memcpy(o, a->ghat, 8 * B * J); o += 8 * B * J;
+  if (h.cfg.unc_len > 0) std::memcpy(o, a->unc_in, 8 * B * W);
+  o += 8 * B * W;
+  if (h.cfg.unc_len > 0) std::memcpy(o, a->unc_out, 8 * B);
+  o += 8 * B;
+  for (size_t b = 0; b < B; ++b) {
+    const float inv = (float)(1.0 / (double)a->scales[b]);
+    std::memcpy(o + 4 * b, &inv, 4);
+  }
+  if (!h.have_table || tab != h.last_table) {
+    if (h.have_table && (e = cudaEventSynchronize(h.upload_ev)) != cudaSuccess) return cuda_fail(e, "table event");
+    std::memcpy(h.h_stage, tab.data(), h.table_bytes);
+    if ((e = cudaMemcpyAsync(h.d_table, h.h_stage, h.table_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+      return cuda_fail(e, "table upload");
+    if ((e = cudaEventRecord(h.upload_ev, s)) != cudaSuccess) return cuda_fail(e, "table event");
+    h.last_table.swap(tab);
+    h.have_table = true;
+  }
+
+  Plan p{};
+  p.B = h.B; p.J = h.J; p.W = h.W; p.r = h.r; p.rp = h.rp;
+  p.gdt = h.gdt; p.edt = h.edt;
+  p.unc_len = h.cfg.unc_len;
+  p.meta = h.d_meta;
+  p.threshold = h.d_threshold;
+  p.tab = h.tab;
+  p.counts = a->counts;
+  p.skip = a->skip;
+  p.mask = (h.cfg.flags & PSGD_FLAG_MASK) ? a->mask_bits : nullptr;
+  p.mask_off = h.d_mask_off;
+  p.err_word = h.d_err;
+
+  cudaEvent_t* ev = nullptr;
+  if (h.prof_used < h.prof_max) ev = &h.prof_events[(size_t)h.prof_used++ * (PSGD_NUM_PHASES + 1)];
+  int phase = 0;
+  auto mark = [&]() { if (ev) cudaEventRecord(ev[phase++], s); };
+  mark();
+  if ((e = cudaMemsetAsync(a->counts, 0, 8 * B * W, s)) != cudaSuccess) return cuda_fail(e, "counts");
+  if ((e = cudaMemsetAsync(h.d_scal_all, 0, 16 * B * J, s)) != cudaSuccess) return cuda_fail(e, "scal");
+  if ((e = launch_ingest(h, p, s)) != cudaSuccess) return cuda_fail(e, "ingest");
+  mark();
+  if ((e = launch_skip_and_unc(h, p, s)) != cudaSuccess) return cuda_fail(e, "skip");
+  mark();
+  if (h.cfg.flags & PSGD_FLAG_STOP_AFTER_INGEST) {
+    while (ev && phase <= PSGD_NUM_PHASES) mark();
+    return PSGD_OK;
+  }
+  if (h.tc) {
+    if ((e = launch_prep_q(h, p, s)) != cudaSuccess) return cuda_fail(e, "prep_q");
+    if ((e = launch_pgemm_tc(h, p, s)) != cudaSuccess) return cuda_fail(e, "pgemm_tc");
+  } else if ((e = launch_pgemm_simt(h, p, s)) != cudaSuccess) {
+    return cuda_fail(e, "pgemm");
+  }
+  mark();
+  if ((e = launch_orth(h, p, s)) != cudaSuccess) return cuda_fail(e, "orth");
+  mark();
+  if (h.tc) {
+    if ((e = launch_qgemm_tc(h, p, s)) != cudaSuccess) return cuda_fail(e, "qgemm_tc");
+  } else if ((e = launch_qgemm_simt(h, p, s)) != cudaSuccess) {
+    return cuda_fail(e, "qgemm");
+  }
+  mark();
+  if ((e = launch_qreduce(h, p, s)) != cudaSuccess) return cuda_fail(e, "qreduce");
+  mark();
+  if (h.tc) {
+    if ((e = launch_decomp_tc(h, p, s)) != cudaSuccess) return cuda_fail(e, "decomp_tc");
+  } else if ((e = launch_decomp_simt(h, p, s)) != cudaSuccess) {
+    return cuda_fail(e, "decomp");
+  }
+  mark();
+  return PSGD_OK;
+}
+
+static void destroy_profile(Handle& h) {
+  for (cudaEvent_t e : h.prof_events)
+    if (e) cudaEventDestroy(e);
+  h.prof_events.clear();
+  h.prof_max = h.prof_used = 0;
+}
+
+psgd_status psgd_profile_begin(psgd_handle* ph, int32_t max_steps) {
+  if (!ph || max_steps < 1) return fail(PSGD_EINVAL, "bad handle or max_steps");
+  Handle& h = ph->h;
+  destroy_profile(h);
+  h.prof_events.assign((size_t)max_steps * (PSGD_NUM_PHASES + 1), nullptr);
+  for (auto& e : h.prof_events) {
+    cudaError_t err = cudaEventCreate(&e);
+    if (err != cudaSuccess) { destroy_profile(h); return cuda_fail(err, "profile events"); }
+  }
+  h.prof_max = max_steps;
+  h.prof_used = 0;
+  return PSGD_OK;
+}
+
+psgd_status psgd_profile_end(psgd_handle* ph, double* phase_ms, int32_t* steps) {
+  if (!ph || !phase_ms || !steps) return fail(PSGD_EINVAL, "NULL argument");
+  Handle& h = ph->h;
+  for (int k = 0; k < PSGD_NUM_PHASES; ++k) phase_ms[k] = 0.0;
+  *steps = h.prof_used;
+  for (int i = 0; i < h.prof_used; ++i) {
+    cudaEvent_t* ev = &h.prof_events[(size_t)i * (PSGD_NUM_PHASES + 1)];
+    cudaError_t e = cudaEventSynchronize(ev[PSGD_NUM_PHASES]);
+    if (e != cudaSuccess) { destroy_profile(h); return cuda_fail(e, "profile sync"); }
+    for (int k = 0; k < PSGD_NUM_PHASES; ++k) {
+      float ms = 0.f;
+      e = cudaEventElapsedTime(&ms, ev[k], ev[k + 1]);
+      if (e != cudaSuccess) { destroy_profile(h); return cuda_fail(e, "profile elapsed"); }
+      phase_ms[k] += ms;
+    }
+  }
+  destroy_profile(h);
+  return PSGD_OK;
+}
+
+int64_t psgd_launch_count(psgd_handle* ph) { return ph ? ph->h.launches : -1; }
+
+psgd_status psgd_check(psgd_handle* ph, void* stream) {
+  if (!ph) return fail(PSGD_EINVAL, "handle is NULL");
+  Handle& h = ph->h;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "psgd_check");
+  int word = 0;
+  if ((e = cudaMemcpy(&word, h.d_err, 4, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e, "psgd_check");
+  if (word != DEVERR_NONE) {
+    cudaMemset(h.d_err, 0, 4);
+    if (word == DEVERR_TIMEOUT) return fail(PSGD_ETIMEOUT, "a bounded device-side wait expired");
+    return fail(PSGD_ECUDA, "device-side check failed (code " + std::to_string(word) + ")");
+  }
+  return PSGD_OK;
+}
+
+psgd_status psgd_finalize(psgd_handle* ph) {
+  if (!ph) return PSGD_OK;
+  Handle& h = ph->h;
+  if (h.upload_ev) { cudaEventSynchronize(h.upload_ev); cudaEventDestroy(h.upload_ev); }
+  if (h.h_stage) cudaFreeHost(h.h_stage);
+  destroy_profile(h);
+  tc_free(h);
+  delete ph;
+  return PSGD_OK;
+}
+
+const void* psgd_debug_m(psgd_handle* ph, int32_t b, int32_t j, int32_t w) {
+  if (!ph) return nullptr;
+  Handle& h = ph->h;
+  if (b < 0 || b >= h.B || j < 0 || j >= h.J || w < 0 || w >= h.W) return nullptr;
+  const MatMeta& mt = h.meta[(size_t)b * h.J + j];
+  return static_cast<const char*>(mt.mscr) + (size_t)w * mt.m * mt.n * esize(h.edt);
+}
+
+const float* psgd_debug_phat(psgd_handle* ph, int32_t b, int32_t j) {
+  if (!ph) return nullptr;
+  Handle& h = ph->h;
+  if (b < 0 || b >= h.B || j < 0 || j >= h.J) return nullptr;
+  return h.meta[(size_t)b * h.J + j].Phat;
+}
+
+const char* psgd_engine(psgd_handle* ph) {
+  if (!ph) return "";
+  return ph->h.tc ? "tcgen05" : "simt";
+}
+
+}  // extern "C"

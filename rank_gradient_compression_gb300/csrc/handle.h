@@ -1,0 +1,72 @@
+// Host-side handle of libpsgd.so (shared by the .cu files; not part of the ABI).
+#pragma once
+
+#include <string>
+#include <vector>
+
+#include "psgd_internal.cuh"
+
+namespace psgd {
+
+// One contiguous range of work for the ingest kernel: matrix (t, w) or gains/biases
+// (b, w). CTAs [cta_start, cta_start + ceil(numel / kIngestChunk)) process it.
+struct IngestSeg {
+  int64_t numel;
+  int64_t cta_start;
+  int32_t kind;  // 0 = matrix, 1 = gains/biases
+  int32_t t;     // matrix index b*J+j (kind 0)
+  int32_t b, w;
+};
+
+constexpr int kIngestThreads = 256;
+constexpr int kIngestVec = 8;     // elements per thread per iteration
+constexpr int kIngestIters = 4;   // iterations per CTA
+constexpr int64_t kIngestChunk = (int64_t)kIngestThreads * kIngestVec * kIngestIters;
+
+struct Handle {
+  psgd_config cfg{};
+  std::vector<psgd_shape> shapes;
+  int B = 0, J = 0, W = 0, r = 0, rp = 0;
+  int gdt = 0, edt = 0;
+  bool tc = false;  // tcgen05 engine for the GEMMs
+  char* ws = nullptr;
+  size_t ws_bytes = 0;
+
+  std::vector<MatMeta> meta;
+  MatMeta* d_meta = nullptr;
+  int64_t* d_threshold = nullptr;
+  int64_t* d_mask_off = nullptr;
+  std::vector<IngestSeg> segs;
+  IngestSeg* d_segs = nullptr;
+  int64_t ingest_ctas = 0;
+
+  // per-step pointer table
+  char* d_table = nullptr;
+  size_t table_bytes = 0;
+  char* h_stage = nullptr;  // pinned
+  std::vector<char> last_table;
+  cudaEvent_t upload_ev = nullptr;
+  bool have_table = false;
+  StepTable tab{};
+
+  int* d_err = nullptr;
+  float* d_scal_all = nullptr;  // [B*J*4] scaling words, zeroed every step
+  int max_mtiles = 0, max_S = 0, max_C = 0, max_ntiles64 = 0, max_mtiles64 = 0;
+  int max_kchunks = 0, max_ntiles128 = 0;
+  void* tc_plan = nullptr;  // tensor-engine work lists (tc.cu)
+  mutable int64_t launches = 0;  // kernels enqueued so far
+  std::vector<cudaEvent_t> prof_events;  // [max_steps][PSGD_NUM_PHASES + 1]
+  int prof_max = 0, prof_used = 0;
+};
+
+// Tensor-engine planning and launches (tc.cu).
+size_t tc_workspace_bytes(const psgd_config* cfg);
+bool tc_supported(const psgd_config* cfg, std::string* why);
+cudaError_t tc_plan(Handle& h, char* ws_tc, cudaStream_t s);
+cudaError_t launch_prep_q(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_decomp_tc(const Handle& h, const Plan& p, cudaStream_t s);
+void tc_free(Handle& h);
+
+}  // namespace psgd

@@ -1,0 +1,123 @@
+// Internal declarations shared by the CUDA translation units of libpsgd.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "psgd.h"
+
+namespace psgd {
+
+enum : int { DT_F32 = PSGD_F32, DT_F16 = PSGD_F16, DT_BF16 = PSGD_BF16 };
+
+// Device error word values (psgd_check maps them to psgd_status).
+enum : int { DEVERR_NONE = 0, DEVERR_TIMEOUT = 1, DEVERR_BOUNDS = 2 };
+
+// Per-matrix metadata, built once by psgd_init (t = b*J + j).
+struct MatMeta {
+  int64_t m, n;
+  int32_t b, j;
+  int32_t S;          // row slices of the Q GEMM (split-K over m)
+  int32_t C;          // row chunks of the Gram matrix
+  int32_t mtiles;     // 128-row tiles
+  int32_t kchunks;    // column chunks of the P GEMM (tensor path)
+  void* mscr;         // W consecutive m x n matrices, error dtype (M_w)
+  float* P;           // m x rp fp32: P (mean over workers)
+  float* Xa;          // m x rp fp32: orthonormalisation work buffers
+  float* Xb;
+  float* Phat;        // m x rp fp32: orthonormal basis
+  int* ostate;        // [kMaxPasses][4]: final, dst buffer, shifted, dead columns
+  float* Ppart;       // kchunks x mpad x rp fp32: P GEMM partial sums (tensor path)
+  float* Qpart;       // S x n x rp fp32: Q GEMM partial sums
+  float* Gpart;       // C x rp x rp fp32: Gram partial sums
+  float* Rinv;        // rp x rp fp32: inverse Cholesky factor of the current pass
+  uint16_t* qsplit;   // [2*rp][n] 16-bit: Q (scaled) hi rows then lo rows, K-major B
+  uint16_t* psplit;   // [2*rp][mpad] 16-bit: P^ (scaled) hi rows then lo rows
+  uint16_t* pdec;     // [mpad][3*rp] 16-bit: [P^hi | P^lo | P^hi] rows (decompress A)
+  uint16_t* qdec;     // [npad][3*rp] 16-bit: [Q hi | Q hi | Q lo] rows (decompress B)
+  float* scal;        // [4]: 0 = max|P| bits, 1 = P^ scale, 2 = Q scale, 3 = spare
+};
+
+constexpr int kMaxPasses = 5;  // CholeskyQR passes at most (shifted ones included)
+constexpr int kMaxRank = 128;  // largest r of this build
+
+// Per-step device pointer tables (uploaded when they change).
+struct StepTable {
+  const void* const* g;          // [B*J*W]
+  void* const* e;                // [B*J*W]
+  float* const* q;               // [B*J]
+  float* const* ghat;            // [B*J]
+  const float* const* unc_in;    // [B*W] or null
+  float* const* unc_out;         // [B] or null
+  const float* inv_scale;        // [B]
+};
+
+struct Plan {
+  int32_t B, J, W, r, rp;        // rp: r rounded up to a multiple of 16 (tensor path)
+  int32_t gdt, edt;
+  int64_t unc_len;
+  const MatMeta* meta;           // [B*J]
+  const int64_t* threshold;      // [B]
+  StepTable tab;
+  int64_t* counts;               // [B*W]
+  uint8_t* skip;                 // [B]
+  uint32_t* mask;                // bitmap or null
+  const int64_t* mask_off;       // [B*J*W]
+  int* err_word;
+};
+
+// ---------------------------------------------------------------- numerics helpers
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// a + b rounded to odd in fp32 (exact sum known through Knuth's TwoSum). A second
+// rounding of a round-to-odd result to a format with at most 22 significant bits is
+// the correctly rounded (RNE) sum in that format (Boldo & Melquiond, "When double
+// rounding is odd"). This is what lets M = round_E(g + E) match an exact-arithmetic
+// reference bit for bit.
+__device__ __forceinline__ float add_round_odd(float a, float b) {
+  float s = __fadd_rn(a, b);
+  float bb = __fsub_rn(s, a);
+  float err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  uint32_t u = __float_as_uint(s);
+  if (err != 0.0f && (u & 1u) == 0u && isfinite(s)) {
+    bool away = (err > 0.0f) == (s > 0.0f);
+    u = away ? u + 1u : u - 1u;
+  }
+  return __uint_as_float(u);
+}
+
+// round_E(a + b) with E = T; exact single rounding for 16-bit T, plain RN for fp32.
+template <typename T> __device__ __forceinline__ T add_to(float a, float b) {
+  return from_f<T>(add_round_odd(a, b));
+}
+template <> __device__ __forceinline__ float add_to<float>(float a, float b) {
+  return __fadd_rn(a, b);
+}
+
+// Bounded spin: returns false after `limit` polls.
+#define PSGD_SPIN_LIMIT (1u << 26)
+
+}  // namespace psgd
+
+// Launchers implemented in the .cu files (host side). Each returns cudaGetLastError().
+namespace psgd {
+struct Handle;
+cudaError_t launch_ingest(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_skip_and_unc(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_pgemm_simt(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_orth(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_qgemm_simt(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_qreduce(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_decomp_simt(const Handle& h, const Plan& p, cudaStream_t s);
+}  // namespace psgd

@@ -1,0 +1,309 @@
+// FFMA engine of the three matrix products of the step: P = (1/W) sum_w M_w Q,
+// Q = (1/W) sum_w M_w^T P^ (split-K partials, then a fixed-order reduction), and
+// G^ = P^ Q^T fused with the error update E_w = round_E(M_w - G^).
+//
+// This engine runs fp32 gradients and serves as the debug reference of the tensor
+// engine (PSGD_FLAG_SIMT). All sums run in a fixed order, so results are
+// deterministic.
+#include "handle.h"
+
+namespace psgd {
+namespace {
+
+constexpr int kT = 256;
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T* p) { return to_f(*p); }
+
+// P tile: 64 rows x 128 columns of r. grid = (ceil(m/64), ceil(r/128), B*J).
+template <typename TE>
+__global__ void __launch_bounds__(kT) k_pgemm(Plan p) {
+  const MatMeta& mt = p.meta[blockIdx.z];
+  if (p.skip[mt.b]) return;
+  const int64_t m = mt.m, n = mt.n;
+  const int r = p.r, rp = p.rp;
+  const int row0 = blockIdx.x * 64;
+  if (row0 >= m) return;
+  const int col0 = blockIdx.y * 128;
+  const float* Q = p.tab.q[blockIdx.z];
+  __shared__ float As[32][64 + 4];
+  __shared__ __align__(16) float Bs[32][128];
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int w = 0; w < p.W; ++w) {
+    const TE* M = static_cast<const TE*>(mt.mscr) + (size_t)w * m * n;
+    for (int64_t k0 = 0; k0 < n; k0 += 32) {
+      {
+        const int rr = tid >> 2, kk = (tid & 3) * 8;
+        const int64_t row = row0 + rr;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int64_t k = k0 + kk + i;
+          As[kk + i][rr] = (row < m && k < n) ? ldf(M + row * n + k) : 0.f;
+        }
+      }
+      {
+        const int kk = tid >> 3, c = (tid & 7) * 16;
+        const int64_t k = k0 + kk;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int col = col0 + c + i;
+          Bs[kk][c + i] = (k < n && col < r) ? Q[k * r + col] : 0.f;
+        }
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < 32; ++kk) {
+        float a[4], b[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+        const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 8]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 8 + 4]);
+        b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+        b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
+      __syncthreads();
+    }
+  }
+  unsigned vmax = 0u;
+  const float fw = (float)p.W;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t row = row0 + ty * 4 + i;
+    if (row >= m) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int col = col0 + tx * 8 + j;
+      if (col < r) {
+        const float v = __fdiv_rn(acc[i][j], fw);
+        mt.P[row * rp + col] = v;
+        vmax = max(vmax, __float_as_uint(fabsf(v)));
+      }
+    }
+  }
+  vmax = __reduce_max_sync(0xffffffffu, vmax);
+  if ((tid & 31) == 0 && vmax) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 1, vmax);
+}
+
+// Q partials: Qpart[s][n-tile 64][r-tile 128] = sum_w sum_{rows of slice s} M_w^T P^.
+// grid = (ceil(n/64), S * ceil(r/128), B*J).
+template <typename TE>
+__global__ void __launch_bounds__(kT) k_qgemm(Plan p) {
+  const MatMeta& mt = p.meta[blockIdx.z];
+  if (p.skip[mt.b]) return;
+  const int64_t m = mt.m, n = mt.n;
+  const int r = p.r, rp = p.rp;
+  const int rtiles = (r + 127) / 128;
+  const int s = blockIdx.y / rtiles, rt = blockIdx.y % rtiles;
+  if (s >= mt.S) return;
+  const int64_t n0 = (int64_t)blockIdx.x * 64;
+  if (n0 >= n) return;
+  const int col0 = rt * 128;
+  const int64_t rows_per = ((m + mt.S - 1) / mt.S + 31) / 32 * 32;
+  const int64_t rbeg = s * rows_per, rend = min(m, rbeg + rows_per);
+  __shared__ float As[32][64 + 4];
+  __shared__ __align__(16) float Bs[32][128];
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int w = 0; w < p.W; ++w) {
+    const TE* M = static_cast<const TE*>(mt.mscr) + (size_t)w * m * n;
+    for (int64_t k0 = rbeg; k0 < rend; k0 += 32) {
+      {
+        const int kk = tid >> 3, c = (tid & 7) * 8;
+        const int64_t row = k0 + kk;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int64_t col = n0 + c + i;
+          As[kk][c + i] = (row < rend && col < n) ? ldf(M + row * n + col) : 0.f;
+        }
+      }
+      {
+        const int kk = tid >> 3, c = (tid & 7) * 16;
+        const int64_t row = k0 + kk;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int col = col0 + c + i;
+          Bs[kk][c + i] = (row < rend && col < r) ? mt.Phat[row * rp + col] : 0.f;
+        }
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < 32; ++kk) {
+        float a[4], b[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+        const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 8]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 8 + 4]);
+        b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+        b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
+      __syncthreads();
+    }
+  }
+  float* out = mt.Qpart + (size_t)s * n * rp;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t col = n0 + ty * 4 + i;
+    if (col >= n) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = col0 + tx * 8 + j;
+      if (c < r) out[col * rp + c] = acc[i][j];
+    }
+  }
+}
+
+// Q = (sum_s Qpart[s]) / W in slice order -> the caller's fp32 Q state (n x r).
+__global__ void k_qreduce(Plan p) {
+  const MatMeta& mt = p.meta[blockIdx.y];
+  if (p.skip[mt.b]) return;
+  const int64_t total = mt.n * p.r;
+  const float fw = (float)p.W;
+  float* q = p.tab.q[blockIdx.y];
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / p.r, c = i % p.r;
+    float acc = 0.f;
+    for (int s = 0; s < mt.S; ++s) acc = __fadd_rn(acc, mt.Qpart[((size_t)s * mt.n + row) * p.rp + c]);
+    q[i] = __fdiv_rn(acc, fw);
+  }
+}
+
+template <typename TE> struct V4;
+template <> struct V4<float> { using T = float4; };
+template <> struct V4<__half> { using T = uint2; };
+template <> struct V4<__nv_bfloat16> { using T = uint2; };
+
+// G^ tile 64 x 64 = P^ Q^T (K = r, fp32 FFMA), then for every worker
+// E_w = round_E(M_w - G^) on the same tile. grid = (ceil(n/64), ceil(m/64), B*J).
+template <typename TE>
+__global__ void __launch_bounds__(kT) k_decomp(Plan p) {
+  const MatMeta& mt = p.meta[blockIdx.z];
+  const int64_t m = mt.m, n = mt.n;
+  const int64_t row0 = (int64_t)blockIdx.y * 64, col0 = (int64_t)blockIdx.x * 64;
+  if (row0 >= m || col0 >= n) return;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float* gh = p.tab.ghat[blockIdx.z];
+  const bool skipped = p.skip[mt.b] != 0;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  if (!skipped) {
+    const int r = p.r, rp = p.rp;
+    const float* Q = p.tab.q[blockIdx.z];
+    __shared__ float As[32][64 + 4];
+    __shared__ float Bs[32][64 + 4];
+    for (int k0 = 0; k0 < r; k0 += 32) {
+      {
+        const int rr = tid >> 2, kk = (tid & 3) * 8;
+        const int64_t row = row0 + rr, col = col0 + rr;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int k = k0 + kk + i;
+          As[kk + i][rr] = (row < m && k < r) ? mt.Phat[row * rp + k] : 0.f;
+          Bs[kk + i][rr] = (col < n && k < r) ? Q[col * r + k] : 0.f;
+        }
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < 32; ++kk) {
+        float a[4], b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { a[i] = As[kk][ty * 4 + i]; b[i] = Bs[kk][tx * 4 + i]; }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
+      __syncthreads();
+    }
+  }
+  const int64_t c = col0 + tx * 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t row = row0 + ty * 4 + i;
+    if (row >= m) continue;
+    if (c + 4 <= n) {
+      *reinterpret_cast<float4*>(gh + row * n + c) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    } else {
+      for (int j = 0; j < 4 && c + j < n; ++j) gh[row * n + c + j] = acc[i][j];
+    }
+  }
+  if (skipped) return;
+  for (int w = 0; w < p.W; ++w) {
+    const TE* M = static_cast<const TE*>(mt.mscr) + (size_t)w * m * n;
+    TE* E = static_cast<TE*>(p.tab.e[(size_t)blockIdx.z * p.W + w]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t row = row0 + ty * 4 + i;
+      if (row >= m) continue;
+      if (c + 4 <= n) {
+        typename V4<TE>::T mv = *reinterpret_cast<const typename V4<TE>::T*>(M + row * n + c);
+        const TE* mx = reinterpret_cast<const TE*>(&mv);
+        TE ev[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ev[j] = add_to<TE>(to_f(mx[j]), -acc[i][j]);
+        *reinterpret_cast<typename V4<TE>::T*>(E + row * n + c) = *reinterpret_cast<const typename V4<TE>::T*>(ev);
+      } else {
+        for (int j = 0; j < 4 && c + j < n; ++j)
+          E[row * n + c + j] = add_to<TE>(to_f(M[row * n + c + j]), -acc[i][j]);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pgemm_simt(const Handle& h, const Plan& p, cudaStream_t s) {
+  dim3 grid(h.max_mtiles64, (p.r + 127) / 128, p.B * p.J);
+  if (h.edt == DT_F16) k_pgemm<__half><<<grid, kT, 0, s>>>(p);
+  else if (h.edt == DT_BF16) k_pgemm<__nv_bfloat16><<<grid, kT, 0, s>>>(p);
+  else k_pgemm<float><<<grid, kT, 0, s>>>(p);
+  h.launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qgemm_simt(const Handle& h, const Plan& p, cudaStream_t s) {
+  dim3 grid(h.max_ntiles64, h.max_S * ((p.r + 127) / 128), p.B * p.J);
+  if (h.edt == DT_F16) k_qgemm<__half><<<grid, kT, 0, s>>>(p);
+  else if (h.edt == DT_BF16) k_qgemm<__nv_bfloat16><<<grid, kT, 0, s>>>(p);
+  else k_qgemm<float><<<grid, kT, 0, s>>>(p);
+  h.launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qreduce(const Handle& h, const Plan& p, cudaStream_t s) {
+  dim3 grid(64, p.B * p.J);
+  k_qreduce<<<grid, 256, 0, s>>>(p);
+  h.launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decomp_simt(const Handle& h, const Plan& p, cudaStream_t s) {
+  dim3 grid(h.max_ntiles64, h.max_mtiles64, p.B * p.J);
+  if (h.edt == DT_F16) k_decomp<__half><<<grid, kT, 0, s>>>(p);
+  else if (h.edt == DT_BF16) k_decomp<__nv_bfloat16><<<grid, kT, 0, s>>>(p);
+  else k_decomp<float><<<grid, kT, 0, s>>>(p);
+  h.launches += 1;
+  return cudaGetLastError();
+}
+
+}  // namespace psgd

@@ -1,0 +1,161 @@
+"""Run a workload through the C ABI on the GPU and through the fp64 oracle on the same
+seeded inputs, and compare. This is test infrastructure; it is imported only by tests.
+
+Blocks listed in ``oracle_blocks`` get their inputs from ``synth`` on the host, so the
+oracle can rebuild them, and are compared. The other blocks of a large workload (the
+64-block stack) are filled on the device with torch's seeded normal generator at the
+same scale. Blocks are independent, so those values never reach a compared output.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+TOL = 1e-4  # relative Frobenius error bound on G-hat and E (fp32 GPU path vs fp64 oracle)
+
+
+def rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
+    nr = float(np.linalg.norm(ref))
+    d = float(np.linalg.norm(gpu.astype(np.float64) - ref))
+    return d / nr if nr > 0 else d
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+class GpuRun:
+    def __init__(self, wl: synth.Workload, oracle_blocks=None, flags: int = 0, device="cuda"):
+        from rank_gradient_compression_gb300.psgd import PowerSGD
+        self.wl = wl
+        self.dev = torch.device(device)
+        self.oracle_blocks = list(range(wl.blocks)) if oracle_blocks is None else list(oracle_blocks)
+        self.ps = PowerSGD(wl.shapes, wl.blocks, wl.workers, wl.rank, wl.grad_dtype,
+                           unc_len=wl.unc_len, skip_fraction=wl.skip_fraction, flags=flags,
+                           device=self.dev)
+        dt = synth.TORCH_DTYPE[wl.grad_dtype]
+        et = synth.TORCH_DTYPE[wl.err_dtype]
+        B, W = wl.blocks, wl.workers
+        self.grads = [[[torch.empty(s, dtype=dt, device=self.dev) for _ in range(W)] for s in wl.shapes]
+                      for _ in range(B)]
+        self.errs = [[[torch.zeros(s, dtype=et, device=self.dev) for _ in range(W)] for s in wl.shapes]
+                     for _ in range(B)]
+        self.q = [[synth.q0(wl, b, j).to(self.dev) for j in range(len(wl.shapes))] for b in range(B)]
+        self.ghat = [[torch.empty(s, dtype=torch.float32, device=self.dev) for s in wl.shapes]
+                     for _ in range(B)]
+        self.unc_in = self.unc_out = None
+        if wl.unc_len:
+            self.unc_in = [[torch.empty(wl.unc_len, dtype=torch.float32, device=self.dev)
+                            for _ in range(W)] for _ in range(B)]
+            self.unc_out = [torch.empty(wl.unc_len, dtype=torch.float32, device=self.dev)
+                            for _ in range(B)]
+        self.scales = [wl.scale(b) for b in range(B)]
+
+    def load_inputs(self, step: int):
+        wl = self.wl
+        gen = torch.Generator(device=self.dev)
+        for b in range(wl.blocks):
+            sampled = b in self.oracle_blocks
+            if not sampled:
+                gen.manual_seed(1_000_003 * step + b)
+            for j in range(len(wl.shapes)):
+                for w in range(wl.workers):
+                    dst = self.grads[b][j][w]
+                    if sampled:
+                        dst.copy_(synth.grad(wl, step, b, j, w))
+                    else:
+                        x = torch.randn(dst.shape, generator=gen, device=self.dev, dtype=torch.float32)
+                        log2_sig = -12 - 4 * b + (4 * b) % 24 if wl.kind == "stack" else -2
+                        dst.copy_((x * 2.0 ** log2_sig).to(dst.dtype))
+            if self.unc_in is not None:
+                for w in range(wl.workers):
+                    self.unc_in[b][w].copy_(synth.unc(wl, step, b, w))
+
+    def step(self):
+        self.ps.step(self.grads, self.errs, self.q, self.scales, self.ghat, self.unc_in, self.unc_out)
+
+
+class OracleRun:
+    def __init__(self, wl: synth.Workload, blocks, orth="householder"):
+        self.wl = wl
+        self.blocks = list(blocks)
+        self.orth = orth
+        self.state = {}
+        for b in self.blocks:
+            self.state[b] = oracle.BlockState(
+                e=[[np.zeros(s) for _ in range(wl.workers)] for s in wl.shapes],
+                q=[synth.q0(wl, b, j).double().numpy() for j in range(len(wl.shapes))])
+
+    def step(self, step: int, pool=None):
+        wl = self.wl
+
+        def one(b):
+            grads = [[synth.grad(wl, step, b, j, w).double().numpy() for w in range(wl.workers)]
+                     for j in range(len(wl.shapes))]
+            unc = None
+            if wl.unc_len:
+                unc = [synth.unc(wl, step, b, w).double().numpy() for w in range(wl.workers)]
+            return b, oracle.block_step(grads, self.state[b], wl.scale(b), wl.err_dtype,
+                                        skip_fraction=wl.skip_fraction, unc=unc, orth=self.orth)
+
+        if pool is None:
+            return dict(one(b) for b in self.blocks)
+        return dict(pool.map(one, self.blocks))
+
+
+def compare_step(g: GpuRun, o_res: dict, o: OracleRun, tol=TOL, check_m=True):
+    """Compare one step. Returns the worst relative errors (G-hat, E)."""
+    wl = g.wl
+    counts = g.ps.counts.cpu().numpy().reshape(wl.blocks, wl.workers)
+    skip = g.ps.skip.cpu().numpy()
+    worst_g = worst_e = 0.0
+    for b, res in o_res.items():
+        assert list(counts[b]) == res.counts, f"block {b}: counts {counts[b]} vs {res.counts}"
+        assert bool(skip[b]) == res.skip, f"block {b}: skip {skip[b]} vs {res.skip}"
+        for j in range(len(wl.shapes)):
+            gh = f64(g.ghat[b][j])
+            if res.skip:
+                assert np.all(gh == 0), f"block {b} matrix {j}: skipped block must give G-hat = 0"
+            else:
+                eg = rel_err(gh, res.g_hat[j])
+                worst_g = max(worst_g, eg)
+                assert eg <= tol, f"block {b} matrix {j}: G-hat rel err {eg:.3e}"
+            for w in range(wl.workers):
+                eg_w = f64(g.errs[b][j][w])
+                ee = rel_err(eg_w, o.state[b].e[j][w])
+                worst_e = max(worst_e, ee)
+                if res.skip:
+                    assert np.array_equal(eg_w, o.state[b].e[j][w]), "skipped block must keep E"
+                else:
+                    assert ee <= tol, f"block {b} matrix {j} worker {w}: E rel err {ee:.3e}"
+                if check_m:
+                    m_gpu = f64(g.ps.debug_m(b, j, w, synth.TORCH_DTYPE[wl.err_dtype]))
+                    assert np.array_equal(m_gpu, res.m[j][w]), f"block {b} matrix {j} worker {w}: M differs"
+        if wl.unc_len:
+            uo = f64(g.unc_out[b])
+            eu = rel_err(uo, res.unc_out)
+            if res.skip:
+                assert np.all(uo == 0)
+            else:
+                assert eu <= 1e-6, f"block {b}: gains/biases rel err {eu:.3e}"
+    return worst_g, worst_e
+
+
+def run_parity(wl, steps=None, oracle_blocks=None, flags=0, tol=TOL, check_m=True, threads=8):
+    steps = wl.steps if steps is None else steps
+    g = GpuRun(wl, oracle_blocks, flags)
+    o = OracleRun(wl, g.oracle_blocks)
+    worst = []
+    with cf.ThreadPoolExecutor(threads) as pool:
+        for t in range(steps):
+            g.load_inputs(t)
+            g.step()
+            torch.cuda.synchronize()
+            res = o.step(t, pool)
+            worst.append(compare_step(g, res, o, tol, check_m))
+    return g, o, worst

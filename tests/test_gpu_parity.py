@@ -1,0 +1,233 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bars: masks, nonfinite counts, skip decisions and M are bit-exact. G-hat and E are
+within 1e-4 relative Frobenius error per matrix, the fp32 GPU path against the fp64
+oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import numerics as nx
+from harness import GpuRun, OracleRun, TOL, compare_step, f64, rel_err, run_parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _psgd():
+    from rank_gradient_compression_gb300 import psgd
+    return psgd
+
+
+# ------------------------------------------------------------------ ingest brute force
+@pytest.mark.parametrize("dtype,scale", [("f16", 2.0 ** 10), ("bf16", 2.0 ** 20), ("f16", 1.0)])
+def test_ingest_every_bit_pattern(dtype, scale):
+    """Every 16-bit pattern as a gradient entry, under random finite error-buffer values.
+    M, the mask bitmap and the counts must equal the oracle's bit for bit."""
+    psgd = _psgd()
+    tdt = synth.TORCH_DTYPE[dtype]
+    rng = np.random.default_rng(11)
+    W, m, n = 2, 256, 256
+    ps = psgd.PowerSGD([(m, n)], 1, W, 1, dtype, flags=psgd.PSGD_FLAG_MASK | psgd.PSGD_FLAG_STOP_AFTER_INGEST)
+    grads, errs, gin, ein = [], [], [], []
+    for w in range(W):
+        bits = rng.permutation(1 << 16).astype(np.uint16)
+        gt = torch.from_numpy(bits.view(np.int16).reshape(m, n)).view(tdt)
+        eb = rng.integers(0, 0x7C00 if dtype == "f16" else 0x7F80, size=m * n).astype(np.uint16)
+        eb |= (rng.random(m * n) < 0.5).astype(np.uint16) << 15
+        et = torch.from_numpy(eb.view(np.int16).reshape(m, n)).view(tdt)
+        grads.append(gt.cuda()); errs.append(et.cuda())
+        gin.append(gt.to(torch.float64).numpy()); ein.append(et.to(torch.float64).numpy())
+    q = [[torch.zeros((n, 1), device="cuda")]]
+    gh = [[torch.zeros((m, n), device="cuda")]]
+    ps.step([[grads]], [[errs]], q, [scale], gh)
+    torch.cuda.synchronize()
+    counts = ps.counts.cpu().numpy()
+    masks = ps.mask.cpu().numpy().view(np.uint8)
+    for w in range(W):
+        g, mask = oracle.unscale_and_mask(gin[w], scale)
+        want_m = oracle.accumulate_error(g, ein[w], dtype)
+        got_m = f64(ps.debug_m(0, 0, w, tdt))
+        same = (got_m == want_m) | (np.isnan(got_m) & np.isnan(want_m))
+        assert same.all(), f"worker {w}: {int((~same).sum())} M entries differ"
+        assert counts[w] == int(mask.sum())
+        off = psgd.psgd_mask_offset(ps.cfg, 0, 0, w) * 4
+        want_bits = np.packbits(mask.reshape(-1), bitorder="little")
+        assert np.array_equal(masks[off:off + want_bits.size], want_bits)
+    assert counts.sum() == 2 * 2048
+
+
+def test_ingest_fp32_specials():
+    psgd = _psgd()
+    rng = np.random.default_rng(12)
+    m, n = 64, 128
+    bits = rng.integers(0, 2 ** 32, size=m * n, dtype=np.uint64).astype(np.uint32)
+    bits[:64] = [0x7F800000, 0xFF800000, 0x7FC00000, 0x00000001, 0x80000001, 0x7F7FFFFF] * 10 + [0, 0x80000000, 1, 2]
+    g = torch.from_numpy(bits.view(np.float32).reshape(m, n).copy())
+    e = torch.from_numpy((rng.standard_normal((m, n)) * 1e-3).astype(np.float32))
+    ps = psgd.PowerSGD([(m, n)], 1, 1, 1, "f32", flags=psgd.PSGD_FLAG_MASK | psgd.PSGD_FLAG_STOP_AFTER_INGEST)
+    ps.step([[[g.cuda()]]], [[[e.cuda()]]], [[torch.zeros((n, 1), device="cuda")]], [4.0],
+            [[torch.zeros((m, n), device="cuda")]])
+    torch.cuda.synchronize()
+    gg, mask = oracle.unscale_and_mask(g.double().numpy(), 4.0)
+    want = oracle.accumulate_error(gg, e.double().numpy(), "f32")
+    got = f64(ps.debug_m(0, 0, 0, torch.float32))
+    assert np.array_equal(got, want)
+    assert int(ps.counts.cpu()[0]) == int(mask.sum())
+
+
+# ------------------------------------------------------------------ whole-step parity
+def test_fp32_small_one_step():
+    """Small fp32 case: a 256x512 matrix, N(0, 1e-3), r = 4, W = 2, one step."""
+    _, _, worst = run_parity(synth.fp32_small())
+    assert worst[0][0] <= TOL
+
+
+def test_planted_rank3_reconstructs():
+    """The planted U V^T of rank 3 at r = 4: G-hat = M within 1e-5 on the GPU, and the
+    mean error buffer is ~0."""
+    wl = synth.planted_rank3()
+    g, o, _ = run_parity(wl)
+    m = synth.grad(wl, 0, 0, 0, 0).double().numpy()
+    assert rel_err(f64(g.ghat[0][0]), m) <= 1e-5
+    e = sum(f64(g.errs[0][0][w]) for w in range(wl.workers)) / wl.workers
+    assert np.linalg.norm(e) <= 1e-5 * np.linalg.norm(m)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("shapes,W,r", [
+    (((200, 136), (64, 40)), 3, 4),
+    (((333, 264),), 2, 16),
+    (((130, 72), (257, 520)), 1, 1),
+    (((256, 512), (384, 128)), 8, 32),
+])
+def test_small_ragged_multi_step(dtype, shapes, W, r):
+    """Ragged shapes (not multiples of any tile), three steps with fresh gradients."""
+    wl = synth.with_shapes(synth.resblock_shard(steps=3, workers=W, rank=r, dtype=dtype), shapes)
+    run_parity(wl)
+
+
+def test_simt_engine_matches_default_engine():
+    """The FFMA debug engine and the default engine agree to the same oracle."""
+    psgd = _psgd()
+    wl = synth.with_shapes(synth.resblock_shard(steps=2, workers=2, rank=8), ((256, 192),))
+    run_parity(wl, flags=psgd.PSGD_FLAG_SIMT)
+
+
+def test_resblock_shard_full_size_ten_steps():
+    """One d_model = 3968 resblock shard: fp16, W = 8, r = 112, ten steps. This is the
+    workload that bench.py times, at full size."""
+    _, _, worst = run_parity(synth.resblock_shard(steps=10))
+    print("worst (G-hat, E) per step:", worst)
+
+
+def test_stress_nonfinite_and_skip():
+    """Log-uniform magnitudes across the fp16 subnormal range, 0.1% of entries +-Inf/NaN,
+    block 1 fully nonfinite at step 1: bit-exact masks/counts/skips, and block 1 keeps
+    E and Q bit-for-bit through the faulted step."""
+    wl = synth.stress()
+    g = GpuRun(wl)
+    o = OracleRun(wl, range(wl.blocks))
+    for t in range(wl.steps):
+        g.load_inputs(t)
+        e_before = [[g.errs[1][j][w].clone() for w in range(wl.workers)] for j in range(4)]
+        q_before = [g.q[1][j].clone() for j in range(4)]
+        g.step()
+        torch.cuda.synchronize()
+        res = o.step(t)
+        compare_step(g, res, o)
+        skip = g.ps.skip.cpu().numpy()
+        assert bool(skip[1]) == (t == 1) and not skip[0]
+        if t == 1:
+            for j in range(4):
+                assert torch.equal(g.q[1][j], q_before[j])
+                for w in range(wl.workers):
+                    assert torch.equal(g.errs[1][j][w], e_before[j][w])
+
+
+def test_stack64_sampled_blocks():
+    """64 resblock shards (bf16, W = 4, r = 112, per-block scales 2^(4b mod 24), fp32
+    gains/biases) in one call. The oracle checks sampled blocks, among them blocks whose
+    gradients are subnormal or all zero."""
+    wl = synth.stack64()
+    run_parity(wl, oracle_blocks=[0, 5, 6, 17, 30, 35, 36, 63])
+
+
+@pytest.mark.parametrize("rank", [16, 112])
+def test_spectrum_rank_sweep(rank):
+    """3968x15872 fp16 gradient with singular values c/k, W = 8 identical copies."""
+    run_parity(synth.spectrum(rank=rank, steps=2))
+
+
+# ------------------------------------------------------------------ properties
+def test_orthonormal_basis_and_ef_identity():
+    wl = synth.with_shapes(synth.resblock_shard(steps=1, workers=3, rank=24), ((700, 312), (1024, 96)))
+    g, o, _ = run_parity(wl)
+    for j, (m, n) in enumerate(wl.shapes):
+        ph = f64(g.ps.debug_phat(0, j))
+        live = np.linalg.norm(ph, axis=0) > 0.5
+        gram = ph[:, live].T @ ph[:, live]
+        assert np.abs(gram - np.eye(int(live.sum()))).max() <= 1e-5
+        # M_w = G-hat + E_w up to the rounding of E (half an ulp of E's type, RNE)
+        gh = f64(g.ghat[0][j])
+        for w in range(wl.workers):
+            mm = f64(g.ps.debug_m(0, j, w, torch.float16))
+            ee = f64(g.errs[0][j][w])
+            assert np.array_equal(ee, nx.round_to_format(ee, "f16"))
+            assert np.abs(mm - gh - ee).max() <= 2.0 ** -11 * np.abs(mm - gh).max() + 1e-12
+
+
+def test_deterministic_and_resumable():
+    """Two runs give bit-identical outputs. Four straight steps equal two steps, a
+    save/restore of the caller-owned state (E, Q) into fresh buffers and a fresh
+    handle, and two more steps."""
+    wl = synth.with_shapes(synth.resblock_shard(steps=4, workers=2, rank=8), ((256, 128),))
+    a = GpuRun(wl)
+    for t in range(4):
+        a.load_inputs(t); a.step()
+    b = GpuRun(wl)
+    for t in range(2):
+        b.load_inputs(t); b.step()
+    torch.cuda.synchronize()
+    saved_e = [x.cpu().clone() for x in b.errs[0][0]]
+    saved_q = b.q[0][0].cpu().clone()
+    del b
+    c = GpuRun(wl)
+    for w in range(wl.workers):
+        c.errs[0][0][w].copy_(saved_e[w])
+    c.q[0][0].copy_(saved_q)
+    for t in range(2, 4):
+        c.load_inputs(t); c.step()
+    torch.cuda.synchronize()
+    assert torch.equal(a.ghat[0][0], c.ghat[0][0])
+    assert torch.equal(a.q[0][0], c.q[0][0])
+    for w in range(wl.workers):
+        assert torch.equal(a.errs[0][0][w], c.errs[0][0][w])
+
+
+# ------------------------------------------------------------------ argument errors
+def test_argument_errors_return_status():
+    psgd = _psgd()
+    ps = psgd.PowerSGD([(64, 32)], 1, 1, 2, "f16")
+    g = torch.zeros((64, 32), dtype=torch.float16, device="cuda")
+    e = torch.zeros_like(g)
+    q = torch.zeros((32, 2), device="cuda")
+    gh = torch.zeros((64, 32), device="cuda")
+    with pytest.raises(psgd.PSGDError) as ex:
+        ps.step([[[g]]], [[[e]]], [[q]], [0.5], [[gh]])
+    assert ex.value.status == psgd.PSGD_EINVAL
+    with pytest.raises(psgd.PSGDError) as ex:
+        ps.step([[[g]]], [[[e]]], [[q]], [float("inf")], [[gh]])
+    assert ex.value.status == psgd.PSGD_EINVAL
+    big = torch.zeros(64 * 32 + 8, dtype=torch.float16, device="cuda")
+    mis = big[1:1 + 64 * 32].view(64, 32)  # 2-byte offset: not 16-byte aligned
+    with pytest.raises(psgd.PSGDError) as ex:
+        ps.step([[[mis]]], [[[e]]], [[q]], [1.0], [[gh]])
+    assert ex.value.status == psgd.PSGD_EINVAL
+    ps.step([[[g]]], [[[e]]], [[q]], [1.0], [[gh]])
+    ps.check()
+    with pytest.raises(psgd.PSGDError) as ex:
+        psgd.PowerSGD([(64, 32)], 1, 1, 40, "f16")
+    assert ex.value.status == psgd.PSGD_EINVAL
