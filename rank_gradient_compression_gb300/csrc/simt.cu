@@ -169,20 +169,26 @@ __global__ void __launch_bounds__(kT) k_qgemm(Plan p) {
   }
 }
 
-// Q = (sum_s Qpart[s]) / W in slice order -> the caller's fp32 Q state (n x r).
-__global__ void k_qreduce(Plan p) {
+// Q = (sum_s Qpart[s]) * qscale / W in slice order -> the caller's fp32 Q state (n x r),
+// and max|Q| -> scal[3]. qscale undoes the power-of-two scale of a split P^ (exact).
+__global__ void k_qreduce(Plan p, float qscale) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
   const int64_t total = mt.n * p.r;
   const float fw = (float)p.W;
   float* q = p.tab.q[blockIdx.y];
+  unsigned vmax = 0u;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = i / p.r, c = i % p.r;
     float acc = 0.f;
     for (int s = 0; s < mt.S; ++s) acc = __fadd_rn(acc, mt.Qpart[((size_t)s * mt.n + row) * p.rp + c]);
-    q[i] = __fdiv_rn(acc, fw);
+    const float v = __fdiv_rn(acc * qscale, fw);
+    q[i] = v;
+    vmax = max(vmax, __float_as_uint(fabsf(v)));
   }
+  vmax = __reduce_max_sync(0xffffffffu, vmax);
+  if ((threadIdx.x & 31) == 0 && vmax) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 3, vmax);
 }
 
 template <typename TE> struct V4;
@@ -292,7 +298,7 @@ cudaError_t launch_qgemm_simt(const Handle& h, const Plan& p, cudaStream_t s) {
 
 cudaError_t launch_qreduce(const Handle& h, const Plan& p, cudaStream_t s) {
   dim3 grid(64, p.B * p.J);
-  k_qreduce<<<grid, 256, 0, s>>>(p);
+  k_qreduce<<<grid, 256, 0, s>>>(p, h.tc ? 0x1p-14f : 1.0f);
   h.launches += 1;
   return cudaGetLastError();
 }

@@ -17,6 +17,10 @@ import oracle
 import synth
 
 TOL = 1e-4  # relative Frobenius error bound on G-hat and E (fp32 GPU path vs fp64 oracle)
+# When the oracle's E is below 2^-20 ||M|| (a planted matrix the step reconstructs), a
+# relative bound on E is meaningless: fp32 arithmetic alone leaves O(2^-24 ||M||) there.
+# E is then bounded absolutely, ||E_gpu - E_oracle|| <= 2^-18 ||M||.
+E_FLOOR, E_ABS = 2.0 ** -20, 2.0 ** -18
 
 
 def rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
@@ -109,7 +113,11 @@ class OracleRun:
 
 
 def compare_step(g: GpuRun, o_res: dict, o: OracleRun, tol=TOL, check_m=True):
-    """Compare one step. Returns the worst relative errors (G-hat, E)."""
+    """Compare one step. Returns the worst relative errors (G-hat, E).
+
+    M = round_E(g + E) is compared bit for bit only when both sides start the step from
+    the same E, i.e. at the first step (E = 0). Later, each side's E carries its own
+    one-ulp rounding differences, and only E's Frobenius error is bounded."""
     wl = g.wl
     counts = g.ps.counts.cpu().numpy().reshape(wl.blocks, wl.workers)
     skip = g.ps.skip.cpu().numpy()
@@ -127,10 +135,16 @@ def compare_step(g: GpuRun, o_res: dict, o: OracleRun, tol=TOL, check_m=True):
                 assert eg <= tol, f"block {b} matrix {j}: G-hat rel err {eg:.3e}"
             for w in range(wl.workers):
                 eg_w = f64(g.errs[b][j][w])
-                ee = rel_err(eg_w, o.state[b].e[j][w])
+                e_ref = o.state[b].e[j][w]
+                m_norm = float(np.linalg.norm(res.m[j][w]))
+                if not res.skip and float(np.linalg.norm(e_ref)) < E_FLOOR * m_norm:
+                    ea = float(np.linalg.norm(eg_w - e_ref))
+                    assert ea <= E_ABS * m_norm, f"block {b} matrix {j} worker {w}: |dE| {ea:.3e} vs |M| {m_norm:.3e}"
+                    continue
+                ee = rel_err(eg_w, e_ref)
                 worst_e = max(worst_e, ee)
                 if res.skip:
-                    assert np.array_equal(eg_w, o.state[b].e[j][w]), "skipped block must keep E"
+                    assert np.array_equal(eg_w, e_ref), "skipped block must keep E"
                 else:
                     assert ee <= tol, f"block {b} matrix {j} worker {w}: E rel err {ee:.3e}"
                 if check_m:
@@ -157,5 +171,5 @@ def run_parity(wl, steps=None, oracle_blocks=None, flags=0, tol=TOL, check_m=Tru
             g.step()
             torch.cuda.synchronize()
             res = o.step(t, pool)
-            worst.append(compare_step(g, res, o, tol, check_m))
+            worst.append(compare_step(g, res, o, tol, check_m and t == 0))
     return g, o, worst

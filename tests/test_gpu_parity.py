@@ -56,7 +56,7 @@ def test_ingest_every_bit_pattern(dtype, scale):
         off = psgd.psgd_mask_offset(ps.cfg, 0, 0, w) * 4
         want_bits = np.packbits(mask.reshape(-1), bitorder="little")
         assert np.array_equal(masks[off:off + want_bits.size], want_bits)
-    assert counts.sum() == 2 * 2048
+    assert counts.sum() == 2 * (2048 if dtype == "f16" else 256)  # all-ones exponent patterns
 
 
 def test_ingest_fp32_specials():
@@ -137,7 +137,7 @@ def test_stress_nonfinite_and_skip():
         g.step()
         torch.cuda.synchronize()
         res = o.step(t)
-        compare_step(g, res, o)
+        compare_step(g, res, o, check_m=(t == 0))
         skip = g.ps.skip.cpu().numpy()
         assert bool(skip[1]) == (t == 1) and not skip[0]
         if t == 1:
