@@ -165,6 +165,7 @@ def run_reference(args):
 def run_ours(args):
     import torch
     import torch.distributed as dist
+    from rank_gradient_compression_gb300 import dist as pdist
     from rank_gradient_compression_gb300 import psgd
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -179,6 +180,8 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
+    # one resblock shard per rank: the blocks of the N-rank job are independent
+    assert pdist.shard_blocks(world, rank, world) == [rank]
     g = torch.Generator(device=dev)
     g.manual_seed(1234 + rank)
     sets = []
@@ -213,11 +216,7 @@ def run_ours(args):
     clk = clocks.stop()
     launches = psgd.psgd_launch_count(ps.handle) - launches0
     phase_ms, nprof = psgd.psgd_profile_end(ps.handle)
-    ms = start.elapsed_time(end) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = pdist.max_over_ranks(start.elapsed_time(end) / args.steps, device=dev)
 
     # ---------------- end to end: pinned host gradients in, G-hat out, every step
     e2e_steps = args.e2e_steps or max(3, args.steps // 10)
@@ -244,11 +243,7 @@ def run_ours(args):
             host_gh[0][j].copy_(ghat[0][j], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = pdist.max_over_ranks(e0.elapsed_time(e1) / e2e_steps, device=dev)
     barrier()
 
     grad_bytes = W * numel_per_worker() * 2  # per rank per step

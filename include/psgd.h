@@ -153,6 +153,12 @@ const void* psgd_debug_m(psgd_handle* h, int32_t b, int32_t j, int32_t w);
 /* Debug: device pointer to P^_{b,j} of the last step, fp32 m x rp row-major with
  * rp = r rounded up to a multiple of 16 (columns r..rp-1 are 0), or NULL. */
 const float* psgd_debug_phat(psgd_handle* h, int32_t b, int32_t j);
+/* Debug: after waiting for `stream`, copy the orthonormalisation pass record of matrix
+ * (b, j) from the last step into out[PSGD_MAX_ORTH_PASSES * 4]: per pass {final flag,
+ * output buffer, shifted flag, dead columns}. Passes after the final one hold stale
+ * values. Returns the number of passes that ran (>= 1), or -1 on error. */
+#define PSGD_MAX_ORTH_PASSES 4
+int32_t psgd_debug_orth(psgd_handle* h, int32_t b, int32_t j, int32_t* out, void* stream);
 /* Name of the GEMM engine this handle uses: "tcgen05" or "simt". */
 const char* psgd_engine(psgd_handle* h);
 

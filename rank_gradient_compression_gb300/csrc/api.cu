@@ -98,7 +98,7 @@ Layout plan_layout(const psgd_config* c) {
     L.Phat.push_back(take(4 * (size_t)mpad * rp));
     L.ostate.push_back(take(4 * 4 * kMaxPasses));
     L.Qpart.push_back(take(4 * (size_t)S * s.n * rp));
-    L.Gpart.push_back(take(4 * (size_t)C * rp * rp));
+    L.Gpart.push_back(take(4 * (size_t)(C + 1) * rp * rp));  // C partials + their sum
     L.Rinv.push_back(take(4 * (size_t)rp * rp));
   }
   L.tc = take(tc_workspace_bytes(c));
@@ -241,6 +241,7 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
       h.segs.push_back(sg);
       cta += ceil_div(sg.numel, kIngestChunk);
     }
+  h.unc_cta_start = cta;
   if (cfg->unc_len > 0)
     for (int b = 0; b < h.B; ++b)
       for (int w = 0; w < h.W; ++w) {
@@ -369,7 +370,16 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   mark();
   if ((e = cudaMemsetAsync(a->counts, 0, 8 * B * W, s)) != cudaSuccess) return cuda_fail(e, "counts");
   if ((e = cudaMemsetAsync(h.d_scal_all, 0, 16 * B * J, s)) != cudaSuccess) return cuda_fail(e, "scal");
-  if ((e = launch_ingest(h, p, s)) != cudaSuccess) return cuda_fail(e, "ingest");
+  // The fused path ingests the gradients and forms the P partial sums in one sweep; the
+  // debug outputs (mask bitmap, stop after ingest) use the separate ingest kernel.
+  const bool fused = h.tc && !(h.cfg.flags & (PSGD_FLAG_MASK | PSGD_FLAG_STOP_AFTER_INGEST));
+  if (fused) {
+    if ((e = launch_prep_q(h, p, s)) != cudaSuccess) return cuda_fail(e, "prep_q");
+    if ((e = launch_ingest_p(h, p, s)) != cudaSuccess) return cuda_fail(e, "ingest_p");
+    if ((e = launch_unc_count(h, p, s)) != cudaSuccess) return cuda_fail(e, "unc_count");
+  } else if ((e = launch_ingest(h, p, s)) != cudaSuccess) {
+    return cuda_fail(e, "ingest");
+  }
   mark();
   if ((e = launch_skip_and_unc(h, p, s)) != cudaSuccess) return cuda_fail(e, "skip");
   mark();
@@ -377,11 +387,14 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
     while (ev && phase <= PSGD_NUM_PHASES) mark();
     return PSGD_OK;
   }
-  if (h.tc) {
+  if (fused) {
+    if ((e = launch_preduce(h, p, s)) != cudaSuccess) return cuda_fail(e, "preduce");
+  } else if (h.tc) {
     if ((e = launch_prep_q(h, p, s)) != cudaSuccess) return cuda_fail(e, "prep_q");
     if ((e = launch_pgemm_tc(h, p, s)) != cudaSuccess) return cuda_fail(e, "pgemm_tc");
-  } else if ((e = launch_pgemm_simt(h, p, s)) != cudaSuccess) {
-    return cuda_fail(e, "pgemm");
+  } else {
+    if ((e = launch_qmax(h, p, s)) != cudaSuccess) return cuda_fail(e, "qmax");
+    if ((e = launch_pgemm_simt(h, p, s)) != cudaSuccess) return cuda_fail(e, "pgemm");
   }
   mark();
   if ((e = launch_orth(h, p, s)) != cudaSuccess) return cuda_fail(e, "orth");
@@ -486,6 +499,20 @@ const float* psgd_debug_phat(psgd_handle* ph, int32_t b, int32_t j) {
   Handle& h = ph->h;
   if (b < 0 || b >= h.B || j < 0 || j >= h.J) return nullptr;
   return h.meta[(size_t)b * h.J + j].Phat;
+}
+
+int32_t psgd_debug_orth(psgd_handle* ph, int32_t b, int32_t j, int32_t* out, void* stream) {
+  static_assert(PSGD_MAX_ORTH_PASSES == kMaxPasses, "pass record size");
+  if (!ph || !out) return -1;
+  Handle& h = ph->h;
+  if (b < 0 || b >= h.B || j < 0 || j >= h.J) return -1;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
+  if (cudaMemcpy(out, h.meta[(size_t)b * h.J + j].ostate, sizeof(int32_t) * 4 * kMaxPasses,
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return -1;
+  for (int p = 0; p < kMaxPasses; ++p)
+    if (out[4 * p] != 0) return p + 1;
+  return kMaxPasses;
 }
 
 const char* psgd_engine(psgd_handle* ph) {

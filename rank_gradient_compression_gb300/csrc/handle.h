@@ -39,6 +39,7 @@ struct Handle {
   std::vector<IngestSeg> segs;
   IngestSeg* d_segs = nullptr;
   int64_t ingest_ctas = 0;
+  int64_t unc_cta_start = 0;  // first CTA of the gains/biases segments
 
   // per-step pointer table
   char* d_table = nullptr;
@@ -64,7 +65,10 @@ size_t tc_workspace_bytes(const psgd_config* cfg);
 bool tc_supported(const psgd_config* cfg, std::string* why);
 cudaError_t tc_plan(Handle& h, char* ws_tc, cudaStream_t s);
 cudaError_t launch_prep_q(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_qmax(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_ingest_p(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_preduce(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_decomp_tc(const Handle& h, const Plan& p, cudaStream_t s);
 void tc_free(Handle& h);

@@ -90,11 +90,12 @@ __device__ __forceinline__ int find_seg(const IngestSeg* segs, int nseg, int64_t
 // count of (b, w), optional mask bits, and max|M| of the matrix. Vectors: the count only.
 template <typename TG, typename TE>
 __global__ void __launch_bounds__(kIngestThreads)
-k_ingest(Plan p, const IngestSeg* __restrict__ segs, int nseg) {
+k_ingest(Plan p, const IngestSeg* __restrict__ segs, int nseg, int64_t cta_offset) {
   __shared__ int sh_i[kIngestThreads / 32];
   __shared__ unsigned sh_u[kIngestThreads / 32];
-  const IngestSeg sg = segs[find_seg(segs, nseg, (int64_t)blockIdx.x)];
-  const int64_t base = ((int64_t)blockIdx.x - sg.cta_start) * kIngestChunk;
+  const int64_t cta = (int64_t)blockIdx.x + cta_offset;
+  const IngestSeg sg = segs[find_seg(segs, nseg, cta)];
+  const int64_t base = (cta - sg.cta_start) * kIngestChunk;
   const float inv_s = p.tab.inv_scale[sg.b];
   const int tid = threadIdx.x;
   int cnt = 0;
@@ -203,14 +204,25 @@ __global__ void k_unc_out(Plan p) {
 
 }  // namespace
 
-cudaError_t launch_ingest(const Handle& h, const Plan& p, cudaStream_t s) {
+cudaError_t launch_ingest_range(const Handle& h, const Plan& p, cudaStream_t s, int64_t first, int64_t count) {
+  if (count <= 0) return cudaSuccess;
   const int nseg = (int)h.segs.size();
-  dim3 grid((unsigned)h.ingest_ctas);
-  if (h.gdt == DT_F16) k_ingest<__half, __half><<<grid, kIngestThreads, 0, s>>>(p, h.d_segs, nseg);
-  else if (h.gdt == DT_BF16) k_ingest<__nv_bfloat16, __nv_bfloat16><<<grid, kIngestThreads, 0, s>>>(p, h.d_segs, nseg);
-  else k_ingest<float, float><<<grid, kIngestThreads, 0, s>>>(p, h.d_segs, nseg);
+  dim3 grid((unsigned)count);
+  if (h.gdt == DT_F16) k_ingest<__half, __half><<<grid, kIngestThreads, 0, s>>>(p, h.d_segs, nseg, first);
+  else if (h.gdt == DT_BF16) k_ingest<__nv_bfloat16, __nv_bfloat16><<<grid, kIngestThreads, 0, s>>>(p, h.d_segs, nseg, first);
+  else k_ingest<float, float><<<grid, kIngestThreads, 0, s>>>(p, h.d_segs, nseg, first);
   h.launches += 1;
   return cudaGetLastError();
+}
+
+cudaError_t launch_ingest(const Handle& h, const Plan& p, cudaStream_t s) {
+  return launch_ingest_range(h, p, s, 0, h.ingest_ctas);
+}
+
+// Gains/biases only: their nonfinite counts, for the skip decision (matrices are
+// ingested by the fused tensor-core kernel).
+cudaError_t launch_unc_count(const Handle& h, const Plan& p, cudaStream_t s) {
+  return launch_ingest_range(h, p, s, h.unc_cta_start, h.ingest_ctas - h.unc_cta_start);
 }
 
 cudaError_t launch_skip_and_unc(const Handle& h, const Plan& p, cudaStream_t s) {

@@ -93,16 +93,33 @@ __global__ void __launch_bounds__(kT) k_gram(Plan p, int pass) {
   }
 }
 
-// Load G = sum_c Gpart[c] (fixed order) into shared memory, plus its diagonal.
+// G = sum_c Gpart[c] in chunk order, one element per thread, into slot C of Gpart.
+// grid = (ceil(rp*rp/256), B*J).
+__global__ void __launch_bounds__(kT) k_gsum(Plan p, int pass) {
+  const MatMeta& mt = p.meta[blockIdx.y];
+  if (pass_skipped(p, mt, pass)) return;
+  const int rp = p.rp;
+  const int idx = blockIdx.x * kT + threadIdx.x;
+  if (idx >= rp * rp) return;
+  const float* src = mt.Gpart + idx;
+  float s = 0.f;
+#pragma unroll 8
+  for (int c = 0; c < mt.C; ++c) s = __fadd_rn(s, __ldg(src + (size_t)c * rp * rp));
+  mt.Gpart[(size_t)mt.C * rp * rp + idx] = s;
+}
+
+// Load the summed Gram matrix (slot C of Gpart) into shared memory, plus its diagonal.
+// Threads work on a 16 x 16 grid of (row, column) strides: no integer division.
 __device__ void load_gram(const MatMeta& mt, int r, int rp, float* G, int ldg, float* diag0,
                           float shift) {
-  for (int idx = threadIdx.x; idx < r * r; idx += blockDim.x) {
-    const int i = idx / r, j = idx % r;
-    float s = 0.f;
-    for (int c = 0; c < mt.C; ++c) s = __fadd_rn(s, mt.Gpart[(size_t)c * rp * rp + i * rp + j]);
-    if (i == j) { diag0[i] = s; s += shift; }
-    G[i * ldg + j] = s;
-  }
+  const float* src = mt.Gpart + (size_t)mt.C * rp * rp;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  for (int i = ty; i < r; i += 16)
+    for (int j = tx; j < r; j += 16) {
+      float s = src[i * rp + j];
+      if (i == j) { diag0[i] = s; s += shift; }
+      G[i * ldg + j] = s;
+    }
   __syncthreads();
 }
 
@@ -112,8 +129,9 @@ __device__ void load_gram(const MatMeta& mt, int r, int rp, float* G, int ldg, f
 // pivot_k / diag0_k goes into ratio[k] (0 for dead columns).
 __device__ void cholesky_smem(float* G, int ldg, int r, const float* diag0, float dead_tol,
                               float* ratio, int* dead) {
-  __shared__ float s_rkk;
+  __shared__ float s_inv;
   __shared__ int s_dead;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
   for (int k = 0; k < r; ++k) {
     if (threadIdx.x == 0) {
       const float d = G[k * ldg + k];
@@ -121,20 +139,21 @@ __device__ void cholesky_smem(float* G, int ldg, int r, const float* diag0, floa
       s_dead = bad;
       dead[k] = bad;
       ratio[k] = bad ? 0.f : d / diag0[k];
-      s_rkk = bad ? 1.f : sqrtf(d);
-      G[k * ldg + k] = s_rkk;
+      const float rkk = bad ? 1.f : sqrtf(d);
+      G[k * ldg + k] = rkk;
+      s_inv = 1.f / rkk;
     }
     __syncthreads();
     const bool isdead = s_dead != 0;
-    const float rkk = s_rkk;
+    const float inv = s_inv;
     for (int j = k + 1 + threadIdx.x; j < r; j += blockDim.x)
-      G[k * ldg + j] = isdead ? 0.f : G[k * ldg + j] / rkk;
+      G[k * ldg + j] = isdead ? 0.f : G[k * ldg + j] * inv;
     __syncthreads();
     if (!isdead) {
-      const int rem = r - k - 1;
-      for (int idx = threadIdx.x; idx < rem * rem; idx += blockDim.x) {
-        const int i = k + 1 + idx / rem, j = k + 1 + idx % rem;
-        if (j >= i) G[i * ldg + j] = fmaf(-G[k * ldg + i], G[k * ldg + j], G[i * ldg + j]);
+      for (int i = k + 1 + ty; i < r; i += 16) {
+        const float gki = G[k * ldg + i];
+        for (int j = k + 1 + tx; j < r; j += 16)
+          if (j >= i) G[i * ldg + j] = fmaf(-gki, G[k * ldg + j], G[i * ldg + j]);
       }
     }
     __syncthreads();
@@ -150,7 +169,7 @@ __global__ void __launch_bounds__(kT) k_chol(Plan p, int pass) {
   float* G = sm;                          // [kMaxRank][kMaxRank + 1]
   float* diag0 = G + kMaxRank * ldg;      // [kMaxRank]
   float* ratio = diag0 + kMaxRank;        // [kMaxRank]
-  int* dead = reinterpret_cast<int*>(ratio + kMaxRank);
+  int* dead = reinterpret_cast<int*>(ratio + kMaxRank);  // [kMaxRank]; R^-1 work after it
   __shared__ float s_trace, s_maxr, s_minr, s_minratio;
   __shared__ int s_ndead, s_retry;
   const bool last = pass == kMaxPasses - 1;
@@ -166,10 +185,11 @@ __global__ void __launch_bounds__(kT) k_chol(Plan p, int pass) {
   __syncthreads();
   const float trace = s_trace;
   bool shifted = false;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
   if (!(trace > 0.f) || !isfinite(trace)) {
     for (int k = threadIdx.x; k < r; k += blockDim.x) dead[k] = 1;
-    for (int idx = threadIdx.x; idx < r * r; idx += blockDim.x)
-      G[(idx / r) * ldg + idx % r] = (idx / r == idx % r) ? 1.f : 0.f;
+    for (int i = ty; i < r; i += 16)
+      for (int j = tx; j < r; j += 16) G[i * ldg + j] = (i == j) ? 1.f : 0.f;
     __syncthreads();
   } else {
     cholesky_smem(G, ldg, r, diag0, last ? 0x1p-40f : 0x1p-16f, ratio, dead);
@@ -198,19 +218,26 @@ __global__ void __launch_bounds__(kT) k_chol(Plan p, int pass) {
     s_maxr = mx; s_minr = mn; s_minratio = mr; s_ndead = nd;
   }
   __syncthreads();
-  // R^-1 (upper triangular), one column per thread; dead columns zeroed.
-  float* Ri = mt.Rinv;
-  for (int j = threadIdx.x; j < r; j += blockDim.x) {
-    // solve R x = e_j for rows j..0 (x_i = 0 for i > j)
-    for (int i = r - 1; i > j; --i) Ri[i * rp + j] = 0.f;
-    for (int i = j; i >= 0; --i) {
-      float s = (i == j) ? 1.f : 0.f;
-      for (int k = i + 1; k <= j; ++k) s = fmaf(-G[i * ldg + k], Ri[k * rp + j], s);
-      Ri[i * rp + j] = s / G[i * ldg + i];
+  // R^-1 (upper triangular) by right-looking elimination in shared memory: X = I, then
+  // for l = r-1 .. 0: X[l,:] /= R[l,l]; X[k,:] -= R[k,l] X[l,:] for k < l. When row l is
+  // finalised, every row below it has already contributed, so X[l,:] is row l of R^-1.
+  float* X = ratio + kMaxRank + kMaxRank;  // [kMaxRank][ldg], after dead[]
+  for (int i = ty; i < r; i += 16)
+    for (int j = tx; j < r; j += 16) X[i * ldg + j] = (i == j) ? 1.f : 0.f;
+  __syncthreads();
+  for (int l = r - 1; l >= 0; --l) {
+    const float inv = 1.f / G[l * ldg + l];
+    for (int j = l + threadIdx.x; j < r; j += blockDim.x) X[l * ldg + j] *= inv;
+    __syncthreads();
+    for (int k = ty; k < l; k += 16) {
+      const float gkl = G[k * ldg + l];
+      for (int j = l + tx; j < r; j += 16) X[k * ldg + j] = fmaf(-gkl, X[l * ldg + j], X[k * ldg + j]);
     }
-    if (dead[j])
-      for (int i = 0; i <= j; ++i) Ri[i * rp + j] = 0.f;
+    __syncthreads();
   }
+  float* Ri = mt.Rinv;
+  for (int i = ty; i < r; i += 16)
+    for (int j = tx; j < r; j += 16) Ri[i * rp + j] = (j >= i && !dead[j]) ? X[i * ldg + j] : 0.f;
   if (threadIdx.x == 0) {
     const bool nearly_orth = !shifted && s_ndead == 0 && s_minratio >= 0.5f &&
                              s_maxr <= 2.f * s_minr;
@@ -288,7 +315,7 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   }
 }
 
-constexpr size_t kCholSmem = (size_t)kMaxRank * (kMaxRank + 1) * 4 + 3 * kMaxRank * 4;
+constexpr size_t kCholSmem = 2 * (size_t)kMaxRank * (kMaxRank + 1) * 4 + 3 * kMaxRank * 4;
 
 }  // namespace
 
@@ -297,9 +324,10 @@ cudaError_t launch_orth(const Handle& h, const Plan& p, cudaStream_t s) {
   const int BJ = p.B * p.J;
   for (int pass = 0; pass < kMaxPasses; ++pass) {
     k_gram<<<dim3(h.max_C, BJ), kT, 0, s>>>(p, pass);
+    k_gsum<<<dim3((p.rp * p.rp + kT - 1) / kT, BJ), kT, 0, s>>>(p, pass);
     k_chol<<<BJ, kT, kCholSmem, s>>>(p, pass);
     k_apply<<<dim3(h.max_mtiles64, BJ), kT, 0, s>>>(p, pass);
-    h.launches += 3;
+    h.launches += 4;
   }
   return cudaGetLastError();
 }

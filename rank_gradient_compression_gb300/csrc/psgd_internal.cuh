@@ -31,7 +31,7 @@ struct MatMeta {
   int* ostate;        // [kMaxPasses][4]: final, dst buffer, shifted, dead columns
   float* Ppart;       // kchunks x mpad x rp fp32: P GEMM partial sums (tensor path)
   float* Qpart;       // S x n x rp fp32: Q GEMM partial sums
-  float* Gpart;       // C x rp x rp fp32: Gram partial sums
+  float* Gpart;       // (C + 1) x rp x rp fp32: Gram partial sums, then their sum
   float* Rinv;        // rp x rp fp32: inverse Cholesky factor of the current pass
   uint16_t* qsplit;   // [2*rp][n] 16-bit: Q (scaled) hi rows then lo rows, K-major B
   uint16_t* psplit;   // [2*rp][mpad] 16-bit: P^ (scaled) hi rows then lo rows
@@ -40,7 +40,7 @@ struct MatMeta {
   float* scal;        // [4]: 0 = max|P| bits, 1 = P^ scale, 2 = Q scale, 3 = spare
 };
 
-constexpr int kMaxPasses = 5;  // CholeskyQR passes at most (shifted ones included)
+constexpr int kMaxPasses = 4;  // CholeskyQR passes at most (shifted ones included)
 constexpr int kMaxRank = 128;  // largest r of this build
 
 // Per-step device pointer tables (uploaded when they change).
@@ -80,21 +80,15 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
   return __float2bfloat16_rn(x);
 }
 
-// a + b rounded to odd in fp32 (exact sum known through Knuth's TwoSum). A second
-// rounding of a round-to-odd result to a format with at most 22 significant bits is
-// the correctly rounded (RNE) sum in that format (Boldo & Melquiond, "When double
-// rounding is odd"). This is what lets M = round_E(g + E) match an exact-arithmetic
-// reference bit for bit.
+// a + b rounded to odd in fp32. The two directed roundings bracket the exact sum: equal
+// when it is exact, else adjacent floats, and exactly one of those has an odd
+// significand. A second rounding of a round-to-odd result to a format with at most 22
+// significant bits is the correctly rounded (RNE) sum in that format (Boldo &
+// Melquiond, "When double rounding is odd"). This lets M = round_E(g + E) and
+// E = round_E(M - G^) equal a single rounding of the exact fp32-operand sum.
 __device__ __forceinline__ float add_round_odd(float a, float b) {
-  float s = __fadd_rn(a, b);
-  float bb = __fsub_rn(s, a);
-  float err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-  uint32_t u = __float_as_uint(s);
-  if (err != 0.0f && (u & 1u) == 0u && isfinite(s)) {
-    bool away = (err > 0.0f) == (s > 0.0f);
-    u = away ? u + 1u : u - 1u;
-  }
-  return __uint_as_float(u);
+  const float up = __fadd_ru(a, b), dn = __fadd_rd(a, b);
+  return (up == dn || (__float_as_uint(up) & 1u)) ? up : dn;
 }
 
 // round_E(a + b) with E = T; exact single rounding for 16-bit T, plain RN for fp32.
@@ -114,6 +108,7 @@ template <> __device__ __forceinline__ float add_to<float>(float a, float b) {
 namespace psgd {
 struct Handle;
 cudaError_t launch_ingest(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_unc_count(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_skip_and_unc(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_pgemm_simt(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_orth(const Handle& h, const Plan& p, cudaStream_t s);

@@ -15,7 +15,10 @@ constexpr int kT = 256;
 template <typename T>
 __device__ __forceinline__ float ldf(const T* p) { return to_f(*p); }
 
-// P tile: 64 rows x 128 columns of r. grid = (ceil(m/64), ceil(r/128), B*J).
+// P tile: 64 rows x 128 columns of r. grid = (ceil(m/64), ceil(r/128), B*J). Q is read
+// scaled by the exact power of two 2^e that puts max|Q| in [2^14, 2^15) (from scal[2]),
+// so P = (1/W) sum_w M_w Q 2^e. P^ does not depend on that scale, and M Q stays inside
+// fp32's range when M and Q are both tiny.
 template <typename TE>
 __global__ void __launch_bounds__(kT) k_pgemm(Plan p) {
   const MatMeta& mt = p.meta[blockIdx.z];
@@ -26,6 +29,9 @@ __global__ void __launch_bounds__(kT) k_pgemm(Plan p) {
   if (row0 >= m) return;
   const int col0 = blockIdx.y * 128;
   const float* Q = p.tab.q[blockIdx.z];
+  const unsigned qbits = reinterpret_cast<const unsigned*>(mt.scal)[2];
+  const int qex = qbits == 0u ? 0 : (int)((qbits >> 23) & 0xff) - 127;
+  const int qsh = 14 - (qex < -126 ? -126 : qex);  // Q * 2^qsh: ldexpf keeps it exact
   __shared__ float As[32][64 + 4];
   __shared__ __align__(16) float Bs[32][128];
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
@@ -52,7 +58,7 @@ __global__ void __launch_bounds__(kT) k_pgemm(Plan p) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int col = col0 + c + i;
-          Bs[kk][c + i] = (k < n && col < r) ? Q[k * r + col] : 0.f;
+          Bs[kk][c + i] = (k < n && col < r) ? ldexpf(Q[k * r + col], qsh) : 0.f;
         }
       }
       __syncthreads();

@@ -39,9 +39,6 @@ using namespace tc;
 constexpr int BM = 128;                // MMA M and A-tile rows (MN extent)
 constexpr int BK = 64;                 // K per stage (one 128-byte swizzle span)
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_MAX_ROWS = 3 * kMaxRank;     // split terms x rp
-constexpr int B_MAX_BYTES = B_MAX_ROWS * BK * 2;  // 48 KB
-constexpr int A_STAGES = 6;
 constexpr int B_STAGES = 2;
 constexpr int PCHUNK_KB = 4;           // P GEMM: k-blocks of 64 columns per unit
 constexpr int QSLICE_ROWS = 512;       // Q GEMM: rows of m per unit (matches Qpart slices)
@@ -100,10 +97,10 @@ __device__ __forceinline__ void split3(float xs, uint16_t& hi, uint16_t& mid, ui
 // Number of 16-bit terms the fp32 operand of the P and Q GEMMs is split into.
 template <typename T> __host__ __device__ constexpr int nterms() { return sizeof(T) == 2 && !std::is_same<T, __half>::value ? 3 : 2; }
 
-// max|Q| of the caller's Q state -> scal[2] (bits). grid = (64, B*J).
+// max|Q| of the caller's Q state -> scal[2] (bits). grid = (64, B*J). This and k_qsplit
+// run for every matrix: they can precede the skip decision of the step.
 __global__ void k_qmax(Plan p) {
   const MatMeta& mt = p.meta[blockIdx.y];
-  if (p.skip[mt.b]) return;
   const float* q = p.tab.q[blockIdx.y];
   const int64_t total = mt.n * p.r;
   unsigned mx = 0u;
@@ -119,7 +116,6 @@ __global__ void k_qmax(Plan p) {
 template <typename T>
 __global__ void k_qsplit(Plan p) {
   const MatMeta& mt = p.meta[blockIdx.z];
-  if (p.skip[mt.b]) return;
   const int c = blockIdx.y, rp = p.rp;
   const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= mt.n) return;
@@ -134,23 +130,32 @@ __global__ void k_qsplit(Plan p) {
   if (nterms<T>() == 3) mt.qsplit[(size_t)(2 * rp + c) * mt.n + j] = t2;
 }
 
-// P = (sum_c Ppart[c]) * 2^-e / W in chunk order, plus max|P| -> scal[1].
+// P = (sum_c Ppart[c]) / W in chunk order, plus max|P| -> scal[1]. P keeps the power-of-
+// two scale 2^e of the split Q: P^ does not depend on it, and removing it would push P
+// below fp32's range when both M and Q are tiny (deep blocks of the stack, M ~ Q ~ 2^-80).
 // grid = (ceil(m*rp / 256), B*J).
 __global__ void k_preduce(Plan p, int pchunk_kb) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
   const int rp = p.rp;
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   const int64_t mpad = (mt.m + 127) / 128 * 128;
   unsigned mx = 0u;
   if (i < mt.m * rp) {
     const int kch = (int)(((mt.n + 63) / 64 + pchunk_kb - 1) / pchunk_kb);
-    float acc = 0.f;
-    for (int c = 0; c < kch; ++c) acc = __fadd_rn(acc, mt.Ppart[(size_t)c * mpad * rp + i]);
-    const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[2]);
-    const float v = __fdiv_rn(ldexpf(acc, -e), (float)p.W);
-    mt.P[i] = v;
-    mx = __float_as_uint(fabsf(v));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < kch; ++c) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(mt.Ppart + (size_t)c * mpad * rp + i));
+      acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
+    }
+    const float fw = (float)p.W;
+    float4 o;
+    o.x = __fdiv_rn(acc.x, fw); o.y = __fdiv_rn(acc.y, fw);
+    o.z = __fdiv_rn(acc.z, fw); o.w = __fdiv_rn(acc.w, fw);
+    *reinterpret_cast<float4*>(mt.P + i) = o;
+    mx = max(max(__float_as_uint(fabsf(o.x)), __float_as_uint(fabsf(o.y))),
+             max(__float_as_uint(fabsf(o.z)), __float_as_uint(fabsf(o.w))));
   }
   mx = __reduce_max_sync(0xffffffffu, mx);
   if ((threadIdx.x & 31) == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 1, mx);
@@ -169,19 +174,33 @@ __global__ void k_psplit(Plan p, int kp) {
   if (row >= mpad) return;
   const int rp = p.rp;
   uint16_t* pd = mt.pdec + (size_t)row * 3 * kp;
-  for (int c = 0; c < kp; ++c) {
-    const float x = (row < mt.m && c < p.r) ? ldexpf(mt.Phat[row * rp + c], 14) : 0.f;
-    uint16_t t0, t1, t2 = 0, hh, hl;
-    if (nterms<T>() == 3) split3<T>(x, t0, t1, t2); else split2<T>(x, t0, t1);
-    split2<__half>(x, hh, hl);
-    if (c < rp) {
-      mt.psplit[(size_t)c * mpad + row] = t0;
-      mt.psplit[(size_t)(rp + c) * mpad + row] = t1;
-      if (nterms<T>() == 3) mt.psplit[(size_t)(2 * rp + c) * mpad + row] = t2;
+  for (int c0 = 0; c0 < kp; c0 += 8) {
+    float x[8];
+    if (row < mt.m && c0 < rp) {
+      const float4 a = *reinterpret_cast<const float4*>(mt.Phat + row * rp + c0);
+      const float4 b = *reinterpret_cast<const float4*>(mt.Phat + row * rp + c0 + 4);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = 0.f;
     }
-    pd[c] = hh;
-    pd[kp + c] = hl;
-    pd[2 * kp + c] = hh;
+    __align__(16) uint16_t hh[8], hl[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float xs = (c0 + i < p.r) ? x[i] * 16384.0f : 0.f;  // * 2^14, exact
+      uint16_t t0, t1, t2 = 0;
+      if (nterms<T>() == 3) split3<T>(xs, t0, t1, t2); else split2<T>(xs, t0, t1);
+      split2<__half>(xs, hh[i], hl[i]);
+      const int c = c0 + i;
+      if (c < rp) {
+        mt.psplit[(size_t)c * mpad + row] = t0;
+        mt.psplit[(size_t)(rp + c) * mpad + row] = t1;
+        if (nterms<T>() == 3) mt.psplit[(size_t)(2 * rp + c) * mpad + row] = t2;
+      }
+    }
+    *reinterpret_cast<uint4*>(pd + c0) = *reinterpret_cast<const uint4*>(hh);
+    *reinterpret_cast<uint4*>(pd + kp + c0) = *reinterpret_cast<const uint4*>(hl);
+    *reinterpret_cast<uint4*>(pd + 2 * kp + c0) = *reinterpret_cast<const uint4*>(hh);
   }
 }
 
@@ -196,34 +215,50 @@ __global__ void k_qdec(Plan p, int kp) {
   const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[3]);
   const float* q = p.tab.q[blockIdx.y];
   uint16_t* qd = mt.qdec + (size_t)row * 3 * kp;
-  for (int c = 0; c < kp; ++c) {
-    const float x = (row < mt.n && c < p.r) ? ldexpf(q[row * p.r + c], e) : 0.f;
-    uint16_t hi, lo;
-    split2<__half>(x, hi, lo);
-    qd[c] = hi;
-    qd[kp + c] = hi;
-    qd[2 * kp + c] = lo;
+  for (int c0 = 0; c0 < kp; c0 += 8) {
+    __align__(16) uint16_t hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = c0 + i;
+      const float x = (row < mt.n && c < p.r) ? ldexpf(q[row * p.r + c], e) : 0.f;
+      split2<__half>(x, hi[i], lo[i]);
+    }
+    *reinterpret_cast<uint4*>(qd + c0) = *reinterpret_cast<const uint4*>(hi);
+    *reinterpret_cast<uint4*>(qd + kp + c0) = *reinterpret_cast<const uint4*>(hi);
+    *reinterpret_cast<uint4*>(qd + 2 * kp + c0) = *reinterpret_cast<const uint4*>(lo);
   }
 }
 
 // ---------------------------------------------------------------- GEMM kernel
-// Shared memory: A ring, B ring, barriers, TMEM address slot.
-struct GemmSmem {
-  alignas(1024) uint8_t a[A_STAGES][A_BYTES];
-  alignas(1024) uint8_t b[B_STAGES][B_MAX_BYTES];
-  uint64_t full_a[A_STAGES], empty_a[A_STAGES];
+// Shared memory, carved at run time: a_stages A tiles (16 KB each), B_STAGES B tiles of
+// b_stage bytes (1 KB multiples), then the barriers and the TMEM address slot.
+constexpr int kMaxAStages = 12;
+struct GemmBars {
+  uint64_t full_a[kMaxAStages], empty_a[kMaxAStages];
   uint64_t full_b[B_STAGES], empty_b[B_STAGES];
   uint64_t acc_full[2], acc_empty[2], done;
   uint32_t tmem;
+};
+struct GemmSmem {
+  uint8_t* a0;
+  uint8_t* b0;
+  GemmBars* bar;
+  __device__ uint8_t* a(int s) const { return a0 + (size_t)s * A_BYTES; }
+  __device__ uint8_t* b(int s, uint32_t b_stage) const { return b0 + (size_t)s * b_stage; }
 };
 
 // MN_A = false: P GEMM (A = M tile K-major, unit = row tile x k-chunk).
 // MN_A = true:  Q GEMM (A = M^T tile MN-major, unit = column tile x m-slice).
 template <bool MN_A, bool BF16>
 __global__ void __launch_bounds__(192, 1)
-k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits) {
+k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
+       int a_stages, uint32_t b_stage) {
   extern __shared__ uint8_t smem_raw[];
-  GemmSmem& sm = *reinterpret_cast<GemmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  GemmSmem S{base, base + (size_t)a_stages * A_BYTES,
+             reinterpret_cast<GemmBars*>(base + (size_t)a_stages * A_BYTES + (size_t)B_STAGES * b_stage)};
+  GemmBars& sm = *S.bar;
+  const int A_STAGES = a_stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int TERMS = BF16 ? 3 : 2;
   const int rp = p.rp, N = TERMS * rp;          // B rows = MMA N in total
@@ -266,7 +301,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
           if (!ok) break;
           mbar_arrive_expect_tx(&sm.full_b[sb], b_bytes);
           for (int x = 0; x < NBOX; ++x)
-            tma_load_2d(sm.b[sb] + x * (N / NBOX) * BK * 2, mb, kb * BK, x * (N / NBOX), &sm.full_b[sb]);
+            tma_load_2d(S.b(sb, b_stage) + x * (N / NBOX) * BK * 2, mb, kb * BK, x * (N / NBOX), &sm.full_b[sb]);
           ++ib;
           for (int w = 0; w < p.W; ++w) {
             const int sa = ia % A_STAGES;
@@ -274,10 +309,10 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
             if (!ok) break;
             mbar_arrive_expect_tx(&sm.full_a[sa], A_BYTES);
             if (!MN_A) {
-              tma_load_3d(sm.a[sa], mm, kb * BK, un.tile * BM, w, &sm.full_a[sa]);
+              tma_load_3d(S.a(sa), mm, kb * BK, un.tile * BM, w, &sm.full_a[sa]);
             } else {
-              tma_load_3d(sm.a[sa], mm, un.tile * BM, kb * BK, w, &sm.full_a[sa]);
-              tma_load_3d(sm.a[sa] + A_BYTES / 2, mm, un.tile * BM + 64, kb * BK, w, &sm.full_a[sa]);
+              tma_load_3d(S.a(sa), mm, un.tile * BM, kb * BK, w, &sm.full_a[sa]);
+              tma_load_3d(S.a(sa) + A_BYTES / 2, mm, un.tile * BM + 64, kb * BK, w, &sm.full_a[sa]);
             }
             ++ia;
           }
@@ -311,13 +346,13 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
           ok = mbar_wait(&sm.full_b[sb], (ib / B_STAGES) & 1, err);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t b_addr = smem_u32(sm.b[sb]);
+          const uint32_t b_addr = smem_u32(S.b(sb, b_stage));
           for (int w = 0; w < p.W; ++w) {
             const int sa = ia % A_STAGES;
             ok = mbar_wait(&sm.full_a[sa], (ia / A_STAGES) & 1, err);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(sm.a[sa]);
+            const uint32_t a_addr = smem_u32(S.a(sa));
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
               const uint64_t adesc = MN_A ? smem_desc(a_addr + k * 2048, A_BYTES / 2, 1024)
@@ -393,21 +428,312 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
   if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
-// ---------------------------------------------------------------- decompression kernel
-struct DecSmem {
-  alignas(1024) uint8_t a[A_STAGES][A_BYTES];          // P^ split tiles, 128 x 64
-  alignas(1024) uint8_t b[A_STAGES][DEC_NT * BK * 2];  // Q split tiles, 128 x 64
-  uint64_t full[A_STAGES], empty[A_STAGES];
+// ---------------------------------------------------------------- fused ingest + P GEMM
+// One HBM sweep of the gradients. A copy warp stages G_w and E_w tiles (128 rows x 64
+// columns, 128-byte rows) into a shared-memory ring with bulk copies. Ingest warps form
+// M_w = round_E(zero_nonfinite(G_w / s_b) + E_w) from the staged tiles, count nonfinite
+// entries per (block, worker), store M_w to its scratch, and write the same tile into
+// shared memory in the UMMA 128-byte-swizzle K-major layout. The MMA thread accumulates
+// M_w (Q_hi | Q_lo [| Q_lo2]) over every worker and k-block of the unit into TMEM. The
+// epilogue writes the unit's P partial sums.
+// Warps: 0 TMA (Q split tiles), 1 MMA, 2..5 epilogue, 6..13 ingest, 14 G/E copies.
+constexpr int kIngWarps = 8;
+constexpr int GE_BYTES = 2 * A_BYTES;  // one staged G tile + one E tile
+constexpr int kMaxGeStages = 4;
+struct IngBars {
+  uint64_t full_a[kMaxAStages], empty_a[kMaxAStages];
+  uint64_t full_b[B_STAGES], empty_b[B_STAGES];
+  uint64_t full_ge[kMaxGeStages], empty_ge[kMaxGeStages];
   uint64_t acc_full[2], acc_empty[2], done;
   uint32_t tmem;
 };
 
-template <typename TE> struct Pack8;
-template <> struct Pack8<__half> { using T = uint4; };
-template <> struct Pack8<__nv_bfloat16> { using T = uint4; };
+// Walk the (unit, k-block, worker) tile sequence of this CTA.
+struct TileIter {
+  int u, kb, w;
+  bool valid;
+  Unit un;
+  __device__ void start(const Unit* units, int nunits) {
+    u = blockIdx.x; w = 0;
+    valid = u < nunits;
+    if (valid) { un = units[u]; kb = un.kb0; }
+  }
+  __device__ void next(const Unit* units, int nunits, int W) {
+    if (++w < W) return;
+    w = 0;
+    if (++kb < un.kb1) return;
+    u += gridDim.x;
+    valid = u < nunits;
+    if (valid) { un = units[u]; kb = un.kb0; }
+  }
+};
 
-// G^ tile 128 x 128 = A B^T over K = 3 kp, then E_w = round_E(M_w - G^) for every w.
-// Warps: 0 TMA, 1 MMA, 2..9 epilogue (two warps per TMEM lane quarter, 64 columns each).
+template <typename TE>
+__global__ void __launch_bounds__(480, 1)
+k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
+           int a_stages, int ge_stages, uint32_t b_stage) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* a0 = base;
+  uint8_t* b0 = a0 + (size_t)a_stages * A_BYTES;
+  uint8_t* ge0 = b0 + (size_t)B_STAGES * b_stage;
+  IngBars& sm = *reinterpret_cast<IngBars*>(ge0 + (size_t)ge_stages * GE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr bool BF16 = std::is_same<TE, __nv_bfloat16>::value;
+  constexpr int TERMS = BF16 ? 3 : 2;
+  const int rp = p.rp, N = TERMS * rp;
+  const int NACC = N <= 256 ? 2 : 1;
+  const int NBOX = N <= 256 ? 1 : 2;
+  const uint32_t b_bytes = (uint32_t)N * BK * 2;
+  int* err = p.err_word;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a_stages; ++i) { mbar_init(&sm.full_a[i], kIngWarps); mbar_init(&sm.empty_a[i], 1); }
+    for (int i = 0; i < B_STAGES; ++i) { mbar_init(&sm.full_b[i], 1); mbar_init(&sm.empty_b[i], 1); }
+    for (int i = 0; i < ge_stages; ++i) { mbar_init(&sm.full_ge[i], 1); mbar_init(&sm.empty_ge[i], kIngWarps); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&sm.acc_full[i], 1); mbar_init(&sm.acc_empty[i], 4); }
+    mbar_init(&sm.done, 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sm.tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA: Q split tiles
+    if (lane == 0) {
+      uint32_t ib = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const Unit un = units[u];
+        const CUtensorMap* mb = maps + (size_t)un.t * NMAPS + MAP_QS;
+        for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
+          const int sb = ib % B_STAGES;
+          ok = mbar_wait(&sm.empty_b[sb], ((ib / B_STAGES) & 1) ^ 1, err);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&sm.full_b[sb], b_bytes);
+          for (int x = 0; x < NBOX; ++x)
+            tma_load_2d(b0 + (size_t)sb * b_stage + x * (N / NBOX) * BK * 2, mb, kb * BK, x * (N / NBOX), &sm.full_b[sb]);
+          ++ib;
+        }
+      }
+      for (uint32_t k = (ib > B_STAGES ? ib - B_STAGES : 0); k < ib; ++k)
+        mbar_wait(&sm.full_b[k % B_STAGES], (k / B_STAGES) & 1, err, 1u << 20);
+    }
+  } else if (warp == 14) {
+    // ------------------------------------------------------------ G/E bulk copies
+    TileIter ti;
+    ti.start(units, nunits);
+    uint32_t ig = 0;
+    bool ok = true;
+    while (ti.valid && ok) {
+      const MatMeta& mt = p.meta[ti.un.t];
+      const size_t slot = (size_t)ti.un.t * p.W + ti.w;
+      const TE* g = static_cast<const TE*>(p.tab.g[slot]);
+      const TE* e = static_cast<const TE*>(p.tab.e[slot]);
+      const int64_t row0 = (int64_t)ti.un.tile * BM, col0 = (int64_t)ti.kb * BK;
+      const int vr = mt.m - row0 < BM ? (int)(mt.m - row0) : BM;
+      const int vc = mt.n - col0 < BK ? (int)(mt.n - col0) : BK;
+      const uint32_t rowb = (uint32_t)vc * 2;
+      const int s = ig % ge_stages;
+      if (lane == 0) ok = mbar_wait(&sm.empty_ge[s], ((ig / ge_stages) & 1) ^ 1, err);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(&sm.full_ge[s], 2u * (uint32_t)vr * rowb);
+      __syncwarp();
+      uint8_t* st = ge0 + (size_t)s * GE_BYTES;
+      for (int r = lane; r < vr; r += 32) {
+        bulk_load(st + r * 128, g + (row0 + r) * mt.n + col0, rowb, &sm.full_ge[s]);
+        bulk_load(st + A_BYTES + r * 128, e + (row0 + r) * mt.n + col0, rowb, &sm.full_ge[s]);
+      }
+      ++ig;
+      ti.next(units, nunits, p.W);
+    }
+    if (lane == 0)
+      for (uint32_t k = (ig > (uint32_t)ge_stages ? ig - ge_stages : 0); k < ig; ++k)
+        mbar_wait(&sm.full_ge[k % ge_stages], (k / ge_stages) & 1, err, 1u << 20);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const int n0 = N <= 256 ? N : 256;
+      const uint32_t idesc0 = idesc_f16(BM, n0, BF16, false, false);
+      const uint32_t idesc1 = idesc_f16(BM, N > 256 ? N - 256 : 16, BF16, false, false);
+      uint32_t ia = 0, ib = 0, ju = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const Unit un = units[u];
+        const int acc = (int)(ju % NACC);
+        ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+        uint32_t accum = 0;
+        for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
+          const int sb = ib % B_STAGES;
+          ok = mbar_wait(&sm.full_b[sb], (ib / B_STAGES) & 1, err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t b_addr = smem_u32(b0 + (size_t)sb * b_stage);
+          for (int w = 0; w < p.W; ++w) {
+            const int sa = ia % a_stages;
+            ok = mbar_wait(&sm.full_a[sa], (ia / a_stages) & 1, err);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(a0 + (size_t)sa * A_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint64_t adesc = smem_desc(a_addr + k * 32, 16, 1024);
+              umma_f16(d_tmem, adesc, smem_desc(b_addr + k * 32, 16, 1024), idesc0, accum);
+              if (N > 256)
+                umma_f16(d_tmem + 256, adesc, smem_desc(b_addr + 256 * 128 + k * 32, 16, 1024), idesc1, accum);
+              accum = 1;
+            }
+            umma_commit(&sm.empty_a[sa]);
+            ++ia;
+          }
+          umma_commit(&sm.empty_b[sb]);
+          ++ib;
+        }
+        umma_commit(&sm.acc_full[acc]);
+        ++ju;
+      }
+      umma_commit(&sm.done);
+      mbar_wait(&sm.done, 0, err, 1u << 22);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    uint32_t ju = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      const Unit un = units[u];
+      const MatMeta& mt = p.meta[un.t];
+      const int acc = (int)(ju % NACC);
+      ok = mbar_wait(&sm.acc_full[acc], (ju / NACC) & 1, err);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(quarter * 32) << 16);
+      const int64_t mpad = (mt.m + 127) / 128 * 128;
+      const int64_t grow = (int64_t)un.tile * BM + row_in_tile;
+      float* out = mt.Ppart + ((size_t)un.slot * mpad + grow) * rp;
+      for (int c = 0; c < rp; c += 16) {
+        float v[16], t[16];
+        tmem_ld16(t_row + c, v);
+#pragma unroll
+        for (int k = 1; k < TERMS; ++k) {
+          tmem_ld16(t_row + k * rp + c, t);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] += t[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(out + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
+      ++ju;
+    }
+  } else {
+    // ------------------------------------------------------------ ingest (warps 6..13)
+    const int it = threadIdx.x - 6 * 32;          // 0..255
+    const int cq = it & 7;                        // 16-byte chunk within the 128-byte row
+    const int rq = it >> 3;                       // first row (0..31); rows rq + 32k
+    TileIter ti;
+    ti.start(units, nunits);
+    uint32_t ia = 0, ig = 0;
+    bool ok = true;
+    while (ti.valid && ok) {
+      const MatMeta& mt = p.meta[ti.un.t];
+      const int sa = ia % a_stages, sg = ig % ge_stages;
+      ok = mbar_wait(&sm.empty_a[sa], ((ia / a_stages) & 1) ^ 1, err);
+      if (ok) ok = mbar_wait(&sm.full_ge[sg], (ig / ge_stages) & 1, err);
+      if (!ok) break;
+      uint8_t* tile = a0 + (size_t)sa * A_BYTES;
+      const uint8_t* gs = ge0 + (size_t)sg * GE_BYTES;
+      const float inv_s = p.tab.inv_scale[mt.b];
+      TE* mo = static_cast<TE*>(mt.mscr) + (size_t)ti.w * mt.m * mt.n;
+      const int64_t col = (int64_t)ti.kb * BK + cq * 8;
+      int cnt = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int rl = rq + 32 * k;
+        const int64_t row = (int64_t)ti.un.tile * BM + rl;
+        uint4 mv = make_uint4(0u, 0u, 0u, 0u);
+        if (row < mt.m && col < mt.n) {
+          const uint4 gv = *reinterpret_cast<const uint4*>(gs + rl * 128 + cq * 16);
+          const uint4 ev = *reinterpret_cast<const uint4*>(gs + A_BYTES + rl * 128 + cq * 16);
+          const TE* gx = reinterpret_cast<const TE*>(&gv);
+          const TE* ex = reinterpret_cast<const TE*>(&ev);
+          TE* mx = reinterpret_cast<TE*>(&mv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float x = to_f(gx[i]) * inv_s;
+            const bool bad = !isfinite(x);
+            cnt += bad;
+            mx[i] = add_to<TE>(bad ? 0.0f : x, to_f(ex[i]));
+          }
+          __stcg(reinterpret_cast<uint4*>(mo + row * mt.n + col), mv);
+        }
+        *reinterpret_cast<uint4*>(tile + rl * 128 + ((cq ^ (rl & 7)) << 4)) = mv;
+      }
+      fence_proxy_async_smem();
+      cnt = __reduce_add_sync(0xffffffffu, cnt);
+      if (lane == 0 && cnt)
+        atomicAdd(reinterpret_cast<unsigned long long*>(p.counts + (size_t)mt.b * p.W + ti.w),
+                  (unsigned long long)cnt);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.full_a[sa]);
+        mbar_arrive(&sm.empty_ge[sg]);
+      }
+      ++ia; ++ig;
+      ti.next(units, nunits, p.W);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+// Stage counts of the fused kernel: A stages for the MMA, G/E staging stages.
+void ingest_stages(int edt, uint32_t b_stage, int* a_st, int* ge_st, size_t* smem) {
+  const size_t budget = 227 * 1024 - 1024 - sizeof(IngBars) - (size_t)B_STAGES * b_stage;
+  int a = edt == DT_BF16 ? 2 : 3;
+  int ge = (int)std::min<size_t>(kMaxGeStages, (budget - (size_t)a * A_BYTES) / GE_BYTES);
+  *a_st = a;
+  *ge_st = ge;
+  *smem = 1024 + (size_t)a * A_BYTES + (size_t)B_STAGES * b_stage + (size_t)ge * GE_BYTES + sizeof(IngBars);
+}
+
+// ---------------------------------------------------------------- decompression kernel
+constexpr int DEC_STAGES = 4;
+constexpr int GS_LD = DEC_NT + 4;  // row stride (floats) of the staged G^ tile
+struct DecSmem {
+  alignas(1024) uint8_t a[DEC_STAGES][A_BYTES];          // P^ split tiles, 128 x 64
+  alignas(1024) uint8_t b[DEC_STAGES][DEC_NT * BK * 2];  // Q split tiles, 128 x 64
+  float g[BM * GS_LD];                                   // staged G^ tile
+  uint64_t full[DEC_STAGES], empty[DEC_STAGES];
+  uint64_t acc_full[2], acc_empty[2], done;
+  uint32_t tmem;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// G^ tile 128 x 128 = A B^T over K = 3 kp (tensor cores), staged through shared memory,
+// then streamed in a coalesced layout: G^ is written once, and E_w = round_E(M_w - G^)
+// for every worker, with each thread holding every worker's loads of two 8-column
+// segments in flight.
+// Warps: 0 TMA, 1 MMA, 2..9 epilogue (256 threads).
 template <typename TE>
 __global__ void __launch_bounds__(320, 1)
 k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits, int kp) {
@@ -419,9 +745,10 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
   constexpr uint32_t STAGE_TX = A_BYTES + DEC_NT * BK * 2;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < A_STAGES; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 1); }
+    for (int i = 0; i < DEC_STAGES; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&sm.acc_full[i], 1); mbar_init(&sm.acc_empty[i], 8); }
     mbar_init(&sm.done, 1);
+    sm.abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -444,8 +771,8 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
         const CUtensorMap* ma = maps + (size_t)un.t * NMAPS + MAP_PD;
         const CUtensorMap* mb = maps + (size_t)un.t * NMAPS + MAP_QD;
         for (int kb = 0; kb < nkb && ok; ++kb) {
-          const int s = it % A_STAGES;
-          ok = mbar_wait(&sm.empty[s], ((it / A_STAGES) & 1) ^ 1, err);
+          const int s = it % DEC_STAGES;
+          ok = mbar_wait(&sm.empty[s], ((it / DEC_STAGES) & 1) ^ 1, err);
           if (!ok) break;
           mbar_arrive_expect_tx(&sm.full[s], STAGE_TX);
           tma_load_2d(sm.a[s], ma, kb * BK, un.tile * BM, &sm.full[s]);
@@ -453,8 +780,8 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
           ++it;
         }
       }
-      for (uint32_t k = (it > A_STAGES ? it - A_STAGES : 0); k < it; ++k)
-        mbar_wait(&sm.full[k % A_STAGES], (k / A_STAGES) & 1, err, 1u << 20);
+      for (uint32_t k = (it > DEC_STAGES ? it - DEC_STAGES : 0); k < it; ++k)
+        mbar_wait(&sm.full[k % DEC_STAGES], (k / DEC_STAGES) & 1, err, 1u << 20);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -471,8 +798,8 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * DEC_NT);
         uint32_t accum = 0;
         for (int kb = 0; kb < nkb && ok; ++kb) {
-          const int s = it % A_STAGES;
-          ok = mbar_wait(&sm.full[s], (it / A_STAGES) & 1, err);
+          const int s = it % DEC_STAGES;
+          ok = mbar_wait(&sm.full[s], (it / DEC_STAGES) & 1, err);
           if (!ok) break;
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sm.a[s]), b_addr = smem_u32(sm.b[s]);
@@ -492,69 +819,101 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
       mbar_wait(&sm.done, 0, err, 1u << 22);
     }
   } else {
-    const int ew = warp - 2;             // 0..7
-    const int quarter = warp & 3;        // TMEM lane quarter this warp may access
-    const int half = ew >> 2;            // column half: 0 -> [0, 64), 1 -> [64, 128)
+    const int et = threadIdx.x - 64;       // 0..255
+    const int quarter = warp & 3;          // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;      // column half staged by this warp
     const int row_in_tile = quarter * 32 + lane;
     uint32_t ju = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
       const Unit un = units[u];
       const MatMeta& mt = p.meta[un.t];
       const int64_t m = mt.m, n = mt.n;
-      const int64_t row = (int64_t)un.tile * BM + row_in_tile;
-      const int64_t col0 = (int64_t)un.kb0 * DEC_NT + half * 64;
       float* gh = p.tab.ghat[un.t];
-      if (p.skip[mt.b]) {
-        if (row < m)
-          for (int c = 0; c < 64; c += 4)
-            if (col0 + c < n) *reinterpret_cast<float4*>(gh + row * n + col0 + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        continue;
-      }
-      const int acc = ju & 1;
-      ok = mbar_wait(&sm.acc_full[acc], (ju >> 1) & 1, err);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t t_row = tmem_base + (uint32_t)(acc * DEC_NT + half * 64) + ((uint32_t)(quarter * 32) << 16);
-      // G^ = acc * 2^-(14 + e): P^ was scaled by 2^14 and Q by 2^e. ldexpf keeps
-      // results that fall into fp32's subnormal range correctly rounded.
-      const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[3]);
-      for (int c = 0; c < 64; c += 16) {
-        float g[16];
-        tmem_ld16(t_row + c, g);
+      const int64_t row0 = (int64_t)un.tile * BM, col0 = (int64_t)un.kb0 * DEC_NT;
+      const bool skipped = p.skip[mt.b] != 0;
+      if (!skipped) {
+        const int acc = ju & 1;
+        if (!mbar_wait(&sm.acc_full[acc], (ju >> 1) & 1, err)) sm.abort_flag = 1;
+        tc_fence_after();
+        if (!sm.abort_flag) {
+          // G^ = acc * 2^-(14 + e) as exact power-of-two factors (one rounding at most)
+          const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[3]);
+          const int tsh = 14 + e;
+          const int t1 = tsh > 126 ? 126 : (tsh < -126 ? -126 : tsh);
+          const float f1 = __uint_as_float((uint32_t)(127 - t1) << 23);
+          const float f2 = __uint_as_float((uint32_t)(127 - (tsh - t1)) << 23);
+          const uint32_t t_row = tmem_base + (uint32_t)(acc * DEC_NT + half * 64) + ((uint32_t)(quarter * 32) << 16);
+          float* gs = sm.g + row_in_tile * GS_LD + half * 64;
+          for (int c = 0; c < 64; c += 16) {
+            float v[16];
+            tmem_ld16(t_row + c, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) g[i] = ldexpf(g[i] * 0x1p-14f, -e);
-        const int64_t col = col0 + c;
-        if (row < m && col < n) {
-          // n is a multiple of 8, so a 16-column group is either fully inside or
-          // ends on a multiple of 8 within it.
-          const int nv = n - col < 16 ? (int)(n - col) : 16;
-          float* gp = gh + row * n + col;
-#pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            if (i < nv) *reinterpret_cast<float4*>(gp + i) = make_float4(g[i], g[i + 1], g[i + 2], g[i + 3]);
-          const TE* mbase = static_cast<const TE*>(mt.mscr) + row * n + col;
-          for (int w = 0; w < p.W; ++w) {
-            const TE* mp = mbase + (size_t)w * m * n;
-            TE* ep = static_cast<TE*>(p.tab.e[(size_t)un.t * p.W + w]) + row * n + col;
-#pragma unroll
-            for (int h = 0; h < 16; h += 8) {
-              if (h < nv) {
-                uint4 mv = *reinterpret_cast<const uint4*>(mp + h);
-                const TE* mx = reinterpret_cast<const TE*>(&mv);
-                TE ev[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) ev[i] = add_to<TE>(to_f(mx[i]), -g[h + i]);
-                *reinterpret_cast<uint4*>(ep + h) = *reinterpret_cast<const uint4*>(ev);
-              }
-            }
+            for (int i = 0; i < 16; i += 4)
+              *reinterpret_cast<float4*>(gs + c + i) =
+                  make_float4((v[i] * f1) * f2, (v[i + 1] * f1) * f2, (v[i + 2] * f1) * f2, (v[i + 3] * f1) * f2);
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
+        ++ju;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
-      ++ju;
+      epi_bar();  // staged tile complete (or an abort recorded)
+      if (sm.abort_flag) break;
+      const TE* mbase = static_cast<const TE*>(mt.mscr);
+      const size_t wstride = (size_t)m * n;
+      // 128 rows x 16 segments of 8 columns; thread et takes segments et + 256 k
+#pragma unroll 1
+      for (int k = 0; k < 8; k += 2) {
+        int64_t rowk[2], colk[2];
+        bool val[2];
+        float gv[2][8];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int sg = et + 256 * (k + q);
+          const int rl = sg >> 4, cs = (sg & 15) * 8;
+          rowk[q] = row0 + rl;
+          colk[q] = col0 + cs;
+          val[q] = rowk[q] < m && colk[q] < n;
+          if (skipped) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) gv[q][i] = 0.f;
+          } else {
+            const float4 a = *reinterpret_cast<const float4*>(sm.g + rl * GS_LD + cs);
+            const float4 b = *reinterpret_cast<const float4*>(sm.g + rl * GS_LD + cs + 4);
+            gv[q][0] = a.x; gv[q][1] = a.y; gv[q][2] = a.z; gv[q][3] = a.w;
+            gv[q][4] = b.x; gv[q][5] = b.y; gv[q][6] = b.z; gv[q][7] = b.w;
+          }
+          if (val[q]) {
+            float* gp = gh + rowk[q] * n + colk[q];
+            *reinterpret_cast<float4*>(gp) = make_float4(gv[q][0], gv[q][1], gv[q][2], gv[q][3]);
+            *reinterpret_cast<float4*>(gp + 4) = make_float4(gv[q][4], gv[q][5], gv[q][6], gv[q][7]);
+          }
+        }
+        if (skipped) continue;
+        for (int w0 = 0; w0 < p.W; w0 += 8) {
+          uint4 mv[2][8];
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              if (val[q] && w0 + kk < p.W)
+                mv[q][kk] = __ldcs(reinterpret_cast<const uint4*>(mbase + (size_t)(w0 + kk) * wstride + rowk[q] * n + colk[q]));
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              if (!val[q] || w0 + kk >= p.W) continue;
+              const TE* mx = reinterpret_cast<const TE*>(&mv[q][kk]);
+              __align__(16) TE ev[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) ev[i] = add_to<TE>(to_f(mx[i]), -gv[q][i]);
+              TE* ep = static_cast<TE*>(p.tab.e[(size_t)un.t * p.W + w0 + kk]) + rowk[q] * n + colk[q];
+              __stcs(reinterpret_cast<uint4*>(ep), *reinterpret_cast<const uint4*>(ev));
+            }
+        }
+      }
+      epi_bar();  // the staged tile may be overwritten by the next unit
     }
   }
   tc_fence_before();
@@ -597,7 +956,18 @@ int num_sms() {
   return sms > 0 ? sms : 148;
 }
 
-size_t gemm_smem() { return sizeof(GemmSmem) + 1024; }
+// B stage bytes and the number of A stages that fit next to two B stages.
+uint32_t gemm_b_stage(int edt, int rp) {
+  const int rows = (edt == DT_BF16 ? 3 : 2) * rp;
+  return (uint32_t)((rows * BK * 2 + 1023) / 1024 * 1024);
+}
+int gemm_a_stages(uint32_t b_stage) {
+  const size_t budget = 227 * 1024 - 1024 - sizeof(GemmBars) - (size_t)B_STAGES * b_stage;
+  return (int)std::min<size_t>(kMaxAStages, budget / A_BYTES);
+}
+size_t gemm_smem(uint32_t b_stage, int a_stages) {
+  return 1024 + (size_t)a_stages * A_BYTES + (size_t)B_STAGES * b_stage + sizeof(GemmBars);
+}
 size_t dec_smem() { return sizeof(DecSmem) + 1024; }
 
 struct TcLayout {
@@ -736,11 +1106,13 @@ cudaError_t tc_plan(Handle& h, char* ws_tc, cudaStream_t s) {
   if (e == cudaSuccess) e = cudaMemcpyAsync(tp->d_dunits, du.data(), sizeof(Unit) * du.size(), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return e;
-  const int gs = (int)gemm_smem(), ds = (int)dec_smem();
+  const int gs = 227 * 1024, ds = (int)dec_smem();
   e = cudaFuncSetAttribute(k_gemm<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_ingest_p<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_ingest_p<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_decomp_tc<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, ds);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_decomp_tc<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, ds);
   return e;
@@ -749,6 +1121,12 @@ cudaError_t tc_plan(Handle& h, char* ws_tc, cudaStream_t s) {
 void tc_free(Handle& h) {
   delete static_cast<TcPlan*>(h.tc_plan);
   h.tc_plan = nullptr;
+}
+
+cudaError_t launch_qmax(const Handle& h, const Plan& p, cudaStream_t s) {
+  k_qmax<<<dim3(64, p.B * p.J), 256, 0, s>>>(p);
+  h.launches += 1;
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prep_q(const Handle& h, const Plan& p, cudaStream_t s) {
@@ -764,12 +1142,36 @@ cudaError_t launch_prep_q(const Handle& h, const Plan& p, cudaStream_t s) {
 cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
   const int grid = std::min(tp->grid, tp->np);
-  if (h.edt == DT_BF16) k_gemm<false, true><<<grid, 192, gemm_smem(), s>>>(p, tp->d_maps, tp->d_punits, tp->np);
-  else k_gemm<false, false><<<grid, 192, gemm_smem(), s>>>(p, tp->d_maps, tp->d_punits, tp->np);
+  const uint32_t bst = gemm_b_stage(h.edt, p.rp);
+  const int ast = gemm_a_stages(bst);
+  const size_t sm = gemm_smem(bst, ast);
+  if (h.edt == DT_BF16) k_gemm<false, true><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst);
+  else k_gemm<false, false><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst);
   int64_t maxe = 0;
   for (const MatMeta& mt : h.meta) maxe = std::max<int64_t>(maxe, mt.m * p.rp);
-  k_preduce<<<dim3((unsigned)((maxe + 255) / 256), p.B * p.J), 256, 0, s>>>(p, PCHUNK_KB);
+  k_preduce<<<dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), 256, 0, s>>>(p, PCHUNK_KB);
   h.launches += 2;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ingest_p(const Handle& h, const Plan& p, cudaStream_t s) {
+  const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
+  const int grid = std::min(tp->grid, tp->np);
+  const uint32_t bst = gemm_b_stage(h.edt, p.rp);
+  int ast, gst;
+  size_t sm;
+  ingest_stages(h.edt, bst, &ast, &gst, &sm);
+  if (h.edt == DT_BF16) k_ingest_p<__nv_bfloat16><<<grid, 480, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst);
+  else k_ingest_p<__half><<<grid, 480, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst);
+  h.launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_preduce(const Handle& h, const Plan& p, cudaStream_t s) {
+  int64_t maxe = 0;
+  for (const MatMeta& mt : h.meta) maxe = std::max<int64_t>(maxe, mt.m * p.rp);
+  k_preduce<<<dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), 256, 0, s>>>(p, PCHUNK_KB);
+  h.launches += 1;
   return cudaGetLastError();
 }
 
@@ -779,8 +1181,11 @@ cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   if (h.edt == DT_BF16) k_psplit<__nv_bfloat16><<<g, 128, 0, s>>>(p, tp->kp);
   else k_psplit<__half><<<g, 128, 0, s>>>(p, tp->kp);
   const int grid = std::min(tp->grid, tp->nq);
-  if (h.edt == DT_BF16) k_gemm<true, true><<<grid, 192, gemm_smem(), s>>>(p, tp->d_maps, tp->d_qunits, tp->nq);
-  else k_gemm<true, false><<<grid, 192, gemm_smem(), s>>>(p, tp->d_maps, tp->d_qunits, tp->nq);
+  const uint32_t bst = gemm_b_stage(h.edt, p.rp);
+  const int ast = gemm_a_stages(bst);
+  const size_t sm = gemm_smem(bst, ast);
+  if (h.edt == DT_BF16) k_gemm<true, true><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst);
+  else k_gemm<true, false><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst);
   h.launches += 2;
   return cudaGetLastError();
 }

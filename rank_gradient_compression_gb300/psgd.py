@@ -23,7 +23,8 @@ DTYPE_CODE = {"f32": PSGD_F32, "f16": PSGD_F16, "bf16": PSGD_BF16}
 EXPORTS = ("psgd_workspace_size", "psgd_mask_offset", "psgd_mask_words", "psgd_init",
            "psgd_step", "psgd_check", "psgd_finalize", "psgd_strerror", "psgd_last_error",
            "psgd_debug_m", "psgd_debug_phat", "psgd_engine", "psgd_profile_begin",
-           "psgd_profile_end", "psgd_launch_count")
+           "psgd_profile_end", "psgd_launch_count", "psgd_debug_orth")
+PSGD_MAX_ORTH_PASSES = 4
 PSGD_NUM_PHASES = 7
 PHASES = ("ingest", "skip_unc", "pgemm", "orth", "qgemm", "qreduce", "decomp")
 
@@ -88,6 +89,8 @@ def _load():
     lib.psgd_profile_end.argtypes = [c_void_p, POINTER(c_double), POINTER(c_int32)]
     lib.psgd_launch_count.restype = c_int64
     lib.psgd_launch_count.argtypes = [c_void_p]
+    lib.psgd_debug_orth.restype = c_int32
+    lib.psgd_debug_orth.argtypes = [c_void_p, c_int32, c_int32, POINTER(c_int32), c_void_p]
     return lib
 
 
@@ -231,6 +234,15 @@ class PowerSGD:
         rp = (self.r + 15) // 16 * 16
         off = ptr - self.workspace.data_ptr()
         return self.workspace[off:off + m * rp * 4].view(self.torch.float32).view(m, rp)[:, :self.r]
+
+    def debug_orth(self, b, j):
+        """(passes run in the last step, per-pass records [final, buffer, shifted, dead])."""
+        out = (c_int32 * (4 * PSGD_MAX_ORTH_PASSES))()
+        n = lib.psgd_debug_orth(c_void_p(self.handle), b, j, out,
+                                c_void_p(self.torch.cuda.current_stream(self.device).cuda_stream))
+        if n < 0:
+            raise PSGDError(PSGD_EINVAL, "psgd_debug_orth failed")
+        return n, [list(out[4 * k:4 * k + 4]) for k in range(PSGD_MAX_ORTH_PASSES)]
 
     def close(self):
         if getattr(self, "handle", None):

@@ -83,6 +83,16 @@ class GpuRun:
     def step(self):
         self.ps.step(self.grads, self.errs, self.q, self.scales, self.ghat, self.unc_in, self.unc_out)
 
+    def load_state(self, o: "OracleRun"):
+        """Overwrite the caller-owned state (E, Q) with the oracle's, so the next step
+        starts from identical inputs on both sides. The conversion is exact: the
+        oracle holds E-dtype and fp32 values."""
+        for b in o.blocks:
+            for j in range(len(self.wl.shapes)):
+                self.q[b][j].copy_(torch.from_numpy(o.state[b].q[j]).to(torch.float32))
+                for w in range(self.wl.workers):
+                    self.errs[b][j][w].copy_(torch.from_numpy(o.state[b].e[j][w]).to(self.errs[b][j][w].dtype))
+
 
 class OracleRun:
     def __init__(self, wl: synth.Workload, blocks, orth="householder"):
@@ -113,15 +123,23 @@ class OracleRun:
 
 
 def compare_step(g: GpuRun, o_res: dict, o: OracleRun, tol=TOL, check_m=True):
-    """Compare one step. Returns the worst relative errors (G-hat, E).
+    """Compare one step. Returns the worst (G-hat, E before storage, stored E) errors.
 
-    M = round_E(g + E) is compared bit for bit only when both sides start the step from
-    the same E, i.e. at the first step (E = 0). Later, each side's E carries its own
-    one-ulp rounding differences, and only E's Frobenius error is bounded."""
+    - Masks/counts and skips: bit-exact.
+    - M = round_E(g + E): bit-exact when both sides start the step from the same E.
+    - G-hat: relative Frobenius error <= tol.
+    - E: the value the step computes is M - G-hat, before it is stored in E's type. That
+      value is held to tol (absolutely, against ||M||, when the oracle's E is tiny). The
+      stored E must be the RNE of the GPU's own M - G-hat, bit for bit: a property of the
+      GPU's outputs, checked with the rounding routine. The stored E's distance to the
+      oracle's stored E is returned, not asserted. Where G-hat is many times E (a
+      decaying spectrum at large r), a G-hat difference far inside tol moves a few
+      entries across a 16-bit rounding boundary, and each such entry costs a whole ulp."""
     wl = g.wl
     counts = g.ps.counts.cpu().numpy().reshape(wl.blocks, wl.workers)
     skip = g.ps.skip.cpu().numpy()
-    worst_g = worst_e = 0.0
+    tdt = synth.TORCH_DTYPE[wl.err_dtype]
+    worst_g = worst_pre = worst_st = 0.0
     for b, res in o_res.items():
         assert list(counts[b]) == res.counts, f"block {b}: counts {counts[b]} vs {res.counts}"
         assert bool(skip[b]) == res.skip, f"block {b}: skip {skip[b]} vs {res.skip}"
@@ -134,22 +152,26 @@ def compare_step(g: GpuRun, o_res: dict, o: OracleRun, tol=TOL, check_m=True):
                 worst_g = max(worst_g, eg)
                 assert eg <= tol, f"block {b} matrix {j}: G-hat rel err {eg:.3e}"
             for w in range(wl.workers):
-                eg_w = f64(g.errs[b][j][w])
+                e_gpu = f64(g.errs[b][j][w])
                 e_ref = o.state[b].e[j][w]
-                m_norm = float(np.linalg.norm(res.m[j][w]))
-                if not res.skip and float(np.linalg.norm(e_ref)) < E_FLOOR * m_norm:
-                    ea = float(np.linalg.norm(eg_w - e_ref))
-                    assert ea <= E_ABS * m_norm, f"block {b} matrix {j} worker {w}: |dE| {ea:.3e} vs |M| {m_norm:.3e}"
-                    continue
-                ee = rel_err(eg_w, e_ref)
-                worst_e = max(worst_e, ee)
-                if res.skip:
-                    assert np.array_equal(eg_w, e_ref), "skipped block must keep E"
-                else:
-                    assert ee <= tol, f"block {b} matrix {j} worker {w}: E rel err {ee:.3e}"
+                m_gpu = f64(g.ps.debug_m(b, j, w, tdt))
                 if check_m:
-                    m_gpu = f64(g.ps.debug_m(b, j, w, synth.TORCH_DTYPE[wl.err_dtype]))
                     assert np.array_equal(m_gpu, res.m[j][w]), f"block {b} matrix {j} worker {w}: M differs"
+                if res.skip:
+                    assert np.array_equal(e_gpu, e_ref), "skipped block must keep E"
+                    continue
+                pre_gpu = m_gpu - gh
+                assert np.array_equal(e_gpu, oracle.round_to_format(pre_gpu, wl.err_dtype)), \
+                    f"block {b} matrix {j} worker {w}: stored E is not RNE(M - G-hat)"
+                m_norm = float(np.linalg.norm(res.m[j][w]))
+                if float(np.linalg.norm(res.e_pre[j][w])) < E_FLOOR * m_norm:
+                    ea = float(np.linalg.norm(pre_gpu - res.e_pre[j][w]))
+                    assert ea <= E_ABS * m_norm, f"block {b} matrix {j} worker {w}: |dE| {ea:.3e} vs |M| {m_norm:.3e}"
+                else:
+                    ep = rel_err(pre_gpu, res.e_pre[j][w])
+                    worst_pre = max(worst_pre, ep)
+                    assert ep <= tol, f"block {b} matrix {j} worker {w}: E (before storage) rel err {ep:.3e}"
+                    worst_st = max(worst_st, rel_err(e_gpu, e_ref))
         if wl.unc_len:
             uo = f64(g.unc_out[b])
             eu = rel_err(uo, res.unc_out)
@@ -157,10 +179,37 @@ def compare_step(g: GpuRun, o_res: dict, o: OracleRun, tol=TOL, check_m=True):
                 assert np.all(uo == 0)
             else:
                 assert eu <= 1e-6, f"block {b}: gains/biases rel err {eu:.3e}"
-    return worst_g, worst_e
+    return worst_g, worst_pre, worst_st
 
 
-def run_parity(wl, steps=None, oracle_blocks=None, flags=0, tol=TOL, check_m=True, threads=8):
+def ulp_diff(a: torch.Tensor, b: np.ndarray) -> int:
+    """Largest distance in units in the last place between two arrays of a 16-bit or
+    fp32 type (finite values; same-sign ordering of the bit patterns)."""
+    dt = a.dtype
+    bt = torch.from_numpy(b).to(dt)
+    it = {torch.float16: torch.int16, torch.bfloat16: torch.int16, torch.float32: torch.int32}[dt]
+    ia = a.detach().cpu().view(it).to(torch.int64)
+    ib = bt.view(it).to(torch.int64)
+    sign = 1 << (15 if it == torch.int16 else 31)
+    # map sign-magnitude bit patterns onto a monotone integer line
+    ia = torch.where(ia < 0, -(ia + sign), ia)
+    ib = torch.where(ib < 0, -(ib + sign), ib)
+    return int((ia - ib).abs().max().item())
+
+
+def run_parity(wl, steps=None, oracle_blocks=None, flags=0, tol=TOL, check_m=True, threads=8,
+               synced=True):
+    """Run both sides over the steps and compare each step.
+
+    synced=True (default) copies the oracle's E and Q into the GPU's caller-owned buffers
+    before every step. Each step then starts from identical inputs, and M is compared bit
+    for bit every step. The maximum one-ulp distance of the stored E is reported by
+    ulp_diff, not asserted: where E is near zero, a G-hat difference far below E's
+    tolerance can span several of E's ulps. With synced=False each side carries its own state. The warm-started power
+    iteration then amplifies the one-ulp differences of the stored E into a growing
+    rotation of the subspace wherever singular-value gaps are small. That is the
+    method's sensitivity, not kernel error, and only the first step is compared at the
+    1e-4 bar in that mode."""
     steps = wl.steps if steps is None else steps
     g = GpuRun(wl, oracle_blocks, flags)
     o = OracleRun(wl, g.oracle_blocks)
@@ -168,8 +217,10 @@ def run_parity(wl, steps=None, oracle_blocks=None, flags=0, tol=TOL, check_m=Tru
     with cf.ThreadPoolExecutor(threads) as pool:
         for t in range(steps):
             g.load_inputs(t)
+            if synced:
+                g.load_state(o)
             g.step()
             torch.cuda.synchronize()
             res = o.step(t, pool)
-            worst.append(compare_step(g, res, o, tol, check_m and t == 0))
+            worst.append(compare_step(g, res, o, tol, check_m and (synced or t == 0)))
     return g, o, worst
