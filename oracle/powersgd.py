@@ -123,7 +123,8 @@ class PowerStepResult:
     g_hat: np.ndarray  # decompressed gradient P_hat Q^T, m x n
 
 
-def power_step(ms, q: np.ndarray, orth: str = "householder") -> PowerStepResult:
+def power_step(ms, q: np.ndarray, orth: str = "householder", accum_noise: float = 0.0,
+               noise_seed: int = 0) -> PowerStepResult:
     """One warm-started subspace-iteration step over W workers that share Q.
 
     [card] 方法适配: the low-rank factors are all-reduced between machines instead of
@@ -137,11 +138,28 @@ def power_step(ms, q: np.ndarray, orth: str = "householder") -> PowerStepResult:
     Each worker's product is formed on its own, and only then averaged. The oracle does
     not factor the mean through M-bar, so the linearity of the mean stays a pin and
     is not an assumption.
+
+    accum_noise = c > 0 models fp32 accumulation: it adds to each entry of P and of the new
+    Q the error c * u32 * z * sqrt(sum of its squared product terms), with z ~ N(0, 1)
+    seeded. That is the probabilistic rounding-error size of a blocked fp32 sum. The
+    default, 0, follows the algorithm. The option measures how much the step's outputs
+    move under the rounding an fp32 implementation's long accumulations leave. That is
+    large where the sums cancel: in the small singular directions of a decaying
+    spectrum the terms are kappa times the result. It sets the tolerance such inputs
+    are tested at.
     """
     w = len(ms)
+    rng = np.random.default_rng(noise_seed)
+    u32 = 2.0 ** -24
     p = sum(np.asarray(mw, dtype=np.float64) @ q for mw in ms) / w
+    if accum_noise > 0:
+        mag = np.sqrt(sum((np.asarray(mw, dtype=np.float64) ** 2) @ (q ** 2) for mw in ms)) / w
+        p = p + accum_noise * u32 * mag * rng.standard_normal(p.shape)
     p_hat = orthonormalize(p, orth)
     q_new = sum(np.asarray(mw, dtype=np.float64).T @ p_hat for mw in ms) / w
+    if accum_noise > 0:
+        mag = np.sqrt(sum((np.asarray(mw, dtype=np.float64) ** 2).T @ (p_hat ** 2) for mw in ms)) / w
+        q_new = q_new + accum_noise * u32 * mag * rng.standard_normal(q_new.shape)
     q_new = round_to_format(q_new, "f32")
     g_hat = p_hat @ q_new.T
     return PowerStepResult(p=p, p_hat=p_hat, q=q_new, g_hat=g_hat)
@@ -200,7 +218,8 @@ class BlockResult:
 
 
 def block_step(grads, state: BlockState, scale: float, err_fmt: str,
-               skip_fraction: float = 1.0, unc=None, orth: str = "householder"):
+               skip_fraction: float = 1.0, unc=None, orth: str = "householder",
+               accum_noise: float = 0.0):
     """One PowerSGD step for one resblock: every matrix j, every worker w.
 
     ``grads[j][w]`` holds the raw (scaled) gradient values as fp64, and ``unc[w]`` the raw
@@ -236,7 +255,7 @@ def block_step(grads, state: BlockState, scale: float, err_fmt: str,
             unc_out=None if unc is None else np.zeros_like(unc_mean))
     g_hats, e_pres, p_hats = [], [], []
     for j in range(J):
-        res = power_step(ms[j], state.q[j], orth)
+        res = power_step(ms[j], state.q[j], orth, accum_noise, noise_seed=j)
         state.q[j] = res.q
         pre_j = []
         for w in range(W):

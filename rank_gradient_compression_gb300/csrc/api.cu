@@ -30,14 +30,14 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Rows of the Q-GEMM slices and Gram chunks of the FFMA engine.
 constexpr int64_t kSliceRows = 512;
-constexpr int64_t kGramRows = 256;
+constexpr int64_t kGramRows = 64;
 
 struct Layout {
   size_t total = 0;
   size_t meta = 0, threshold = 0, mask_off = 0, segs = 0, table = 0, err = 0, scal = 0;
   std::vector<size_t> mscr, P, Xa, Xb, Phat, ostate, Qpart, Gpart, Rinv;
   size_t tc = 0;
-  size_t table_bytes = 0;
+  size_t table_bytes = 0, maps_bytes = 0;
   int64_t nseg = 0;
 };
 
@@ -83,9 +83,11 @@ Layout plan_layout(const psgd_config* c) {
   L.nseg = (int64_t)B * J * W + (c->unc_len > 0 ? (int64_t)B * W : 0);
   L.segs = take(sizeof(IngestSeg) * L.nseg);
   L.table_bytes = 8 * ((size_t)2 * B * J * W + 2 * (size_t)B * J + (size_t)B * W + B) + 4 * (size_t)B;
-  L.table = take(L.table_bytes);
+  L.table_bytes = (L.table_bytes + 127) / 128 * 128;
+  L.maps_bytes = tc_ge_maps_bytes(c);
+  L.table = take(L.table_bytes + L.maps_bytes);
   L.err = take(16);
-  L.scal = take(16 * (size_t)B * J);
+  L.scal = take(4 * kScalWords * (size_t)B * J);
   for (int t = 0; t < B * J; ++t) {
     const psgd_shape s = c->shapes[t % J];
     const int64_t mpad = ceil_div(s.m, 128) * 128;
@@ -193,6 +195,7 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
   h.d_segs = reinterpret_cast<IngestSeg*>(h.ws + L.segs);
   h.d_table = h.ws + L.table;
   h.table_bytes = L.table_bytes;
+  h.maps_bytes = h.tc ? L.maps_bytes : 0;
   h.d_err = reinterpret_cast<int*>(h.ws + L.err);
   h.d_scal_all = reinterpret_cast<float*>(h.ws + L.scal);
 
@@ -214,7 +217,7 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
     mt.Qpart = reinterpret_cast<float*>(h.ws + L.Qpart[t]);
     mt.Gpart = reinterpret_cast<float*>(h.ws + L.Gpart[t]);
     mt.Rinv = reinterpret_cast<float*>(h.ws + L.Rinv[t]);
-    mt.scal = h.d_scal_all + 4 * t;
+    mt.scal = h.d_scal_all + kScalWords * t;
     h.max_mtiles = std::max(h.max_mtiles, mt.mtiles);
     h.max_S = std::max(h.max_S, mt.S);
     h.max_C = std::max(h.max_C, mt.C);
@@ -267,7 +270,7 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
   if (e == cudaSuccess) e = cudaMemcpyAsync(h.d_segs, h.segs.data(), sizeof(IngestSeg) * h.segs.size(), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(h.d_err, 0, 16, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&h.h_stage), h.table_bytes, cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&h.h_stage), h.table_bytes + h.maps_bytes, cudaHostAllocDefault);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.upload_ev, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     if (h.h_stage) cudaFreeHost(h.h_stage);
@@ -284,6 +287,7 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
   h.tab.unc_in = reinterpret_cast<const float* const*>(base + 16 * B * J * W + 16 * B * J);
   h.tab.unc_out = reinterpret_cast<float* const*>(base + 16 * B * J * W + 16 * B * J + 8 * B * W);
   h.tab.inv_scale = reinterpret_cast<const float*>(base + 16 * B * J * W + 16 * B * J + 8 * B * W + 8 * B);
+  h.tab.ge_maps = h.maps_bytes ? base + h.table_bytes : nullptr;
   *out = ph;
   return PSGD_OK;
 }
@@ -343,7 +347,9 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   if (!h.have_table || tab != h.last_table) {
     if (h.have_table && (e = cudaEventSynchronize(h.upload_ev)) != cudaSuccess) return cuda_fail(e, "table event");
     std::memcpy(h.h_stage, tab.data(), h.table_bytes);
-    if ((e = cudaMemcpyAsync(h.d_table, h.h_stage, h.table_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    if (h.maps_bytes && !tc_encode_ge_maps(h, a->grads, a->errs, h.h_stage + h.table_bytes))
+      return fail(PSGD_ECUDA, "cuTensorMapEncodeTiled failed for a gradient or error buffer");
+    if ((e = cudaMemcpyAsync(h.d_table, h.h_stage, h.table_bytes + h.maps_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
       return cuda_fail(e, "table upload");
     if ((e = cudaEventRecord(h.upload_ev, s)) != cudaSuccess) return cuda_fail(e, "table event");
     h.last_table.swap(tab);
@@ -369,7 +375,7 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   auto mark = [&]() { if (ev) cudaEventRecord(ev[phase++], s); };
   mark();
   if ((e = cudaMemsetAsync(a->counts, 0, 8 * B * W, s)) != cudaSuccess) return cuda_fail(e, "counts");
-  if ((e = cudaMemsetAsync(h.d_scal_all, 0, 16 * B * J, s)) != cudaSuccess) return cuda_fail(e, "scal");
+  if ((e = cudaMemsetAsync(h.d_scal_all, 0, 4 * kScalWords * B * J, s)) != cudaSuccess) return cuda_fail(e, "scal");
   // The fused path ingests the gradients and forms the P partial sums in one sweep; the
   // debug outputs (mask bitmap, stop after ingest) use the separate ingest kernel.
   const bool fused = h.tc && !(h.cfg.flags & (PSGD_FLAG_MASK | PSGD_FLAG_STOP_AFTER_INGEST));
@@ -388,10 +394,12 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
     return PSGD_OK;
   }
   if (fused) {
+    if (h.edt == DT_BF16 && (e = launch_rescale_tiny(h, p, s)) != cudaSuccess) return cuda_fail(e, "rescale");
     if ((e = launch_preduce(h, p, s)) != cudaSuccess) return cuda_fail(e, "preduce");
   } else if (h.tc) {
     if ((e = launch_prep_q(h, p, s)) != cudaSuccess) return cuda_fail(e, "prep_q");
     if ((e = launch_pgemm_tc(h, p, s)) != cudaSuccess) return cuda_fail(e, "pgemm_tc");
+    if (h.edt == DT_BF16 && (e = launch_rescale_tiny(h, p, s)) != cudaSuccess) return cuda_fail(e, "rescale");
   } else {
     if ((e = launch_qmax(h, p, s)) != cudaSuccess) return cuda_fail(e, "qmax");
     if ((e = launch_pgemm_simt(h, p, s)) != cudaSuccess) return cuda_fail(e, "pgemm");

@@ -51,7 +51,8 @@ struct Handle {
   StepTable tab{};
 
   int* d_err = nullptr;
-  float* d_scal_all = nullptr;  // [B*J*4] scaling words, zeroed every step
+  float* d_scal_all = nullptr;  // [B*J*kScalWords] scaling words, zeroed every step
+  size_t maps_bytes = 0;        // TMA maps of the callers' G and E (tensor engine), after the table
   int max_mtiles = 0, max_S = 0, max_C = 0, max_ntiles64 = 0, max_mtiles64 = 0;
   int max_kchunks = 0, max_ntiles128 = 0;
   void* tc_plan = nullptr;  // tensor-engine work lists (tc.cu)
@@ -69,6 +70,9 @@ cudaError_t launch_qmax(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_ingest_p(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_preduce(const Handle& h, const Plan& p, cudaStream_t s);
+size_t tc_ge_maps_bytes(const psgd_config* cfg);
+bool tc_encode_ge_maps(const Handle& h, const void* const* grads, void* const* errs, void* out);
+cudaError_t launch_rescale_tiny(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_decomp_tc(const Handle& h, const Plan& p, cudaStream_t s);
 void tc_free(Handle& h);

@@ -93,19 +93,24 @@ __global__ void __launch_bounds__(kT) k_gram(Plan p, int pass) {
   }
 }
 
-// G = sum_c Gpart[c] in chunk order, one element per thread, into slot C of Gpart.
-// grid = (ceil(rp*rp/256), B*J).
+// G = sum_c Gpart[c] into slot C of Gpart. Eight threads share an entry: thread k sums
+// the partials c = k, k+8, ... in order, then the eight sums are added in a fixed tree
+// order (deterministic). grid = (ceil(rp*rp/32), B*J).
 __global__ void __launch_bounds__(kT) k_gsum(Plan p, int pass) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if (pass_skipped(p, mt, pass)) return;
   const int rp = p.rp;
-  const int idx = blockIdx.x * kT + threadIdx.x;
-  if (idx >= rp * rp) return;
-  const float* src = mt.Gpart + idx;
+  const int idx = blockIdx.x * (kT / 8) + (threadIdx.x >> 3);
+  const int part = threadIdx.x & 7;
+  const bool live = idx < rp * rp;
+  const float* src = mt.Gpart + (live ? idx : 0);
   float s = 0.f;
-#pragma unroll 8
-  for (int c = 0; c < mt.C; ++c) s = __fadd_rn(s, __ldg(src + (size_t)c * rp * rp));
-  mt.Gpart[(size_t)mt.C * rp * rp + idx] = s;
+  if (live)
+    for (int c = part; c < mt.C; c += 8) s = __fadd_rn(s, __ldg(src + (size_t)c * rp * rp));
+  s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));
+  s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2));
+  s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 4));
+  if (live && part == 0) mt.Gpart[(size_t)mt.C * rp * rp + idx] = s;
 }
 
 // Load the summed Gram matrix (slot C of Gpart) into shared memory, plus its diagonal.
@@ -123,37 +128,95 @@ __device__ void load_gram(const MatMeta& mt, int r, int rp, float* G, int ldg, f
   __syncthreads();
 }
 
-// In-place right-looking Cholesky of the upper triangle of G (r x r, shared memory).
-// Pivot k is dead when it is <= dead_tol * diag0[k] (or not finite): row k of R
-// becomes e_k and column k is left out of the trailing update. The pivot ratio
-// pivot_k / diag0_k goes into ratio[k] (0 for dead columns).
+constexpr int NB = 16;  // panel width of the blocked factorisations
+
+// In-place blocked right-looking Cholesky of the upper triangle of G (r x r, shared
+// memory): G = R^T R. Pivot k is dead when it is <= dead_tol * diag0[k] (or not finite):
+// row k of R becomes e_k and column k takes no part in later updates. The pivot ratio
+// pivot_k / diag0_k goes into ratio[k] (0 for dead columns). Per 16-wide panel: warp 0
+// factors the diagonal block, the panel rows are solved column by column, then one
+// rank-16 update of the trailing matrix: three barriers a panel.
 __device__ void cholesky_smem(float* G, int ldg, int r, const float* diag0, float dead_tol,
                               float* ratio, int* dead) {
-  __shared__ float s_inv;
-  __shared__ int s_dead;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-  for (int k = 0; k < r; ++k) {
-    if (threadIdx.x == 0) {
-      const float d = G[k * ldg + k];
-      const bool bad = !(d > dead_tol * diag0[k]) || !isfinite(d) || !(diag0[k] > 0.f);
-      s_dead = bad;
-      dead[k] = bad;
-      ratio[k] = bad ? 0.f : d / diag0[k];
-      const float rkk = bad ? 1.f : sqrtf(d);
-      G[k * ldg + k] = rkk;
-      s_inv = 1.f / rkk;
+  for (int kb = 0; kb < r; kb += NB) {
+    const int nb = min(NB, r - kb);
+    if (warp == 0) {
+      for (int k = 0; k < nb; ++k) {
+        const int kk = kb + k;
+        float d = G[kk * ldg + kk];
+        const bool bad = !(d > dead_tol * diag0[kk]) || !isfinite(d) || !(diag0[kk] > 0.f);
+        const float rkk = bad ? 1.f : sqrtf(d);
+        const float inv = 1.f / rkk;
+        __syncwarp();
+        if (lane == 0) {
+          dead[kk] = bad;
+          ratio[kk] = bad ? 0.f : d / diag0[kk];
+          G[kk * ldg + kk] = rkk;
+        }
+        // row kk of the diagonal block
+        if (lane > k && lane < nb) G[kk * ldg + kb + lane] = bad ? 0.f : G[kk * ldg + kb + lane] * inv;
+        __syncwarp();
+        if (!bad) {
+          for (int q = lane; q < (nb - k - 1) * (nb - k - 1); q += 32) {
+            const int i = kb + k + 1 + q / (nb - k - 1), j = kb + k + 1 + q % (nb - k - 1);
+            if (j >= i) G[i * ldg + j] = fmaf(-G[kk * ldg + i], G[kk * ldg + j], G[i * ldg + j]);
+          }
+        }
+        __syncwarp();
+      }
     }
     __syncthreads();
-    const bool isdead = s_dead != 0;
-    const float inv = s_inv;
-    for (int j = k + 1 + threadIdx.x; j < r; j += blockDim.x)
-      G[k * ldg + j] = isdead ? 0.f : G[k * ldg + j] * inv;
+    // panel rows kb..kb+nb-1, columns j >= kb+nb: solve D^T x = g column by column
+    for (int j = kb + nb + threadIdx.x; j < r; j += blockDim.x) {
+      float x[NB];
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        if (k >= nb) break;
+        const int kk = kb + k;
+        float v = G[kk * ldg + j];
+        for (int q = 0; q < k; ++q) v = fmaf(-G[(kb + q) * ldg + kk], x[q], v);
+        x[k] = dead[kk] ? 0.f : v / G[kk * ldg + kk];
+        G[kk * ldg + j] = x[k];
+      }
+    }
     __syncthreads();
-    if (!isdead) {
-      for (int i = k + 1 + ty; i < r; i += 16) {
-        const float gki = G[k * ldg + i];
-        for (int j = k + 1 + tx; j < r; j += 16)
-          if (j >= i) G[i * ldg + j] = fmaf(-gki, G[k * ldg + j], G[i * ldg + j]);
+    // trailing update: G[i][j] -= sum_q R[kb+q][i] R[kb+q][j], kb+nb <= i <= j < r
+    for (int i = kb + nb + ty; i < r; i += 16)
+      for (int j = kb + nb + tx; j < r; j += 16) {
+        if (j < i) continue;
+        float v = G[i * ldg + j];
+        for (int q = 0; q < nb; ++q) v = fmaf(-G[(kb + q) * ldg + i], G[(kb + q) * ldg + j], v);
+        G[i * ldg + j] = v;
+      }
+    __syncthreads();
+  }
+}
+
+// X = R^-1 (upper triangular, r x r, shared memory) by blocked back substitution: for the
+// panels from the bottom, T = I - R[panel, below] X[below, :], then D X[panel, :] = T
+// with the panel's diagonal block D. Two barriers a panel. X must start as zero.
+__device__ void inverse_upper(const float* G, int ldg, int r, float* X) {
+  const int last = ((r - 1) / NB) * NB;
+  for (int kb = last; kb >= 0; kb -= NB) {
+    const int nb = min(NB, r - kb);
+    // T[i][j] for i in the panel, j >= kb (kept in X's panel rows)
+    for (int q = threadIdx.x; q < nb * (r - kb); q += blockDim.x) {
+      const int i = kb + q / (r - kb), j = kb + q % (r - kb);
+      float v = (i == j) ? 1.f : 0.f;
+      for (int l = kb + nb; l <= j; ++l) v = fmaf(-G[i * ldg + l], X[l * ldg + j], v);
+      X[i * ldg + j] = v;
+    }
+    __syncthreads();
+    // back substitution within the panel, one column per thread
+    for (int j = kb + threadIdx.x; j < r; j += blockDim.x) {
+      for (int k = nb - 1; k >= 0; --k) {
+        const int i = kb + k;
+        if (i > j) continue;
+        float v = X[i * ldg + j];
+        for (int q = k + 1; q < nb && kb + q <= j; ++q) v = fmaf(-G[i * ldg + kb + q], X[(kb + q) * ldg + j], v);
+        X[i * ldg + j] = v / G[i * ldg + i];
       }
     }
     __syncthreads();
@@ -218,23 +281,12 @@ __global__ void __launch_bounds__(kT) k_chol(Plan p, int pass) {
     s_maxr = mx; s_minr = mn; s_minratio = mr; s_ndead = nd;
   }
   __syncthreads();
-  // R^-1 (upper triangular) by right-looking elimination in shared memory: X = I, then
-  // for l = r-1 .. 0: X[l,:] /= R[l,l]; X[k,:] -= R[k,l] X[l,:] for k < l. When row l is
-  // finalised, every row below it has already contributed, so X[l,:] is row l of R^-1.
+  // R^-1 (upper triangular), blocked, in shared memory
   float* X = ratio + kMaxRank + kMaxRank;  // [kMaxRank][ldg], after dead[]
   for (int i = ty; i < r; i += 16)
-    for (int j = tx; j < r; j += 16) X[i * ldg + j] = (i == j) ? 1.f : 0.f;
+    for (int j = tx; j < r; j += 16) X[i * ldg + j] = 0.f;
   __syncthreads();
-  for (int l = r - 1; l >= 0; --l) {
-    const float inv = 1.f / G[l * ldg + l];
-    for (int j = l + threadIdx.x; j < r; j += blockDim.x) X[l * ldg + j] *= inv;
-    __syncthreads();
-    for (int k = ty; k < l; k += 16) {
-      const float gkl = G[k * ldg + l];
-      for (int j = l + tx; j < r; j += 16) X[k * ldg + j] = fmaf(-gkl, X[l * ldg + j], X[k * ldg + j]);
-    }
-    __syncthreads();
-  }
+  inverse_upper(G, ldg, r, X);
   float* Ri = mt.Rinv;
   for (int i = ty; i < r; i += 16)
     for (int j = tx; j < r; j += 16) Ri[i * rp + j] = (j >= i && !dead[j]) ? X[i * ldg + j] : 0.f;
@@ -324,7 +376,7 @@ cudaError_t launch_orth(const Handle& h, const Plan& p, cudaStream_t s) {
   const int BJ = p.B * p.J;
   for (int pass = 0; pass < kMaxPasses; ++pass) {
     k_gram<<<dim3(h.max_C, BJ), kT, 0, s>>>(p, pass);
-    k_gsum<<<dim3((p.rp * p.rp + kT - 1) / kT, BJ), kT, 0, s>>>(p, pass);
+    k_gsum<<<dim3((p.rp * p.rp + kT / 8 - 1) / (kT / 8), BJ), kT, 0, s>>>(p, pass);
     k_chol<<<BJ, kT, kCholSmem, s>>>(p, pass);
     k_apply<<<dim3(h.max_mtiles64, BJ), kT, 0, s>>>(p, pass);
     h.launches += 4;

@@ -37,7 +37,8 @@ struct MatMeta {
   uint16_t* psplit;   // [2*rp][mpad] 16-bit: P^ (scaled) hi rows then lo rows
   uint16_t* pdec;     // [mpad][3*rp] 16-bit: [P^hi | P^lo | P^hi] rows (decompress A)
   uint16_t* qdec;     // [npad][3*rp] 16-bit: [Q hi | Q hi | Q lo] rows (decompress B)
-  float* scal;        // [4]: 0 = max|P| bits, 1 = P^ scale, 2 = Q scale, 3 = spare
+  float* scal;        // [8] words, zeroed every step: max|M|, max|P|, max|Q| (state),
+                      // max|Q| (new), the exponent shift of a rescaled M scratch (int)
 };
 
 constexpr int kMaxPasses = 4;  // CholeskyQR passes at most (shifted ones included)
@@ -52,7 +53,11 @@ struct StepTable {
   const float* const* unc_in;    // [B*W] or null
   float* const* unc_out;         // [B] or null
   const float* inv_scale;        // [B]
+  const void* ge_maps;           // [B*J*W][2] TMA maps of G and E (tensor engine) or null
 };
+
+constexpr int kScalWords = 8;
+enum { SC_MAXM = 0, SC_MAXP = 1, SC_MAXQ = 2, SC_MAXQN = 3, SC_MSHIFT = 4 };
 
 struct Plan {
   int32_t B, J, W, r, rp;        // rp: r rounded up to a multiple of 16 (tensor path)

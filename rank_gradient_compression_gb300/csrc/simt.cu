@@ -183,13 +183,14 @@ __global__ void k_qreduce(Plan p, float qscale) {
   const int64_t total = mt.n * p.r;
   const float fw = (float)p.W;
   float* q = p.tab.q[blockIdx.y];
+  const int msh = reinterpret_cast<const int*>(mt.scal)[SC_MSHIFT];  // rescaled M: Q * 2^msh
   unsigned vmax = 0u;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = i / p.r, c = i % p.r;
     float acc = 0.f;
     for (int s = 0; s < mt.S; ++s) acc = __fadd_rn(acc, mt.Qpart[((size_t)s * mt.n + row) * p.rp + c]);
-    const float v = __fdiv_rn(acc * qscale, fw);
+    const float v = ldexpf(__fdiv_rn(acc * qscale, fw), -msh);
     q[i] = v;
     vmax = max(vmax, __float_as_uint(fabsf(v)));
   }

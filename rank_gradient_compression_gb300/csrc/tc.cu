@@ -247,12 +247,19 @@ struct GemmSmem {
   __device__ uint8_t* b(int s, uint32_t b_stage) const { return b0 + (size_t)s * b_stage; }
 };
 
+// A unit is left out for a skipped block, and, in the rerun over rescaled bf16
+// matrices (only_shifted), for every matrix whose M scratch was not rescaled.
+__device__ __forceinline__ bool unit_off(const Plan& p, const MatMeta& mt, int only_shifted) {
+  if (p.skip[mt.b]) return true;
+  return only_shifted && reinterpret_cast<const int*>(mt.scal)[SC_MSHIFT] == 0;
+}
+
 // MN_A = false: P GEMM (A = M tile K-major, unit = row tile x k-chunk).
 // MN_A = true:  Q GEMM (A = M^T tile MN-major, unit = column tile x m-slice).
 template <bool MN_A, bool BF16>
 __global__ void __launch_bounds__(192, 1)
 k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
-       int a_stages, uint32_t b_stage) {
+       int a_stages, uint32_t b_stage, int only_shifted) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   GemmSmem S{base, base + (size_t)a_stages * A_BYTES,
@@ -292,7 +299,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const Unit un = units[u];
         const MatMeta& mt = p.meta[un.t];
-        if (p.skip[mt.b]) continue;
+        if (unit_off(p, mt, only_shifted)) continue;
         const CUtensorMap* mm = maps + (size_t)un.t * NMAPS + (MN_A ? MAP_MQ : MAP_MP);
         const CUtensorMap* mb = maps + (size_t)un.t * NMAPS + (MN_A ? MAP_PS : MAP_QS);
         for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
@@ -334,7 +341,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
       bool ok = true;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const Unit un = units[u];
-        if (p.skip[p.meta[un.t].b]) continue;
+        if (unit_off(p, p.meta[un.t], only_shifted)) continue;
         const int acc = (int)(ju % NACC);
         ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
         if (!ok) break;
@@ -383,7 +390,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       const Unit un = units[u];
       const MatMeta& mt = p.meta[un.t];
-      if (p.skip[mt.b]) continue;
+      if (unit_off(p, mt, only_shifted)) continue;
       const int acc = (int)(ju % NACC);
       ok = mbar_wait(&sm.acc_full[acc], (ju / NACC) & 1, err);
       if (!ok) break;
@@ -429,14 +436,15 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
 }
 
 // ---------------------------------------------------------------- fused ingest + P GEMM
-// One HBM sweep of the gradients. A copy warp stages G_w and E_w tiles (128 rows x 64
-// columns, 128-byte rows) into a shared-memory ring with bulk copies. Ingest warps form
+// One HBM sweep of the gradients. A TMA warp stages G_w and E_w tiles (128 rows x 64
+// columns, 128-byte rows, zero-filled past the matrix edge) into a shared-memory ring. Ingest warps form
 // M_w = round_E(zero_nonfinite(G_w / s_b) + E_w) from the staged tiles, count nonfinite
 // entries per (block, worker), store M_w to its scratch, and write the same tile into
 // shared memory in the UMMA 128-byte-swizzle K-major layout. The MMA thread accumulates
 // M_w (Q_hi | Q_lo [| Q_lo2]) over every worker and k-block of the unit into TMEM. The
 // epilogue writes the unit's P partial sums.
-// Warps: 0 TMA (Q split tiles), 1 MMA, 2..5 epilogue, 6..13 ingest, 14 G/E copies.
+// Warps: 0 TMA (Q split tiles), 1 MMA, 2..5 epilogue, 6..13 ingest, 14 TMA (G/E tiles).
+// The ingest warps also record max|M| per matrix (for the bf16 subnormal rescale).
 constexpr int kIngWarps = 8;
 constexpr int GE_BYTES = 2 * A_BYTES;  // one staged G tile + one E tile
 constexpr int kMaxGeStages = 4;
@@ -527,37 +535,28 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
         mbar_wait(&sm.full_b[k % B_STAGES], (k / B_STAGES) & 1, err, 1u << 20);
     }
   } else if (warp == 14) {
-    // ------------------------------------------------------------ G/E bulk copies
-    TileIter ti;
-    ti.start(units, nunits);
-    uint32_t ig = 0;
-    bool ok = true;
-    while (ti.valid && ok) {
-      const MatMeta& mt = p.meta[ti.un.t];
-      const size_t slot = (size_t)ti.un.t * p.W + ti.w;
-      const TE* g = static_cast<const TE*>(p.tab.g[slot]);
-      const TE* e = static_cast<const TE*>(p.tab.e[slot]);
-      const int64_t row0 = (int64_t)ti.un.tile * BM, col0 = (int64_t)ti.kb * BK;
-      const int vr = mt.m - row0 < BM ? (int)(mt.m - row0) : BM;
-      const int vc = mt.n - col0 < BK ? (int)(mt.n - col0) : BK;
-      const uint32_t rowb = (uint32_t)vc * 2;
-      const int s = ig % ge_stages;
-      if (lane == 0) ok = mbar_wait(&sm.empty_ge[s], ((ig / ge_stages) & 1) ^ 1, err);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&sm.full_ge[s], 2u * (uint32_t)vr * rowb);
-      __syncwarp();
-      uint8_t* st = ge0 + (size_t)s * GE_BYTES;
-      for (int r = lane; r < vr; r += 32) {
-        bulk_load(st + r * 128, g + (row0 + r) * mt.n + col0, rowb, &sm.full_ge[s]);
-        bulk_load(st + A_BYTES + r * 128, e + (row0 + r) * mt.n + col0, rowb, &sm.full_ge[s]);
+    // ------------------------------------------------------------ TMA: G/E tiles
+    if (lane == 0) {
+      const CUtensorMap* gem = static_cast<const CUtensorMap*>(p.tab.ge_maps);
+      TileIter ti;
+      ti.start(units, nunits);
+      uint32_t ig = 0;
+      bool ok = true;
+      while (ti.valid && ok) {
+        const size_t slot = (size_t)ti.un.t * p.W + ti.w;
+        const int s = ig % ge_stages;
+        ok = mbar_wait(&sm.empty_ge[s], ((ig / ge_stages) & 1) ^ 1, err);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&sm.full_ge[s], GE_BYTES);
+        uint8_t* st = ge0 + (size_t)s * GE_BYTES;
+        tma_load_2d(st, gem + 2 * slot, ti.kb * BK, ti.un.tile * BM, &sm.full_ge[s]);
+        tma_load_2d(st + A_BYTES, gem + 2 * slot + 1, ti.kb * BK, ti.un.tile * BM, &sm.full_ge[s]);
+        ++ig;
+        ti.next(units, nunits, p.W);
       }
-      ++ig;
-      ti.next(units, nunits, p.W);
-    }
-    if (lane == 0)
       for (uint32_t k = (ig > (uint32_t)ge_stages ? ig - ge_stages : 0); k < ig; ++k)
         mbar_wait(&sm.full_ge[k % ge_stages], (k / ge_stages) & 1, err, 1u << 20);
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -662,6 +661,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
       TE* mo = static_cast<TE*>(mt.mscr) + (size_t)ti.w * mt.m * mt.n;
       const int64_t col = (int64_t)ti.kb * BK + cq * 8;
       int cnt = 0;
+      unsigned mmax = 0u;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int rl = rq + 32 * k;
@@ -679,6 +679,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
             const bool bad = !isfinite(x);
             cnt += bad;
             mx[i] = add_to<TE>(bad ? 0.0f : x, to_f(ex[i]));
+            mmax = max(mmax, __float_as_uint(fabsf(to_f(mx[i]))));
           }
           __stcg(reinterpret_cast<uint4*>(mo + row * mt.n + col), mv);
         }
@@ -686,9 +687,11 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
       }
       fence_proxy_async_smem();
       cnt = __reduce_add_sync(0xffffffffu, cnt);
+      mmax = __reduce_max_sync(0xffffffffu, mmax);
       if (lane == 0 && cnt)
         atomicAdd(reinterpret_cast<unsigned long long*>(p.counts + (size_t)mt.b * p.W + ti.w),
                   (unsigned long long)cnt);
+      if (lane == 0 && mmax) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + SC_MAXM, mmax);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&sm.full_a[sa]);
@@ -860,8 +863,11 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
       }
       epi_bar();  // staged tile complete (or an abort recorded)
       if (sm.abort_flag) break;
-      const TE* mbase = static_cast<const TE*>(mt.mscr);
+      TE* mbase = static_cast<TE*>(mt.mscr);
       const size_t wstride = (size_t)m * n;
+      // a rescaled bf16 M scratch holds M * 2^sh: undo it exactly, and restore M
+      const int msh = reinterpret_cast<const int*>(mt.scal)[SC_MSHIFT];
+      const float munscale = __uint_as_float((uint32_t)(127 - msh) << 23);
       // 128 rows x 16 segments of 8 columns; thread et takes segments et + 256 k
 #pragma unroll 1
       for (int k = 0; k < 8; k += 2) {
@@ -905,11 +911,18 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
             for (int kk = 0; kk < 8; ++kk) {
               if (!val[q] || w0 + kk >= p.W) continue;
               const TE* mx = reinterpret_cast<const TE*>(&mv[q][kk]);
-              __align__(16) TE ev[8];
+              __align__(16) TE ev[8], mr[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) ev[i] = add_to<TE>(to_f(mx[i]), -gv[q][i]);
+              for (int i = 0; i < 8; ++i) {
+                const float mval = to_f(mx[i]) * munscale;  // exact: a power of two
+                ev[i] = add_to<TE>(mval, -gv[q][i]);
+                mr[i] = from_f<TE>(mval);
+              }
               TE* ep = static_cast<TE*>(p.tab.e[(size_t)un.t * p.W + w0 + kk]) + rowk[q] * n + colk[q];
               __stcs(reinterpret_cast<uint4*>(ep), *reinterpret_cast<const uint4*>(ev));
+              if (msh != 0)
+                *reinterpret_cast<uint4*>(mbase + (size_t)(w0 + kk) * wstride + rowk[q] * n + colk[q]) =
+                    *reinterpret_cast<const uint4*>(mr);
             }
         }
       }
@@ -936,7 +949,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_map(CUtensorMap* out, void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-              const uint32_t* box) {
+              const uint32_t* box, bool swizzle = true) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[3], s[2];
@@ -944,8 +957,9 @@ bool make_map(CUtensorMap* out, void* base, int rank, const uint64_t* dims, cons
   for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
   for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
   CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, (cuuint32_t)rank, base, d, s, b, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -1012,6 +1026,62 @@ TcLayout tc_layout(const psgd_config* c) {
 }
 
 }  // namespace
+
+// Rescale the M scratch of bf16 matrices whose max|M| is below 2^-100 by 2^64 (exact:
+// bf16 has fp32's exponent range, so even subnormal values scale losslessly), and record
+// the shift. The tensor cores flush subnormal bf16 operands, and such matrices have most
+// of their mass there. grid = (chunks, B*J*W).
+__global__ void k_rescale_tiny(Plan p) {
+  const int t = blockIdx.y / p.W, w = blockIdx.y % p.W;
+  const MatMeta& mt = p.meta[t];
+  const unsigned mx = reinterpret_cast<const unsigned*>(mt.scal)[SC_MAXM];
+  if (p.skip[mt.b] || mx == 0u || mx >= 0x0D800000u) return;  // skipped, zero, or max|M| >= 2^-100
+  if (blockIdx.x == 0 && threadIdx.x == 0 && w == 0) reinterpret_cast<int*>(mt.scal)[SC_MSHIFT] = 64;
+  __nv_bfloat16* mo = static_cast<__nv_bfloat16*>(mt.mscr) + (size_t)w * mt.m * mt.n;
+  const int64_t total = mt.m * mt.n;
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < total;
+       i += (int64_t)gridDim.x * blockDim.x * 8) {
+    uint4 v = *reinterpret_cast<const uint4*>(mo + i);
+    __nv_bfloat16* x = reinterpret_cast<__nv_bfloat16*>(&v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = __float2bfloat16_rn(__bfloat162float(x[k]) * 0x1p64f);
+    *reinterpret_cast<uint4*>(mo + i) = v;
+  }
+}
+
+size_t tc_ge_maps_bytes(const psgd_config* cfg) {
+  if (cfg->err_dtype == PSGD_F32 || (cfg->flags & PSGD_FLAG_SIMT)) return 0;
+  return 2 * sizeof(CUtensorMap) * (size_t)cfg->num_blocks * cfg->mats_per_block * cfg->num_workers;
+}
+
+// TMA maps of each (matrix, worker) G and E: 2D {n, m}, 128 x 64 boxes, no swizzle.
+bool tc_encode_ge_maps(const Handle& h, const void* const* grads, void* const* errs, void* out) {
+  CUtensorMap* maps = static_cast<CUtensorMap*>(out);
+  for (int t = 0; t < h.B * h.J; ++t) {
+    const MatMeta& mt = h.meta[t];
+    uint64_t d[2] = {(uint64_t)mt.n, (uint64_t)mt.m}, st[1] = {(uint64_t)mt.n * 2};
+    uint32_t box[2] = {64, 128};
+    for (int w = 0; w < h.W; ++w) {
+      const size_t slot = (size_t)t * h.W + w;
+      if (!make_map(&maps[2 * slot], const_cast<void*>(grads[slot]), 2, d, st, box, false)) return false;
+      if (!make_map(&maps[2 * slot + 1], errs[slot], 2, d, st, box, false)) return false;
+    }
+  }
+  return true;
+}
+
+cudaError_t launch_rescale_tiny(const Handle& h, const Plan& p, cudaStream_t s) {
+  k_rescale_tiny<<<dim3(64, p.B * p.J * p.W), 256, 0, s>>>(p);
+  h.launches += 1;
+  const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
+  const int grid = std::min(tp->grid, tp->np);
+  const uint32_t bst = gemm_b_stage(h.edt, p.rp);
+  const int ast = gemm_a_stages(bst);
+  const size_t sm = gemm_smem(bst, ast);
+  k_gemm<false, true><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 1);
+  h.launches += 1;
+  return cudaGetLastError();
+}
 
 size_t tc_workspace_bytes(const psgd_config* cfg) {
   if (cfg->err_dtype == PSGD_F32 || (cfg->flags & PSGD_FLAG_SIMT)) return 0;
@@ -1145,8 +1215,8 @@ cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const uint32_t bst = gemm_b_stage(h.edt, p.rp);
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
-  if (h.edt == DT_BF16) k_gemm<false, true><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst);
-  else k_gemm<false, false><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst);
+  if (h.edt == DT_BF16) k_gemm<false, true><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0);
+  else k_gemm<false, false><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0);
   int64_t maxe = 0;
   for (const MatMeta& mt : h.meta) maxe = std::max<int64_t>(maxe, mt.m * p.rp);
   k_preduce<<<dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), 256, 0, s>>>(p, PCHUNK_KB);
@@ -1184,8 +1254,8 @@ cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const uint32_t bst = gemm_b_stage(h.edt, p.rp);
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
-  if (h.edt == DT_BF16) k_gemm<true, true><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst);
-  else k_gemm<true, false><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst);
+  if (h.edt == DT_BF16) k_gemm<true, true><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0);
+  else k_gemm<true, false><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0);
   h.launches += 2;
   return cudaGetLastError();
 }

@@ -122,6 +122,10 @@ class OracleRun:
         return dict(pool.map(one, self.blocks))
 
 
+def _tol(tol, kind, b, j):
+    return tol(kind, b, j) if callable(tol) else tol
+
+
 def compare_step(g: GpuRun, o_res: dict, o: OracleRun, tol=TOL, check_m=True):
     """Compare one step. Returns the worst (G-hat, E before storage, stored E) errors.
 
@@ -150,7 +154,7 @@ def compare_step(g: GpuRun, o_res: dict, o: OracleRun, tol=TOL, check_m=True):
             else:
                 eg = rel_err(gh, res.g_hat[j])
                 worst_g = max(worst_g, eg)
-                assert eg <= tol, f"block {b} matrix {j}: G-hat rel err {eg:.3e}"
+                assert eg <= _tol(tol, "g", b, j), f"block {b} matrix {j}: G-hat rel err {eg:.3e}"
             for w in range(wl.workers):
                 e_gpu = f64(g.errs[b][j][w])
                 e_ref = o.state[b].e[j][w]
@@ -170,15 +174,23 @@ def compare_step(g: GpuRun, o_res: dict, o: OracleRun, tol=TOL, check_m=True):
                 else:
                     ep = rel_err(pre_gpu, res.e_pre[j][w])
                     worst_pre = max(worst_pre, ep)
-                    assert ep <= tol, f"block {b} matrix {j} worker {w}: E (before storage) rel err {ep:.3e}"
+                    assert ep <= _tol(tol, "e", b, j), \
+                        f"block {b} matrix {j} worker {w}: E (before storage) rel err {ep:.3e}"
                     worst_st = max(worst_st, rel_err(e_gpu, e_ref))
         if wl.unc_len:
             uo = f64(g.unc_out[b])
-            eu = rel_err(uo, res.unc_out)
             if res.skip:
                 assert np.all(uo == 0)
             else:
-                assert eu <= 1e-6, f"block {b}: gains/biases rel err {eu:.3e}"
+                # The output is fp32, so the oracle's mean is compared after its own rounding
+                # to fp32. Terms below fp32's range (deep blocks of the stack) underflow on
+                # both sides; the floor allows one subnormal ulp per worker and entry.
+                ref = oracle.round_to_format(res.unc_out, "f32")
+                utol = TOL if callable(tol) else tol
+                du = float(np.linalg.norm(uo - ref))
+                floor = wl.workers * 2.0 ** -149 * np.sqrt(ref.size)
+                assert du <= utol * float(np.linalg.norm(ref)) + floor, \
+                    f"block {b}: gains/biases error {du:.3e} (|ref| {np.linalg.norm(ref):.3e})"
     return worst_g, worst_pre, worst_st
 
 
