@@ -34,9 +34,14 @@ __device__ __forceinline__ float p_scale(const MatMeta& mt) {
   return exp2f((float)(127 - max(ex, 1)));
 }
 
+// A pass runs only when every earlier pass ran and was not final. The scan stops at the
+// first final pass, so every entry it reads was written earlier in this same step; the
+// entries of passes that did not run hold values from older steps and are never read.
 __device__ __forceinline__ bool pass_skipped(const Plan& p, const MatMeta& mt, int pass) {
   if (p.skip[mt.b]) return true;
-  return pass > 0 && mt.ostate[(pass - 1) * 4 + 0] != 0;
+  for (int q = 0; q < pass; ++q)
+    if (mt.ostate[q * 4 + 0] != 0) return true;
+  return false;
 }
 
 // Gram partial sums over a row chunk: Gpart[c] = X_c^T X_c (rp x rp, r <= 128).
