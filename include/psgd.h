@@ -162,6 +162,39 @@ int32_t psgd_debug_orth(psgd_handle* h, int32_t b, int32_t j, int32_t* out, void
 /* Name of the GEMM engine this handle uses: "tcgen05" or "simt". */
 const char* psgd_engine(psgd_handle* h);
 
+/* Orthonormalise one fp32 matrix with scratch that is part of the library image.
+ *
+ * The pages have no counterpart of this call. It runs the adaptive shifted CholeskyQR
+ * passes that psgd_step applies to each P ("Cholesky-QR or Gram-Schmidt in fp32" on the
+ * reading card's PowerSGD list) for a single matrix, without a handle or a workspace,
+ * and it allocates no memory of any kind. It serves callers that hold one P but no
+ * handle and cannot allocate at that point: cudaMalloc/cudaFree synchronise the device
+ * and would stall the work queued around the call, and a process whose device memory is
+ * all handed out to a caching allocator or a fixed budget has none to give.
+ *
+ *   p     device, fp32, m x r row-major, dense (leading dimension r), 4-byte aligned.
+ *         Read only. Entries must be finite.
+ *   phat  device, fp32, m x r row-major, dense, 4-byte aligned; receives P^, an
+ *         orthonormal basis of span(P) (a numerically dependent column comes out 0).
+ *         Must not overlap p. Owned by the caller.
+ *   m, r  1 <= r <= m, m <= PSGD_STATIC_MAX_ROWS, r <= PSGD_STATIC_MAX_COLS. Larger
+ *         sizes return PSGD_EINVAL (with the limit in psgd_last_error) before any work.
+ *   stream  cudaStream_t (NULL: the legacy default stream); the call is asynchronous.
+ *
+ * Scratch: a fixed __device__ array of 16.1 MiB in each device's copy of the library
+ * module (Gram partial sums, R^-1, plan and pass state). The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress, with the device current)
+ * and keeps it; make that first call on each device before any stream capture begins.
+ * Every call clears the scratch words that must start at zero before it uses them.
+ * All calls share the one array: calls that overlap on the GPU (different streams of a
+ * device) race on it, so the caller must serialise them, e.g. on one stream.
+ * Errors: PSGD_EINVAL for bad arguments, PSGD_ECUDA for a CUDA error (message in
+ * psgd_last_error). */
+#define PSGD_STATIC_MAX_ROWS 16384
+#define PSGD_STATIC_MAX_COLS 128
+psgd_status psgd_orthonormalize_static(const float* p, float* phat, int64_t m, int32_t r,
+                                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,6 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Rows of the Q-GEMM slices and Gram chunks of the FFMA engine.
 constexpr int64_t kSliceRows = 512;
-constexpr int64_t kGramRows = 64;
 
 struct Layout {
   size_t total = 0;
@@ -109,6 +108,11 @@ Layout plan_layout(const psgd_config* c) {
 }
 
 }  // namespace
+
+// Error reporting for the entry points that live in other files.
+psgd_status report_error(psgd_status s, const std::string& msg) { return fail(s, msg); }
+psgd_status report_cuda_error(cudaError_t e, const char* where) { return cuda_fail(e, where); }
+
 }  // namespace psgd
 
 using namespace psgd;

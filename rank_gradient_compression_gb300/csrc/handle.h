@@ -77,4 +77,12 @@ cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_decomp_tc(const Handle& h, const Plan& p, cudaStream_t s);
 void tc_free(Handle& h);
 
+// Per-thread error message of the C ABI (api.cu), for entry points in other files.
+psgd_status report_error(psgd_status s, const std::string& msg);
+psgd_status report_cuda_error(cudaError_t e, const char* where);
+
+// The orthonormalisation passes for one matrix whose plan, pass state and scratch were
+// not laid out by psgd_init (orth.cu). C: Gram row chunks; mtiles64: 64-row tiles.
+cudaError_t launch_orth_one(const Plan& p, int C, int mtiles64, cudaStream_t s);
+
 }  // namespace psgd

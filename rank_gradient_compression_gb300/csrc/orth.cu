@@ -389,4 +389,17 @@ cudaError_t launch_orth(const Handle& h, const Plan& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_orth_one(const Plan& p, int C, int mtiles64, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_chol, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kCholSmem);
+  if (e != cudaSuccess) return e;
+  for (int pass = 0; pass < kMaxPasses; ++pass) {
+    k_gram<<<dim3(C, 1), kT, 0, s>>>(p, pass);
+    k_gsum<<<dim3((p.rp * p.rp + kT / 8 - 1) / (kT / 8), 1), kT, 0, s>>>(p, pass);
+    k_chol<<<1, kT, kCholSmem, s>>>(p, pass);
+    k_apply<<<dim3(mtiles64, 1), kT, 0, s>>>(p, pass);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace psgd

@@ -43,6 +43,7 @@ struct MatMeta {
 
 constexpr int kMaxPasses = 4;  // CholeskyQR passes at most (shifted ones included)
 constexpr int kMaxRank = 128;  // largest r of this build
+constexpr int64_t kGramRows = 64;  // rows per partial sum of the Gram matrix X^T X
 
 // Per-step device pointer tables (uploaded when they change).
 struct StepTable {

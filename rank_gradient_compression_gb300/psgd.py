@@ -23,7 +23,9 @@ DTYPE_CODE = {"f32": PSGD_F32, "f16": PSGD_F16, "bf16": PSGD_BF16}
 EXPORTS = ("psgd_workspace_size", "psgd_mask_offset", "psgd_mask_words", "psgd_init",
            "psgd_step", "psgd_check", "psgd_finalize", "psgd_strerror", "psgd_last_error",
            "psgd_debug_m", "psgd_debug_phat", "psgd_engine", "psgd_profile_begin",
-           "psgd_profile_end", "psgd_launch_count", "psgd_debug_orth")
+           "psgd_profile_end", "psgd_launch_count", "psgd_debug_orth",
+           "psgd_orthonormalize_static")
+PSGD_STATIC_MAX_ROWS, PSGD_STATIC_MAX_COLS = 16384, 128
 PSGD_MAX_ORTH_PASSES = 4
 PSGD_NUM_PHASES = 7
 PHASES = ("ingest", "skip_unc", "pgemm", "orth", "qgemm", "qreduce", "decomp")
@@ -91,6 +93,8 @@ def _load():
     lib.psgd_launch_count.argtypes = [c_void_p]
     lib.psgd_debug_orth.restype = c_int32
     lib.psgd_debug_orth.argtypes = [c_void_p, c_int32, c_int32, POINTER(c_int32), c_void_p]
+    lib.psgd_orthonormalize_static.restype = c_int32
+    lib.psgd_orthonormalize_static.argtypes = [c_void_p, c_void_p, c_int64, c_int32, c_void_p]
     return lib
 
 
@@ -164,6 +168,13 @@ def psgd_profile_end(handle: int):
 
 def psgd_launch_count(handle: int) -> int:
     return int(lib.psgd_launch_count(c_void_p(handle)))
+
+
+def psgd_orthonormalize_static(p_ptr: int, phat_ptr: int, m: int, r: int, stream: int):
+    """P^ <- orthonormal basis of span(P), P and P^ dense fp32 m x r on the device, with
+    the library's fixed scratch array (no allocation, no handle)."""
+    _check(lib.psgd_orthonormalize_static(c_void_p(p_ptr), c_void_p(phat_ptr), int(m), int(r),
+                                          c_void_p(stream)))
 
 
 def _ptrs(tensors):
