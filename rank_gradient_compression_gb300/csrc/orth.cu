@@ -110,191 +110,264 @@ __global__ void __launch_bounds__(kT) k_gsum(Plan p, int pass) {
   const bool live = idx < rp * rp;
   const float* src = mt.Gpart + (live ? idx : 0);
   float s = 0.f;
-  if (live)
+  if (live) {
+#pragma unroll 8
     for (int c = part; c < mt.C; c += 8) s = __fadd_rn(s, __ldg(src + (size_t)c * rp * rp));
+  }
   s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));
   s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2));
   s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 4));
   if (live && part == 0) mt.Gpart[(size_t)mt.C * rp * rp + idx] = s;
 }
 
-// Load the summed Gram matrix (slot C of Gpart) into shared memory, plus its diagonal.
-// Threads work on a 16 x 16 grid of (row, column) strides: no integer division.
-__device__ void load_gram(const MatMeta& mt, int r, int rp, float* G, int ldg, float* diag0,
-                          float shift) {
-  const float* src = mt.Gpart + (size_t)mt.C * rp * rp;
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-  for (int i = ty; i < r; i += 16)
-    for (int j = tx; j < r; j += 16) {
-      float s = src[i * rp + j];
-      if (i == j) { diag0[i] = s; s += shift; }
-      G[i * ldg + j] = s;
-    }
-  __syncthreads();
+// ---------------------------------------------------------------- Cholesky + R^-1
+// One CTA of kCholWarps warps per matrix. The Gram matrix lives in registers: warp w owns
+// the 8-row panel [8w, 8w + 8), and lane l holds columns l, l + 32, l + 64, l + 96 of
+// those rows. r <= 128, so every row has an owner.
+//
+// Factorisation G = R^T R (right-looking, by panels): the owner warp factors its panel
+// with shuffles only and writes the panel's 8 rows of R to shared memory; after one
+// block barrier every later warp subtracts the rank-8 update from its rows. Pivot k is
+// dead when it is <= dead_tol * diag0[k] (or not finite): row k of R becomes e_k and
+// column k takes no part in later updates.
+//
+// R^-1 (upper triangular) by the same panels from the bottom: the owner warp finishes
+// the rows of its panel, X_k = T_k / r_kk with T_k = e_k minus the contributions of the
+// rows below, and publishes them; the warps above subtract R[i][panel] X[panel].
+// Two block barriers per 8 rows in all, instead of one or two per row.
+constexpr int kCholWarps = 16;
+constexpr int kCholThreads = kCholWarps * 32;
+constexpr int kPanel = 8;
+static_assert(kCholWarps * kPanel >= kMaxRank, "every row needs an owner warp");
+constexpr int kRsLd = kMaxRank + 1;  // row stride of R in shared memory
+
+struct CholSmem {
+  float R[kMaxRank * kRsLd];           // rows of R as they are finished
+  float X[2][kPanel * kRsLd];          // published rows of R^-1 (ping-pong by panel)
+  float diag0[kMaxRank];               // diagonal of the unshifted Gram matrix
+  float ratio[kMaxRank];               // pivot / diag0 (0 for dead pivots)
+  int dead[kMaxRank];
+};
+
+// Select a[q] for a warp-uniform q in 0..3 without dynamic register indexing.
+__device__ __forceinline__ float pick4(const float a[4], int q) {
+  return q == 0 ? a[0] : q == 1 ? a[1] : q == 2 ? a[2] : a[3];
 }
 
-constexpr int NB = 16;  // panel width of the blocked factorisations
-
-// In-place blocked right-looking Cholesky of the upper triangle of G (r x r, shared
-// memory): G = R^T R. Pivot k is dead when it is <= dead_tol * diag0[k] (or not finite):
-// row k of R becomes e_k and column k takes no part in later updates. The pivot ratio
-// pivot_k / diag0_k goes into ratio[k] (0 for dead columns). Per 16-wide panel: warp 0
-// factors the diagonal block, the panel rows are solved column by column, then one
-// rank-16 update of the trailing matrix: three barriers a panel.
-__device__ void cholesky_smem(float* G, int ldg, int r, const float* diag0, float dead_tol,
-                              float* ratio, int* dead) {
+// Load rows [8 warp, 8 warp + 8) of the summed Gram matrix (slot C of Gpart) into
+// registers, zero outside r x r, and add `shift` to the diagonal. With record set, the
+// unshifted diagonal goes to diag0.
+__device__ __forceinline__ void load_gram_regs(const MatMeta& mt, int r, int rp, float a[kPanel][4],
+                                               float shift, CholSmem& S, bool record) {
+  const float* src = mt.Gpart + (size_t)mt.C * rp * rp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-  for (int kb = 0; kb < r; kb += NB) {
-    const int nb = min(NB, r - kb);
-    if (warp == 0) {
-      for (int k = 0; k < nb; ++k) {
-        const int kk = kb + k;
-        float d = G[kk * ldg + kk];
-        const bool bad = !(d > dead_tol * diag0[kk]) || !isfinite(d) || !(diag0[kk] > 0.f);
-        const float rkk = bad ? 1.f : sqrtf(d);
-        const float inv = 1.f / rkk;
-        __syncwarp();
-        if (lane == 0) {
-          dead[kk] = bad;
-          ratio[kk] = bad ? 0.f : d / diag0[kk];
-          G[kk * ldg + kk] = rkk;
-        }
-        // row kk of the diagonal block
-        if (lane > k && lane < nb) G[kk * ldg + kb + lane] = bad ? 0.f : G[kk * ldg + kb + lane] * inv;
-        __syncwarp();
-        if (!bad) {
-          for (int q = lane; q < (nb - k - 1) * (nb - k - 1); q += 32) {
-            const int i = kb + k + 1 + q / (nb - k - 1), j = kb + k + 1 + q % (nb - k - 1);
-            if (j >= i) G[i * ldg + j] = fmaf(-G[kk * ldg + i], G[kk * ldg + j], G[i * ldg + j]);
-          }
-        }
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-    // panel rows kb..kb+nb-1, columns j >= kb+nb: solve D^T x = g column by column
-    for (int j = kb + nb + threadIdx.x; j < r; j += blockDim.x) {
-      float x[NB];
 #pragma unroll
-      for (int k = 0; k < NB; ++k) {
-        if (k >= nb) break;
-        const int kk = kb + k;
-        float v = G[kk * ldg + j];
-        for (int q = 0; q < k; ++q) v = fmaf(-G[(kb + q) * ldg + kk], x[q], v);
-        x[k] = dead[kk] ? 0.f : v / G[kk * ldg + kk];
-        G[kk * ldg + j] = x[k];
+  for (int t = 0; t < kPanel; ++t) {
+    const int i = warp * kPanel + t;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = lane + 32 * q;
+      float v = (i < r && j < r) ? src[(size_t)i * rp + j] : 0.f;
+      if (i == j && i < r) {
+        if (record) S.diag0[i] = v;
+        v += shift;
       }
+      a[t][q] = v;
     }
-    __syncthreads();
-    // trailing update: G[i][j] -= sum_q R[kb+q][i] R[kb+q][j], kb+nb <= i <= j < r
-    for (int i = kb + nb + ty; i < r; i += 16)
-      for (int j = kb + nb + tx; j < r; j += 16) {
-        if (j < i) continue;
-        float v = G[i * ldg + j];
-        for (int q = 0; q < nb; ++q) v = fmaf(-G[(kb + q) * ldg + i], G[(kb + q) * ldg + j], v);
-        G[i * ldg + j] = v;
-      }
-    __syncthreads();
   }
 }
 
-// X = R^-1 (upper triangular, r x r, shared memory) by blocked back substitution: for the
-// panels from the bottom, T = I - R[panel, below] X[below, :], then D X[panel, :] = T
-// with the panel's diagonal block D. Two barriers a panel. X must start as zero.
-__device__ void inverse_upper(const float* G, int ldg, int r, float* X) {
-  const int last = ((r - 1) / NB) * NB;
-  for (int kb = last; kb >= 0; kb -= NB) {
-    const int nb = min(NB, r - kb);
-    // T[i][j] for i in the panel, j >= kb (kept in X's panel rows)
-    for (int q = threadIdx.x; q < nb * (r - kb); q += blockDim.x) {
-      const int i = kb + q / (r - kb), j = kb + q % (r - kb);
-      float v = (i == j) ? 1.f : 0.f;
-      for (int l = kb + nb; l <= j; ++l) v = fmaf(-G[i * ldg + l], X[l * ldg + j], v);
-      X[i * ldg + j] = v;
+// Factor the registers' panels in place (rows of R) and fill S.R, S.dead, S.ratio.
+__device__ void cholesky_panels(float a[kPanel][4], int r, float dead_tol, CholSmem& S) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int npan = (r + kPanel - 1) / kPanel;
+  for (int pn = 0; pn < npan; ++pn) {
+    const int k0 = pn * kPanel;
+    if (warp == pn) {
+      const int qk = k0 >> 5;  // column group of this panel (panels never straddle 32)
+#pragma unroll
+      for (int t = 0; t < kPanel; ++t) {
+        const int k = k0 + t;
+        if (k < r) {
+          const float d = __shfl_sync(0xffffffffu, pick4(a[t], qk), k & 31);
+          const float d0 = S.diag0[k];
+          const bool bad = !(d > dead_tol * d0) || !isfinite(d) || !(d0 > 0.f);
+          const float rkk = bad ? 1.f : sqrtf(d);
+          const float inv = 1.f / rkk;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int j = lane + 32 * q;
+            a[t][q] = j < k ? 0.f : (j == k ? rkk : (bad ? 0.f : a[t][q] * inv));
+          }
+          if (lane == 0) {
+            S.dead[k] = bad;
+            S.ratio[k] = bad ? 0.f : d / d0;
+          }
+          // the rows below k in this panel
+#pragma unroll
+          for (int t2 = t + 1; t2 < kPanel; ++t2) {
+            const float c = __shfl_sync(0xffffffffu, pick4(a[t], qk), (k0 + t2) & 31);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) a[t2][q] = fmaf(-c, a[t][q], a[t2][q]);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kPanel; ++t)
+        if (k0 + t < r) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) S.R[(k0 + t) * kRsLd + lane + 32 * q] = a[t][q];
+        }
     }
     __syncthreads();
-    // back substitution within the panel, one column per thread
-    for (int j = kb + threadIdx.x; j < r; j += blockDim.x) {
-      for (int k = nb - 1; k >= 0; --k) {
-        const int i = kb + k;
-        if (i > j) continue;
-        float v = X[i * ldg + j];
-        for (int q = k + 1; q < nb && kb + q <= j; ++q) v = fmaf(-G[i * ldg + kb + q], X[(kb + q) * ldg + j], v);
-        X[i * ldg + j] = v / G[i * ldg + i];
+    if (warp > pn) {
+      const int kend = min(kPanel, r - k0);
+      const int i0 = warp * kPanel;
+#pragma unroll
+      for (int pp = 0; pp < kPanel; ++pp) {
+        if (pp >= kend) break;
+        const float* Rk = S.R + (k0 + pp) * kRsLd;
+        float rj[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) rj[q] = Rk[lane + 32 * q];
+#pragma unroll
+        for (int t = 0; t < kPanel; ++t) {  // rows i >= r hold zeros and stay unused
+          const float c = Rk[i0 + t];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) a[t][q] = fmaf(-c, rj[q], a[t][q]);
+        }
       }
     }
+  }
+}
+
+// R^-1 into the registers (rows of this warp's panel), from S.R.
+__device__ void inverse_panels(float a[kPanel][4], int r, CholSmem& S) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int t = 0; t < kPanel; ++t)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) a[t][q] = (warp * kPanel + t == lane + 32 * q) ? 1.f : 0.f;
+  const int npan = (r + kPanel - 1) / kPanel;
+  for (int pn = npan - 1; pn >= 0; --pn) {
+    const int k0 = pn * kPanel;
+    float* Xp = S.X[pn & 1];
+    if (warp == pn) {
+#pragma unroll
+      for (int t = kPanel - 1; t >= 0; --t) {
+        const int k = k0 + t;
+        if (k < r) {
+          const float inv = 1.f / S.R[k * kRsLd + k];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) a[t][q] *= inv;
+#pragma unroll
+          for (int t2 = 0; t2 < t; ++t2) {
+            const float c = S.R[(k0 + t2) * kRsLd + k];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) a[t2][q] = fmaf(-c, a[t][q], a[t2][q]);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kPanel; ++t)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) Xp[t * kRsLd + lane + 32 * q] = a[t][q];
+    }
     __syncthreads();
+    if (warp < pn) {
+      const int kend = min(kPanel, r - k0);
+      const float* Ri = S.R + (warp * kPanel) * kRsLd + k0;
+#pragma unroll
+      for (int pp = 0; pp < kPanel; ++pp) {
+        if (pp >= kend) break;
+        float xj[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) xj[q] = Xp[pp * kRsLd + lane + 32 * q];
+#pragma unroll
+        for (int t = 0; t < kPanel; ++t) {
+          const float c = Ri[t * kRsLd + pp];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) a[t][q] = fmaf(-c, xj[q], a[t][q]);
+        }
+      }
+    }
   }
 }
 
 // One CTA per matrix: factor the Gram matrix of this pass, decide shift/final, write R^-1.
-__global__ void __launch_bounds__(kT) k_chol(Plan p, int pass) {
+__global__ void __launch_bounds__(kCholThreads) k_chol(Plan p, int pass) {
   const MatMeta& mt = p.meta[blockIdx.x];
   if (pass_skipped(p, mt, pass)) return;
-  const int r = p.r, rp = p.rp, ldg = kMaxRank + 1;
-  extern __shared__ float sm[];
-  float* G = sm;                          // [kMaxRank][kMaxRank + 1]
-  float* diag0 = G + kMaxRank * ldg;      // [kMaxRank]
-  float* ratio = diag0 + kMaxRank;        // [kMaxRank]
-  int* dead = reinterpret_cast<int*>(ratio + kMaxRank);  // [kMaxRank]; R^-1 work after it
-  __shared__ float s_trace, s_maxr, s_minr, s_minratio;
-  __shared__ int s_ndead, s_retry;
+  const int r = p.r, rp = p.rp;
+  extern __shared__ __align__(16) unsigned char chol_smem[];
+  CholSmem& S = *reinterpret_cast<CholSmem*>(chol_smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool last = pass == kMaxPasses - 1;
   int* st = mt.ostate + pass * 4;
   const int src = pass == 0 ? 0 : mt.ostate[(pass - 1) * 4 + 1];
 
-  load_gram(mt, r, rp, G, ldg, diag0, 0.f);
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int k = 0; k < r; ++k) t += diag0[k];
-    s_trace = t;
-  }
+  float a[kPanel][4];
+  load_gram_regs(mt, r, rp, a, 0.f, S, true);
   __syncthreads();
-  const float trace = s_trace;
+  float trace = 0.f;
+  for (int k = 0; k < r; ++k) trace += S.diag0[k];  // same order in every thread
   bool shifted = false;
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
   if (!(trace > 0.f) || !isfinite(trace)) {
-    for (int k = threadIdx.x; k < r; k += blockDim.x) dead[k] = 1;
-    for (int i = ty; i < r; i += 16)
-      for (int j = tx; j < r; j += 16) G[i * ldg + j] = (i == j) ? 1.f : 0.f;
+    for (int k = threadIdx.x; k < r; k += blockDim.x) { S.dead[k] = 1; S.ratio[k] = 0.f; }
+    for (int idx = threadIdx.x; idx < r * kRsLd; idx += blockDim.x) {
+      const int i = idx / kRsLd, j = idx - i * kRsLd;
+      S.R[idx] = (i == j) ? 1.f : 0.f;
+    }
     __syncthreads();
   } else {
-    cholesky_smem(G, ldg, r, diag0, last ? 0x1p-40f : 0x1p-16f, ratio, dead);
-    if (threadIdx.x == 0) {
-      int nd = 0;
-      for (int k = 0; k < r; ++k) nd += dead[k];
-      s_retry = (nd > 0 && !last) ? 1 : 0;
-    }
+    cholesky_panels(a, r, last ? 0x1p-40f : 0x1p-16f, S);
     __syncthreads();
-    if (s_retry) {
+    int nd = 0;
+    for (int k = lane; k < r; k += 32) nd += S.dead[k];
+    nd = __reduce_add_sync(0xffffffffu, nd);  // every warp computes the same count
+    if (nd > 0 && !last) {
       shifted = true;
       const float shift = 0x1p-20f * sqrtf((float)mt.m) * trace;
-      load_gram(mt, r, rp, G, ldg, diag0, shift);
-      cholesky_smem(G, ldg, r, diag0, 0x1p-40f, ratio, dead);
+      load_gram_regs(mt, r, rp, a, shift, S, false);
+      __syncthreads();
+      cholesky_panels(a, r, 0x1p-40f, S);
+      __syncthreads();
     }
   }
-  // statistics of the factor
-  if (threadIdx.x == 0) {
+  // statistics of the factor: warp 0 reduces over the pivots
+  __shared__ float s_maxr, s_minr, s_minratio;
+  __shared__ int s_ndead;
+  if (warp == 0) {
     float mx = 0.f, mn = 3.4e38f, mr = 1.f;
     int nd = 0;
-    for (int k = 0; k < r; ++k) {
-      if (dead[k]) { ++nd; continue; }
-      const float d = G[k * ldg + k];
-      mx = fmaxf(mx, d); mn = fminf(mn, d); mr = fminf(mr, ratio[k]);
+    for (int k = lane; k < r; k += 32) {
+      if (S.dead[k]) { ++nd; continue; }
+      const float d = S.R[k * kRsLd + k];
+      mx = fmaxf(mx, d); mn = fminf(mn, d); mr = fminf(mr, S.ratio[k]);
     }
-    s_maxr = mx; s_minr = mn; s_minratio = mr; s_ndead = nd;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mr = fminf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+    }
+    nd = __reduce_add_sync(0xffffffffu, nd);
+    if (lane == 0) { s_maxr = mx; s_minr = mn; s_minratio = mr; s_ndead = nd; }
   }
-  __syncthreads();
-  // R^-1 (upper triangular), blocked, in shared memory
-  float* X = ratio + kMaxRank + kMaxRank;  // [kMaxRank][ldg], after dead[]
-  for (int i = ty; i < r; i += 16)
-    for (int j = tx; j < r; j += 16) X[i * ldg + j] = 0.f;
-  __syncthreads();
-  inverse_upper(G, ldg, r, X);
+  inverse_panels(a, r, S);
+  // R^-1 to global, dead columns zeroed
   float* Ri = mt.Rinv;
-  for (int i = ty; i < r; i += 16)
-    for (int j = tx; j < r; j += 16) Ri[i * rp + j] = (j >= i && !dead[j]) ? X[i * ldg + j] : 0.f;
+#pragma unroll
+  for (int t = 0; t < kPanel; ++t) {
+    const int i = warp * kPanel + t;
+    if (i < r) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = lane + 32 * q;
+        if (j < r) Ri[i * rp + j] = (j >= i && !S.dead[j]) ? a[t][q] : 0.f;
+      }
+    }
+  }
   if (threadIdx.x == 0) {
     const bool nearly_orth = !shifted && s_ndead == 0 && s_minratio >= 0.5f &&
                              s_maxr <= 2.f * s_minr;
@@ -372,7 +445,7 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   }
 }
 
-constexpr size_t kCholSmem = 2 * (size_t)kMaxRank * (kMaxRank + 1) * 4 + 3 * kMaxRank * 4;
+constexpr size_t kCholSmem = sizeof(CholSmem);
 
 }  // namespace
 
@@ -382,7 +455,7 @@ cudaError_t launch_orth(const Handle& h, const Plan& p, cudaStream_t s) {
   for (int pass = 0; pass < kMaxPasses; ++pass) {
     k_gram<<<dim3(h.max_C, BJ), kT, 0, s>>>(p, pass);
     k_gsum<<<dim3((p.rp * p.rp + kT / 8 - 1) / (kT / 8), BJ), kT, 0, s>>>(p, pass);
-    k_chol<<<BJ, kT, kCholSmem, s>>>(p, pass);
+    k_chol<<<BJ, kCholThreads, kCholSmem, s>>>(p, pass);
     k_apply<<<dim3(h.max_mtiles64, BJ), kT, 0, s>>>(p, pass);
     h.launches += 4;
   }
@@ -396,7 +469,7 @@ cudaError_t launch_orth_one(const Plan& p, int C, int mtiles64, cudaStream_t s) 
   for (int pass = 0; pass < kMaxPasses; ++pass) {
     k_gram<<<dim3(C, 1), kT, 0, s>>>(p, pass);
     k_gsum<<<dim3((p.rp * p.rp + kT / 8 - 1) / (kT / 8), 1), kT, 0, s>>>(p, pass);
-    k_chol<<<1, kT, kCholSmem, s>>>(p, pass);
+    k_chol<<<1, kCholThreads, kCholSmem, s>>>(p, pass);
     k_apply<<<dim3(mtiles64, 1), kT, 0, s>>>(p, pass);
   }
   return cudaGetLastError();

@@ -177,25 +177,30 @@ __global__ void __launch_bounds__(kT) k_qgemm(Plan p) {
 
 // Q = (sum_s Qpart[s]) * qscale / W in slice order -> the caller's fp32 Q state (n x r),
 // and max|Q| -> scal[3]. qscale undoes the power-of-two scale of a split P^ (exact).
-__global__ void k_qreduce(Plan p, float qscale) {
+__global__ void __launch_bounds__(256) k_qreduce(Plan p, float qscale) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
-  const int64_t total = mt.n * p.r;
+  // one warp per row of Q; lane covers columns lane, lane + 32, ...
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   const float fw = (float)p.W;
   float* q = p.tab.q[blockIdx.y];
   const int msh = reinterpret_cast<const int*>(mt.scal)[SC_MSHIFT];  // rescaled M: Q * 2^msh
+  const size_t stride = (size_t)mt.n * p.rp;  // one slice of Qpart
   unsigned vmax = 0u;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = i / p.r, c = i % p.r;
-    float acc = 0.f;
-    for (int s = 0; s < mt.S; ++s) acc = __fadd_rn(acc, mt.Qpart[((size_t)s * mt.n + row) * p.rp + c]);
-    const float v = ldexpf(__fdiv_rn(acc * qscale, fw), -msh);
-    q[i] = v;
-    vmax = max(vmax, __float_as_uint(fabsf(v)));
+  if (row < mt.n) {
+    for (int c = lane; c < p.r; c += 32) {
+      const float* src = mt.Qpart + (size_t)row * p.rp + c;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int s = 0; s < mt.S; ++s) acc = __fadd_rn(acc, src[(size_t)s * stride]);
+      const float v = ldexpf(__fdiv_rn(acc * qscale, fw), -msh);
+      q[row * p.r + c] = v;
+      vmax = max(vmax, __float_as_uint(fabsf(v)));
+    }
   }
   vmax = __reduce_max_sync(0xffffffffu, vmax);
-  if ((threadIdx.x & 31) == 0 && vmax) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 3, vmax);
+  if (lane == 0 && vmax) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 3, vmax);
 }
 
 template <typename TE> struct V4;
@@ -304,7 +309,9 @@ cudaError_t launch_qgemm_simt(const Handle& h, const Plan& p, cudaStream_t s) {
 }
 
 cudaError_t launch_qreduce(const Handle& h, const Plan& p, cudaStream_t s) {
-  dim3 grid(64, p.B * p.J);
+  int64_t max_n = 0;
+  for (const MatMeta& mt : h.meta) max_n = std::max<int64_t>(max_n, mt.n);
+  dim3 grid((unsigned)((max_n + 7) / 8), p.B * p.J);
   k_qreduce<<<grid, 256, 0, s>>>(p, h.tc ? 0x1p-14f : 1.0f);
   h.launches += 1;
   return cudaGetLastError();

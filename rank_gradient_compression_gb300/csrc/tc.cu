@@ -41,6 +41,17 @@ constexpr int BK = 64;                 // K per stage (one 128-byte swizzle span
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_STAGES = 2;
 constexpr int PCHUNK_KB = 4;           // P GEMM: k-blocks of 64 columns per unit
+// Accumulator segments. The tensor cores' fp32 accumulation loses about 2^-24 of the
+// accumulator per chained MMA, and those losses add up (they do not cancel like
+// round-to-nearest errors). So no accumulator chains more than a few MMAs: after each
+// segment of (k-block, worker) steps the epilogue adds the accumulator into a running sum
+// with round-to-nearest fp32 adds. The separate GEMMs keep that sum in registers and
+// close a segment every kGemmSegSteps steps (16 MMAs per column set). The fused ingest kernel keeps it
+// in TMEM, next to two accumulators of rp columns: there each K step issues one MMA per
+// split term of Q into the same accumulator, and a segment of kIngSegSteps steps chains
+// 8 (fp16) or 12 (bf16) MMAs per step.
+constexpr int kGemmSegSteps = 4;
+constexpr int kIngSegSteps = 2;
 constexpr int QSLICE_ROWS = 512;       // Q GEMM: rows of m per unit (matches Qpart slices)
 constexpr int DEC_NT = 128;            // G^ tile columns
 constexpr int NMAPS = 6;               // tensor maps per matrix
@@ -112,22 +123,43 @@ __global__ void k_qmax(Plan p) {
 
 // qsplit[terms*rp][n]: rows k*rp + c hold term k of Q[:, c] * 2^e (k = 0 hi, then mid
 // for bf16, then lo); e puts max|Q| * 2^e in [2^14, 2^15). Padding rows are 0.
-// grid = (ceil(n/256), rp, B*J).
+// A block stages 32 rows of Q (n x r row-major: one contiguous run) in shared memory,
+// then writes 8 consecutive entries of one qsplit row per 16-byte store (n is a multiple
+// of 8, so a group of 8 is wholly inside or outside the matrix). grid = (ceil(n/32), B*J).
 template <typename T>
-__global__ void k_qsplit(Plan p) {
-  const MatMeta& mt = p.meta[blockIdx.z];
-  const int c = blockIdx.y, rp = p.rp;
-  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= mt.n) return;
+__global__ void __launch_bounds__(256) k_qsplit(Plan p) {
+  const MatMeta& mt = p.meta[blockIdx.y];
+  const int64_t j0 = (int64_t)blockIdx.x * 32;
+  if (j0 >= mt.n) return;
+  const int r = p.r, rp = p.rp;
+  __shared__ float xs[32][kMaxRank + 1];
+  const float* q = p.tab.q[blockIdx.y] + j0 * r;
+  const int64_t left = mt.n - j0;
+  const int nrows = left < 32 ? (int)left : 32;
   const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[2]);
-  uint16_t t0 = 0, t1 = 0, t2 = 0;
-  if (c < p.r) {
-    const float x = ldexpf(p.tab.q[blockIdx.z][j * p.r + c], e);
-    if (nterms<T>() == 3) split3<T>(x, t0, t1, t2); else split2<T>(x, t0, t1);
+  for (int idx = threadIdx.x; idx < nrows * r; idx += blockDim.x) {
+    const int rr = idx / r, c = idx - rr * r;
+    xs[rr][c] = ldexpf(q[idx], e);
   }
-  mt.qsplit[(size_t)c * mt.n + j] = t0;
-  mt.qsplit[(size_t)(rp + c) * mt.n + j] = t1;
-  if (nterms<T>() == 3) mt.qsplit[(size_t)(2 * rp + c) * mt.n + j] = t2;
+  __syncthreads();
+  for (int it = threadIdx.x; it < rp * 4; it += blockDim.x) {
+    const int c = it >> 2, g = it & 3;
+    if (8 * g >= nrows) continue;
+    __align__(16) uint16_t t0[8], t1[8], t2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      t0[i] = t1[i] = t2[i] = 0;
+      if (c < r) {
+        if (nterms<T>() == 3) split3<T>(xs[8 * g + i][c], t0[i], t1[i], t2[i]);
+        else split2<T>(xs[8 * g + i][c], t0[i], t1[i]);
+      }
+    }
+    const size_t col = (size_t)j0 + 8 * g;
+    *reinterpret_cast<uint4*>(mt.qsplit + (size_t)c * mt.n + col) = *reinterpret_cast<const uint4*>(t0);
+    *reinterpret_cast<uint4*>(mt.qsplit + (size_t)(rp + c) * mt.n + col) = *reinterpret_cast<const uint4*>(t1);
+    if (nterms<T>() == 3)
+      *reinterpret_cast<uint4*>(mt.qsplit + (size_t)(2 * rp + c) * mt.n + col) = *reinterpret_cast<const uint4*>(t2);
+  }
 }
 
 // P = (sum_c Ppart[c]) / W in chunk order, plus max|P| -> scal[1]. P keeps the power-of-
@@ -144,6 +176,7 @@ __global__ void k_preduce(Plan p, int pchunk_kb) {
   if (i < mt.m * rp) {
     const int kch = (int)(((mt.n + 63) / 64 + pchunk_kb - 1) / pchunk_kb);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (int c = 0; c < kch; ++c) {
       const float4 v = __ldg(reinterpret_cast<const float4*>(mt.Ppart + (size_t)c * mpad * rp + i));
       acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
@@ -163,66 +196,84 @@ __global__ void k_preduce(Plan p, int pchunk_kb) {
 
 // From P^ (m x rp fp32, |entries| <= 1): psplit[terms*rp][mpad] = the terms of
 // (P^ * 2^14)^T in type T (the type of M), and pdec[mpad][3 kp] = [hi | lo | hi] in fp16
-// for the decompression.
-// grid = (ceil(mpad/128), B*J), block 128: thread = row.
+// for the decompression. A block stages 32 rows of P^ (one contiguous run) in shared
+// memory; pdec rows are written 8 columns per 16-byte store, psplit rows 8 rows of P^
+// per 16-byte store. grid = (mpad / 32, B*J).
 template <typename T>
-__global__ void k_psplit(Plan p, int kp) {
+__global__ void __launch_bounds__(256) k_psplit(Plan p, int kp) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
   const int64_t mpad = (mt.m + 127) / 128 * 128;
-  const int64_t row = (int64_t)blockIdx.x * 128 + threadIdx.x;
-  if (row >= mpad) return;
-  const int rp = p.rp;
-  uint16_t* pd = mt.pdec + (size_t)row * 3 * kp;
-  for (int c0 = 0; c0 < kp; c0 += 8) {
-    float x[8];
-    if (row < mt.m && c0 < rp) {
-      const float4 a = *reinterpret_cast<const float4*>(mt.Phat + row * rp + c0);
-      const float4 b = *reinterpret_cast<const float4*>(mt.Phat + row * rp + c0 + 4);
-      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = 0.f;
-    }
+  const int64_t row0 = (int64_t)blockIdx.x * 32;
+  if (row0 >= mpad) return;
+  const int r = p.r, rp = p.rp;
+  __shared__ float xs[32][kMaxRank + 1];
+  const int64_t left = mt.m - row0;
+  const int nrows = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
+  const float* src = mt.Phat + row0 * rp;
+  for (int idx = threadIdx.x; idx < 32 * rp; idx += blockDim.x) {
+    const int rr = idx / rp, c = idx - rr * rp;
+    xs[rr][c] = (rr < nrows && c < r) ? src[idx] * 16384.0f : 0.f;  // * 2^14, exact
+  }
+  __syncthreads();
+  // pdec rows: [hi | lo | hi], kp / 8 groups of 8 columns per segment
+  const int gpr = kp / 8;
+  for (int it = threadIdx.x; it < 32 * gpr; it += blockDim.x) {
+    const int rr = it / gpr, c0 = (it - rr * gpr) * 8;
     __align__(16) uint16_t hh[8], hl[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float xs = (c0 + i < p.r) ? x[i] * 16384.0f : 0.f;  // * 2^14, exact
-      uint16_t t0, t1, t2 = 0;
-      if (nterms<T>() == 3) split3<T>(xs, t0, t1, t2); else split2<T>(xs, t0, t1);
-      split2<__half>(xs, hh[i], hl[i]);
-      const int c = c0 + i;
-      if (c < rp) {
-        mt.psplit[(size_t)c * mpad + row] = t0;
-        mt.psplit[(size_t)(rp + c) * mpad + row] = t1;
-        if (nterms<T>() == 3) mt.psplit[(size_t)(2 * rp + c) * mpad + row] = t2;
-      }
-    }
+    for (int i = 0; i < 8; ++i) split2<__half>(c0 + i < rp ? xs[rr][c0 + i] : 0.f, hh[i], hl[i]);
+    uint16_t* pd = mt.pdec + (size_t)(row0 + rr) * 3 * kp;
     *reinterpret_cast<uint4*>(pd + c0) = *reinterpret_cast<const uint4*>(hh);
     *reinterpret_cast<uint4*>(pd + kp + c0) = *reinterpret_cast<const uint4*>(hl);
     *reinterpret_cast<uint4*>(pd + 2 * kp + c0) = *reinterpret_cast<const uint4*>(hh);
   }
+  // psplit rows: term k of column c, rows row0 + 8g .. row0 + 8g + 7
+  for (int it = threadIdx.x; it < rp * 4; it += blockDim.x) {
+    const int c = it >> 2, g = it & 3;
+    __align__(16) uint16_t t0[8], t1[8], t2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      t2[i] = 0;
+      if (nterms<T>() == 3) split3<T>(xs[8 * g + i][c], t0[i], t1[i], t2[i]);
+      else split2<T>(xs[8 * g + i][c], t0[i], t1[i]);
+    }
+    const size_t col = (size_t)row0 + 8 * g;
+    *reinterpret_cast<uint4*>(mt.psplit + (size_t)c * mpad + col) = *reinterpret_cast<const uint4*>(t0);
+    *reinterpret_cast<uint4*>(mt.psplit + (size_t)(rp + c) * mpad + col) = *reinterpret_cast<const uint4*>(t1);
+    if (nterms<T>() == 3)
+      *reinterpret_cast<uint4*>(mt.psplit + (size_t)(2 * rp + c) * mpad + col) = *reinterpret_cast<const uint4*>(t2);
+  }
 }
 
 // qdec[npad][3 kp] = [hi | hi | lo] of the new Q * 2^e in fp16 (e from max|Q|, scal[3]).
-// grid = (ceil(npad/128), B*J), block 128: thread = row of Q.
-__global__ void k_qdec(Plan p, int kp) {
+// A block stages 32 rows of Q (n x r row-major) in shared memory and writes 8 columns
+// per 16-byte store. grid = (npad / 32, B*J).
+__global__ void __launch_bounds__(256) k_qdec(Plan p, int kp) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
   const int64_t npad = (mt.n + DEC_NT - 1) / DEC_NT * DEC_NT;
-  const int64_t row = (int64_t)blockIdx.x * 128 + threadIdx.x;
-  if (row >= npad) return;
+  const int64_t row0 = (int64_t)blockIdx.x * 32;
+  if (row0 >= npad) return;
+  const int r = p.r;
+  __shared__ float xs[32][kMaxRank + 1];
+  const int64_t left = mt.n - row0;
+  const int nrows = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
   const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[3]);
-  const float* q = p.tab.q[blockIdx.y];
-  uint16_t* qd = mt.qdec + (size_t)row * 3 * kp;
-  for (int c0 = 0; c0 < kp; c0 += 8) {
+  const float* q = p.tab.q[blockIdx.y] + row0 * r;
+  for (int idx = threadIdx.x; idx < nrows * r; idx += blockDim.x) {
+    const int rr = idx / r, c = idx - rr * r;
+    xs[rr][c] = ldexpf(q[idx], e);
+  }
+  __syncthreads();
+  const int gpr = kp / 8;
+  for (int it = threadIdx.x; it < 32 * gpr; it += blockDim.x) {
+    const int rr = it / gpr, c0 = (it - rr * gpr) * 8;
     __align__(16) uint16_t hi[8], lo[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int c = c0 + i;
-      const float x = (row < mt.n && c < p.r) ? ldexpf(q[row * p.r + c], e) : 0.f;
-      split2<__half>(x, hi[i], lo[i]);
-    }
+    for (int i = 0; i < 8; ++i)
+      split2<__half>((rr < nrows && c0 + i < r) ? xs[rr][c0 + i] : 0.f, hi[i], lo[i]);
+    uint16_t* qd = mt.qdec + (size_t)(row0 + rr) * 3 * kp;
     *reinterpret_cast<uint4*>(qd + c0) = *reinterpret_cast<const uint4*>(hi);
     *reinterpret_cast<uint4*>(qd + kp + c0) = *reinterpret_cast<const uint4*>(hi);
     *reinterpret_cast<uint4*>(qd + 2 * kp + c0) = *reinterpret_cast<const uint4*>(lo);
@@ -256,10 +307,12 @@ __device__ __forceinline__ bool unit_off(const Plan& p, const MatMeta& mt, int o
 
 // MN_A = false: P GEMM (A = M tile K-major, unit = row tile x k-chunk).
 // MN_A = true:  Q GEMM (A = M^T tile MN-major, unit = column tile x m-slice).
+constexpr int kGemmThreads = 320;  // warps: 0 TMA, 1 MMA, 2..9 epilogue
+constexpr int kGemmEpiWarps = 8;   // two per TMEM lane quarter, each with half the columns
 template <bool MN_A, bool BF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
 k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
-       int a_stages, uint32_t b_stage, int only_shifted) {
+       int a_stages, uint32_t b_stage, int only_shifted, int seg) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   GemmSmem S{base, base + (size_t)a_stages * A_BYTES,
@@ -277,7 +330,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
   if (threadIdx.x == 0) {
     for (int i = 0; i < A_STAGES; ++i) { mbar_init(&sm.full_a[i], 1); mbar_init(&sm.empty_a[i], 1); }
     for (int i = 0; i < B_STAGES; ++i) { mbar_init(&sm.full_b[i], 1); mbar_init(&sm.empty_b[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&sm.acc_full[i], 1); mbar_init(&sm.acc_empty[i], 4); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&sm.acc_full[i], 1); mbar_init(&sm.acc_empty[i], kGemmEpiWarps); }
     mbar_init(&sm.done, 1);
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -342,12 +395,9 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const Unit un = units[u];
         if (unit_off(p, p.meta[un.t], only_shifted)) continue;
-        const int acc = (int)(ju % NACC);
-        ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
-        uint32_t accum = 0;
+        const int nsteps = (un.kb1 - un.kb0) * p.W;
+        int step = 0, acc = 0;
+        uint32_t d_tmem = tmem_base, accum = 0;
         for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
           const int sb = ib % B_STAGES;
           ok = mbar_wait(&sm.full_b[sb], (ib / B_STAGES) & 1, err);
@@ -355,6 +405,14 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
           tc_fence_after();
           const uint32_t b_addr = smem_u32(S.b(sb, b_stage));
           for (int w = 0; w < p.W; ++w) {
+            if (step % seg == 0) {  // open an accumulator segment
+              acc = (int)(ju % NACC);
+              ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
+              if (!ok) break;
+              tc_fence_after();
+              d_tmem = tmem_base + (uint32_t)(acc * 256);
+              accum = 0;
+            }
             const int sa = ia % A_STAGES;
             ok = mbar_wait(&sm.full_a[sa], (ia / A_STAGES) & 1, err);
             if (!ok) break;
@@ -371,31 +429,66 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
             }
             umma_commit(&sm.empty_a[sa]);
             ++ia;
+            if (++step % seg == 0 || step == nsteps) {  // close the segment
+              umma_commit(&sm.acc_full[acc]);
+              ++ju;
+            }
           }
           umma_commit(&sm.empty_b[sb]);
           ++ib;
         }
-        umma_commit(&sm.acc_full[acc]);
-        ++ju;
       }
       umma_commit(&sm.done);
       mbar_wait(&sm.done, 0, err, 1u << 22);
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------ epilogue (warps 2..9)
+    // A warp may read only its own TMEM lane quarter (warp index mod 4). Two warps share
+    // a quarter: half 0 takes the first ceil(rp/32) 16-column chunks, half 1 the rest.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = quarter * 32 + lane;
+    const int nch = rp / 16, ch0 = half ? (nch + 1) / 2 : 0, ch1 = half ? nch : (nch + 1) / 2;
     uint32_t ju = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       const Unit un = units[u];
       const MatMeta& mt = p.meta[un.t];
       if (unit_off(p, mt, only_shifted)) continue;
-      const int acc = (int)(ju % NACC);
-      ok = mbar_wait(&sm.acc_full[acc], (ju / NACC) & 1, err);
+      // Running sum of this row's chunks over the unit's accumulator segments, added in
+      // segment order with round-to-nearest fp32 adds.
+      float run[kMaxRank / 2];
+      const int nseg = ((un.kb1 - un.kb0) * p.W + seg - 1) / seg;
+      for (int sg = 0; sg < nseg && ok; ++sg) {
+        const int acc = (int)(ju % NACC);
+        ok = mbar_wait(&sm.acc_full[acc], (ju / NACC) & 1, err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+        for (int cc = 0; cc < kMaxRank / 32; ++cc) {
+          if (ch0 + cc < ch1) {
+            const int c = (ch0 + cc) * 16;
+            float t0[16], t1[16];  // split terms hi and lo (bf16: then the third, lo2)
+            tmem_ld16x2(t_row + c, t_row + rp + c, t0, t1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float x = sg == 0 ? t0[i] : __fadd_rn(run[cc * 16 + i], t0[i]);
+              run[cc * 16 + i] = __fadd_rn(x, t1[i]);
+            }
+            if (TERMS == 3) {
+              tmem_ld16(t_row + 2 * rp + c, t0);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) run[cc * 16 + i] = __fadd_rn(run[cc * 16 + i], t0[i]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
+        ++ju;
+      }
       if (!ok) break;
-      tc_fence_after();
-      const uint32_t t_row = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(quarter * 32) << 16);
       float* out;
       int64_t grow, limit;
       if (!MN_A) {
@@ -408,25 +501,18 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
         limit = mt.n;
         out = mt.Qpart + ((size_t)un.slot * mt.n + grow) * rp;
       }
-      for (int c = 0; c < rp; c += 16) {
-        float v[16], t[16];
-        tmem_ld16(t_row + c, v);
+      if (grow < limit) {
 #pragma unroll
-        for (int k = 1; k < TERMS; ++k) {
-          tmem_ld16(t_row + k * rp + c, t);
+        for (int cc = 0; cc < kMaxRank / 32; ++cc) {
+          if (ch0 + cc < ch1) {
+            const int c = (ch0 + cc) * 16;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] += t[i];
-        }
-        if (grow < limit) {
-#pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(out + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            for (int i = 0; i < 16; i += 4)
+              *reinterpret_cast<float4*>(out + c + i) = make_float4(
+                  run[cc * 16 + i], run[cc * 16 + i + 1], run[cc * 16 + i + 2], run[cc * 16 + i + 3]);
+          }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
-      ++ju;
     }
   }
   tc_fence_before();
@@ -437,12 +523,12 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
 
 // ---------------------------------------------------------------- fused ingest + P GEMM
 // One HBM sweep of the gradients. A TMA warp stages G_w and E_w tiles (128 rows x 64
-// columns, 128-byte rows, zero-filled past the matrix edge) into a shared-memory ring. Ingest warps form
-// M_w = round_E(zero_nonfinite(G_w / s_b) + E_w) from the staged tiles, count nonfinite
-// entries per (block, worker), store M_w to its scratch, and write the same tile into
-// shared memory in the UMMA 128-byte-swizzle K-major layout. The MMA thread accumulates
-// M_w (Q_hi | Q_lo [| Q_lo2]) over every worker and k-block of the unit into TMEM. The
-// epilogue writes the unit's P partial sums.
+// columns, 128-byte rows, zero-filled past the matrix edge) into a shared-memory ring. Ingest warps form M_w = round_E(zero_nonfinite(G_w / s_b) + E_w)
+// from the staged tiles, count nonfinite entries per (block, worker), store M_w to its
+// scratch, and write the same tile into shared memory in the UMMA 128-byte-swizzle
+// K-major layout. The MMA thread multiplies M_w by each split term of Q (Q_hi, Q_lo
+// [, Q_lo2]) into one accumulator, over every worker and k-block of the unit, in
+// segments; the epilogue sums the segments and writes the unit's P partial sums.
 // Warps: 0 TMA (Q split tiles), 1 MMA, 2..5 epilogue, 6..13 ingest, 14 TMA (G/E tiles).
 // The ingest warps also record max|M| per matrix (for the bf16 subnormal rescale).
 constexpr int kIngWarps = 8;
@@ -479,7 +565,7 @@ struct TileIter {
 template <typename TE>
 __global__ void __launch_bounds__(480, 1)
 k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
-           int a_stages, int ge_stages, uint32_t b_stage) {
+           int a_stages, int ge_stages, uint32_t b_stage, int seg) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* a0 = base;
@@ -490,8 +576,11 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
   constexpr bool BF16 = std::is_same<TE, __nv_bfloat16>::value;
   constexpr int TERMS = BF16 ? 3 : 2;
   const int rp = p.rp, N = TERMS * rp;
-  const int NACC = N <= 256 ? 2 : 1;
   const int NBOX = N <= 256 ? 1 : 2;
+  // TMEM: accumulators at columns 0 and 128 (rp <= 128 each: the split terms of Q go
+  // along K into the same accumulator), the running sum of the unit at column 256.
+  constexpr int NACC = 2;
+  constexpr uint32_t kAccCols = 128, kRunCol = 256;
   const uint32_t b_bytes = (uint32_t)N * BK * 2;
   int* err = p.err_word;
 
@@ -560,19 +649,14 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const int n0 = N <= 256 ? N : 256;
-      const uint32_t idesc0 = idesc_f16(BM, n0, BF16, false, false);
-      const uint32_t idesc1 = idesc_f16(BM, N > 256 ? N - 256 : 16, BF16, false, false);
+      const uint32_t idesc = idesc_f16(BM, rp, BF16, false, false);
       uint32_t ia = 0, ib = 0, ju = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const Unit un = units[u];
-        const int acc = (int)(ju % NACC);
-        ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
-        uint32_t accum = 0;
+        const int nsteps = (un.kb1 - un.kb0) * p.W;
+        int step = 0, acc = 0;
+        uint32_t d_tmem = tmem_base, accum = 0;
         for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
           const int sb = ib % B_STAGES;
           ok = mbar_wait(&sm.full_b[sb], (ib / B_STAGES) & 1, err);
@@ -580,6 +664,14 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
           tc_fence_after();
           const uint32_t b_addr = smem_u32(b0 + (size_t)sb * b_stage);
           for (int w = 0; w < p.W; ++w) {
+            if (step % seg == 0) {  // open an accumulator segment
+              acc = (int)(ju % NACC);
+              ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
+              if (!ok) break;
+              tc_fence_after();
+              d_tmem = tmem_base + (uint32_t)acc * kAccCols;
+              accum = 0;
+            }
             const int sa = ia % a_stages;
             ok = mbar_wait(&sm.full_a[sa], (ia / a_stages) & 1, err);
             if (!ok) break;
@@ -588,19 +680,23 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
               const uint64_t adesc = smem_desc(a_addr + k * 32, 16, 1024);
-              umma_f16(d_tmem, adesc, smem_desc(b_addr + k * 32, 16, 1024), idesc0, accum);
-              if (N > 256)
-                umma_f16(d_tmem + 256, adesc, smem_desc(b_addr + 256 * 128 + k * 32, 16, 1024), idesc1, accum);
-              accum = 1;
+#pragma unroll
+              for (int tm = 0; tm < TERMS; ++tm) {  // B rows [tm rp, (tm + 1) rp): term tm of Q
+                umma_f16(d_tmem, adesc, smem_desc(b_addr + tm * rp * 128 + k * 32, 16, 1024), idesc,
+                         accum);
+                accum = 1;
+              }
             }
             umma_commit(&sm.empty_a[sa]);
             ++ia;
+            if (++step % seg == 0 || step == nsteps) {  // close the segment
+              umma_commit(&sm.acc_full[acc]);
+              ++ju;
+            }
           }
           umma_commit(&sm.empty_b[sb]);
           ++ib;
         }
-        umma_commit(&sm.acc_full[acc]);
-        ++ju;
       }
       umma_commit(&sm.done);
       mbar_wait(&sm.done, 0, err, 1u << 22);
@@ -614,31 +710,44 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       const Unit un = units[u];
       const MatMeta& mt = p.meta[un.t];
-      const int acc = (int)(ju % NACC);
-      ok = mbar_wait(&sm.acc_full[acc], (ju / NACC) & 1, err);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t t_row = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(quarter * 32) << 16);
       const int64_t mpad = (mt.m + 127) / 128 * 128;
       const int64_t grow = (int64_t)un.tile * BM + row_in_tile;
       float* out = mt.Ppart + ((size_t)un.slot * mpad + grow) * rp;
-      for (int c = 0; c < rp; c += 16) {
-        float v[16], t[16];
-        tmem_ld16(t_row + c, v);
+      // Running sum of the unit's accumulator segments in TMEM (this thread's lane only),
+      // added in segment order with round-to-nearest fp32 adds; the last segment writes
+      // the unit's P partial row.
+      const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+      const uint32_t t_run = tmem_base + kRunCol + lane_off;
+      const int nseg = ((un.kb1 - un.kb0) * p.W + seg - 1) / seg;
+      for (int sg = 0; sg < nseg && ok; ++sg) {
+        const int acc = (int)(ju % NACC);
+        ok = mbar_wait(&sm.acc_full[acc], (ju / NACC) & 1, err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t t_acc = tmem_base + (uint32_t)acc * kAccCols + lane_off;
+        const bool last_seg = sg == nseg - 1;
+        for (int c = 0; c < rp; c += 16) {
+          float v[16], o[16];
+          if (sg == 0) {
+            tmem_ld16(t_acc + c, v);
+          } else {
+            tmem_ld16x2(t_acc + c, t_run + c, v, o);
 #pragma unroll
-        for (int k = 1; k < TERMS; ++k) {
-          tmem_ld16(t_row + k * rp + c, t);
+            for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(o[i], v[i]);
+          }
+          if (last_seg) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] += t[i];
+            for (int i = 0; i < 16; i += 4)
+              *reinterpret_cast<float4*>(out + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          } else {
+            tmem_st16(t_run + c, v);
+          }
         }
-#pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(out + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
+        ++ju;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
-      ++ju;
     }
   } else {
     // ------------------------------------------------------------ ingest (warps 6..13)
@@ -1078,7 +1187,7 @@ cudaError_t launch_rescale_tiny(const Handle& h, const Plan& p, cudaStream_t s) 
   const uint32_t bst = gemm_b_stage(h.edt, p.rp);
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
-  k_gemm<false, true><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 1);
+  k_gemm<false, true><<<grid, kGemmThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 1, kGemmSegSteps);
   h.launches += 1;
   return cudaGetLastError();
 }
@@ -1202,7 +1311,7 @@ cudaError_t launch_qmax(const Handle& h, const Plan& p, cudaStream_t s) {
 cudaError_t launch_prep_q(const Handle& h, const Plan& p, cudaStream_t s) {
   const int BJ = p.B * p.J;
   k_qmax<<<dim3(64, BJ), 256, 0, s>>>(p);
-  dim3 g((unsigned)((h.max_ntiles64 * 64 + 255) / 256), p.rp, BJ);
+  dim3 g((unsigned)((h.max_ntiles64 * 64 + 31) / 32), BJ);
   if (h.edt == DT_BF16) k_qsplit<__nv_bfloat16><<<g, 256, 0, s>>>(p);
   else k_qsplit<__half><<<g, 256, 0, s>>>(p);
   h.launches += 2;
@@ -1215,8 +1324,9 @@ cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const uint32_t bst = gemm_b_stage(h.edt, p.rp);
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
-  if (h.edt == DT_BF16) k_gemm<false, true><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0);
-  else k_gemm<false, false><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0);
+  const int seg = kGemmSegSteps;
+  if (h.edt == DT_BF16) k_gemm<false, true><<<grid, kGemmThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg);
+  else k_gemm<false, false><<<grid, kGemmThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg);
   int64_t maxe = 0;
   for (const MatMeta& mt : h.meta) maxe = std::max<int64_t>(maxe, mt.m * p.rp);
   k_preduce<<<dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), 256, 0, s>>>(p, PCHUNK_KB);
@@ -1231,8 +1341,9 @@ cudaError_t launch_ingest_p(const Handle& h, const Plan& p, cudaStream_t s) {
   int ast, gst;
   size_t sm;
   ingest_stages(h.edt, bst, &ast, &gst, &sm);
-  if (h.edt == DT_BF16) k_ingest_p<__nv_bfloat16><<<grid, 480, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst);
-  else k_ingest_p<__half><<<grid, 480, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst);
+  const int seg = kIngSegSteps;
+  if (h.edt == DT_BF16) k_ingest_p<__nv_bfloat16><<<grid, 480, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst, seg);
+  else k_ingest_p<__half><<<grid, 480, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst, seg);
   h.launches += 1;
   return cudaGetLastError();
 }
@@ -1247,23 +1358,24 @@ cudaError_t launch_preduce(const Handle& h, const Plan& p, cudaStream_t s) {
 
 cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
-  dim3 g((unsigned)h.max_mtiles, p.B * p.J);
-  if (h.edt == DT_BF16) k_psplit<__nv_bfloat16><<<g, 128, 0, s>>>(p, tp->kp);
-  else k_psplit<__half><<<g, 128, 0, s>>>(p, tp->kp);
+  dim3 g((unsigned)h.max_mtiles * 4, p.B * p.J);
+  if (h.edt == DT_BF16) k_psplit<__nv_bfloat16><<<g, 256, 0, s>>>(p, tp->kp);
+  else k_psplit<__half><<<g, 256, 0, s>>>(p, tp->kp);
   const int grid = std::min(tp->grid, tp->nq);
   const uint32_t bst = gemm_b_stage(h.edt, p.rp);
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
-  if (h.edt == DT_BF16) k_gemm<true, true><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0);
-  else k_gemm<true, false><<<grid, 192, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0);
+  const int seg = kGemmSegSteps;
+  if (h.edt == DT_BF16) k_gemm<true, true><<<grid, kGemmThreads, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg);
+  else k_gemm<true, false><<<grid, kGemmThreads, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg);
   h.launches += 2;
   return cudaGetLastError();
 }
 
 cudaError_t launch_decomp_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
-  dim3 g((unsigned)((h.max_ntiles128 * 128 + 127) / 128), p.B * p.J);
-  k_qdec<<<g, 128, 0, s>>>(p, tp->kp);
+  dim3 g((unsigned)h.max_ntiles128 * 4, p.B * p.J);
+  k_qdec<<<g, 256, 0, s>>>(p, tp->kp);
   const int grid = std::min(tp->grid, tp->nd);
   if (h.edt == DT_BF16) k_decomp_tc<__nv_bfloat16><<<grid, 320, dec_smem(), s>>>(p, tp->d_maps, tp->d_dunits, tp->nd, tp->kp);
   else k_decomp_tc<__half><<<grid, 320, dec_smem(), s>>>(p, tp->d_maps, tp->d_dunits, tp->nd, tp->kp);
