@@ -74,6 +74,23 @@ struct Plan {
   int* err_word;
 };
 
+// Max of v over the block, returned in thread 0 (every thread of the block must call it;
+// blockDim.x a multiple of 32). One atomic per block instead of one per warp: atomics on
+// one address serialise at its L2 slice.
+__device__ __forceinline__ unsigned block_max_u32(unsigned v) {
+  __shared__ unsigned s_wmax[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  v = __reduce_max_sync(0xffffffffu, v);
+  if (lane == 0) s_wmax[warp] = v;
+  __syncthreads();
+  unsigned r = 0u;
+  if (warp == 0) {
+    r = lane < (int)(blockDim.x >> 5) ? s_wmax[lane] : 0u;
+    r = __reduce_max_sync(0xffffffffu, r);
+  }
+  return r;
+}
+
 // ---------------------------------------------------------------- numerics helpers
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }

@@ -199,8 +199,8 @@ __global__ void __launch_bounds__(256) k_qreduce(Plan p, float qscale) {
       vmax = max(vmax, __float_as_uint(fabsf(v)));
     }
   }
-  vmax = __reduce_max_sync(0xffffffffu, vmax);
-  if (lane == 0 && vmax) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 3, vmax);
+  vmax = block_max_u32(vmax);
+  if (threadIdx.x == 0 && vmax) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 3, vmax);
 }
 
 template <typename TE> struct V4;

@@ -117,8 +117,8 @@ __global__ void k_qmax(Plan p) {
   unsigned mx = 0u;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x)
     mx = max(mx, __float_as_uint(fabsf(q[i])));
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if ((threadIdx.x & 31) == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 2, mx);
+  mx = block_max_u32(mx);
+  if (threadIdx.x == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 2, mx);
 }
 
 // qsplit[terms*rp][n]: rows k*rp + c hold term k of Q[:, c] * 2^e (k = 0 hi, then mid
@@ -190,8 +190,8 @@ __global__ void k_preduce(Plan p, int pchunk_kb) {
     mx = max(max(__float_as_uint(fabsf(o.x)), __float_as_uint(fabsf(o.y))),
              max(__float_as_uint(fabsf(o.z)), __float_as_uint(fabsf(o.w))));
   }
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if ((threadIdx.x & 31) == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 1, mx);
+  mx = block_max_u32(mx);
+  if (threadIdx.x == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 1, mx);
 }
 
 // From P^ (m x rp fp32, |entries| <= 1): psplit[terms*rp][mpad] = the terms of
@@ -523,7 +523,8 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
 
 // ---------------------------------------------------------------- fused ingest + P GEMM
 // One HBM sweep of the gradients. A TMA warp stages G_w and E_w tiles (128 rows x 64
-// columns, 128-byte rows, zero-filled past the matrix edge) into a shared-memory ring. Ingest warps form M_w = round_E(zero_nonfinite(G_w / s_b) + E_w)
+// columns, 128-byte rows in the 128-byte swizzle, zero-filled past the matrix edge) into a
+// shared-memory ring. Ingest warps form M_w = round_E(zero_nonfinite(G_w / s_b) + E_w)
 // from the staged tiles, count nonfinite entries per (block, worker), store M_w to its
 // scratch, and write the same tile into shared memory in the UMMA 128-byte-swizzle
 // K-major layout. The MMA thread multiplies M_w by each split term of Q (Q_hi, Q_lo
@@ -777,8 +778,9 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
         const int64_t row = (int64_t)ti.un.tile * BM + rl;
         uint4 mv = make_uint4(0u, 0u, 0u, 0u);
         if (row < mt.m && col < mt.n) {
-          const uint4 gv = *reinterpret_cast<const uint4*>(gs + rl * 128 + cq * 16);
-          const uint4 ev = *reinterpret_cast<const uint4*>(gs + A_BYTES + rl * 128 + cq * 16);
+          const int so = rl * 128 + ((cq ^ (rl & 7)) << 4);  // 128-byte swizzle of the staged tiles
+          const uint4 gv = *reinterpret_cast<const uint4*>(gs + so);
+          const uint4 ev = *reinterpret_cast<const uint4*>(gs + A_BYTES + so);
           const TE* gx = reinterpret_cast<const TE*>(&gv);
           const TE* ex = reinterpret_cast<const TE*>(&ev);
           TE* mx = reinterpret_cast<TE*>(&mv);
@@ -788,7 +790,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
             const bool bad = !isfinite(x);
             cnt += bad;
             mx[i] = add_to<TE>(bad ? 0.0f : x, to_f(ex[i]));
-            mmax = max(mmax, __float_as_uint(fabsf(to_f(mx[i]))));
+            if (BF16) mmax = max(mmax, __float_as_uint(fabsf(to_f(mx[i]))));
           }
           __stcg(reinterpret_cast<uint4*>(mo + row * mt.n + col), mv);
         }
@@ -796,11 +798,12 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
       }
       fence_proxy_async_smem();
       cnt = __reduce_add_sync(0xffffffffu, cnt);
-      mmax = __reduce_max_sync(0xffffffffu, mmax);
+      if (BF16) mmax = __reduce_max_sync(0xffffffffu, mmax);
       if (lane == 0 && cnt)
         atomicAdd(reinterpret_cast<unsigned long long*>(p.counts + (size_t)mt.b * p.W + ti.w),
                   (unsigned long long)cnt);
-      if (lane == 0 && mmax) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + SC_MAXM, mmax);
+      if (BF16 && lane == 0 && mmax)  // only the bf16 subnormal rescale reads max|M|
+        atomicMax(reinterpret_cast<unsigned*>(mt.scal) + SC_MAXM, mmax);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&sm.full_a[sa]);
@@ -827,27 +830,27 @@ void ingest_stages(int edt, uint32_t b_stage, int* a_st, int* ge_st, size_t* sme
 }
 
 // ---------------------------------------------------------------- decompression kernel
-constexpr int DEC_STAGES = 4;
-constexpr int GS_LD = DEC_NT + 4;  // row stride (floats) of the staged G^ tile
+constexpr int DEC_STAGES = 2;   // P^ / Q operand stages of the G^ MMA
+constexpr int DEC_MSTAGES = 4;  // M_w tile ring (E is formed in place and stored from it)
+constexpr int DEC_THREADS = 352;
 struct DecSmem {
   alignas(1024) uint8_t a[DEC_STAGES][A_BYTES];          // P^ split tiles, 128 x 64
   alignas(1024) uint8_t b[DEC_STAGES][DEC_NT * BK * 2];  // Q split tiles, 128 x 64
-  float g[BM * GS_LD];                                   // staged G^ tile
+  alignas(1024) uint8_t mt[DEC_MSTAGES][2 * A_BYTES];    // M_w tile 128 x 128: two swizzled boxes
   uint64_t full[DEC_STAGES], empty[DEC_STAGES];
   uint64_t acc_full[2], acc_empty[2], done;
+  uint64_t mfull[DEC_MSTAGES], mdone[DEC_MSTAGES];
   uint32_t tmem;
-  int abort_flag;
 };
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-// G^ tile 128 x 128 = A B^T over K = 3 kp (tensor cores), staged through shared memory,
-// then streamed in a coalesced layout: G^ is written once, and E_w = round_E(M_w - G^)
-// for every worker, with each thread holding every worker's loads of two 8-column
-// segments in flight.
-// Warps: 0 TMA, 1 MMA, 2..9 epilogue (256 threads).
+// G^ tile 128 x 128 = A B^T over K = 3 kp (tensor cores, accumulated in TMEM). The
+// epilogue warps read it once from TMEM into registers (two warps per TMEM lane
+// quarter, 64 columns each), write G^, and then, for every worker, form
+// E_w = round_E(M_w - G^) in place in the staged M_w tile. A TMA warp streams the M_w
+// tiles through a ring of shared-memory stages and stores the E_w tiles from them.
+// Warps: 0 TMA (operands), 1 MMA, 2..9 epilogue, 10 TMA (M_w in, E_w out).
 template <typename TE>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(DEC_THREADS, 1)
 k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits, int kp) {
   extern __shared__ uint8_t smem_raw[];
   DecSmem& sm = *reinterpret_cast<DecSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -859,8 +862,8 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
   if (threadIdx.x == 0) {
     for (int i = 0; i < DEC_STAGES; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&sm.acc_full[i], 1); mbar_init(&sm.acc_empty[i], 8); }
+    for (int i = 0; i < DEC_MSTAGES; ++i) { mbar_init(&sm.mfull[i], 1); mbar_init(&sm.mdone[i], 8); }
     mbar_init(&sm.done, 1);
-    sm.abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -874,6 +877,7 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
   const uint32_t tmem_base = sm.tmem;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ TMA: G^ operands
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -896,6 +900,7 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
         mbar_wait(&sm.full[k % DEC_STAGES], (k / DEC_STAGES) & 1, err, 1u << 20);
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(BM, DEC_NT, false, false, false);
       uint32_t it = 0, ju = 0;
@@ -930,112 +935,137 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
       umma_commit(&sm.done);
       mbar_wait(&sm.done, 0, err, 1u << 22);
     }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ TMA: M_w in, E_w out
+    if (lane == 0) {
+      const CUtensorMap* gem = static_cast<const CUtensorMap*>(p.tab.ge_maps);
+      // tiles held by the stages: (matrix, worker, row0, col0)
+      int st_t[DEC_MSTAGES] = {}, st_w[DEC_MSTAGES] = {}, st_r[DEC_MSTAGES] = {}, st_c[DEC_MSTAGES] = {},
+          st_two[DEC_MSTAGES] = {};
+      uint32_t i = 0;
+      bool ok = true;
+      auto store_tile = [&](uint32_t j) -> bool {
+        const int s = (int)(j % DEC_MSTAGES);
+        if (!mbar_wait(&sm.mdone[s], (j / DEC_MSTAGES) & 1, err)) return false;
+        const CUtensorMap* em = gem + 2 * ((size_t)st_t[s] * p.W + st_w[s]) + 1;
+        tma_store_2d(em, sm.mt[s], st_c[s], st_r[s]);
+        if (st_two[s]) tma_store_2d(em, sm.mt[s] + A_BYTES, st_c[s] + 64, st_r[s]);
+        bulk_commit();
+        return true;
+      };
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const Unit un = units[u];
+        const MatMeta& mt = p.meta[un.t];
+        if (p.skip[mt.b]) continue;
+        const CUtensorMap* mm = maps + (size_t)un.t * NMAPS + MAP_MP;
+        const int row0 = un.tile * BM, col0 = un.kb0 * DEC_NT;
+        const int two = (int64_t)col0 + 64 < mt.n ? 1 : 0;
+        for (int w = 0; w < p.W && ok; ++w) {
+          const int s = (int)(i % DEC_MSTAGES);
+          if (i >= DEC_MSTAGES) {  // the stage's previous tile: store its E, then reuse
+            ok = store_tile(i - DEC_MSTAGES);
+            if (!ok) break;
+            bulk_wait_read_all();
+          }
+          st_t[s] = un.t; st_w[s] = w; st_r[s] = row0; st_c[s] = col0; st_two[s] = two;
+          mbar_arrive_expect_tx(&sm.mfull[s], (uint32_t)(1 + two) * A_BYTES);
+          tma_load_3d(sm.mt[s], mm, col0, row0, w, &sm.mfull[s]);
+          if (two) tma_load_3d(sm.mt[s] + A_BYTES, mm, col0 + 64, row0, w, &sm.mfull[s]);
+          ++i;
+        }
+      }
+      // store the tiles still held by the stages
+      for (uint32_t j = (i > DEC_MSTAGES ? i - DEC_MSTAGES : 0); j < i && ok; ++j) ok = store_tile(j);
+      if (!ok)  // wait (bounded) for the loads this thread issued before the CTA may exit
+        for (uint32_t j = (i > DEC_MSTAGES ? i - DEC_MSTAGES : 0); j < i; ++j)
+          mbar_wait(&sm.mfull[j % DEC_MSTAGES], (j / DEC_MSTAGES) & 1, err, 1u << 20);
+      bulk_wait_all();
+    }
   } else {
-    const int et = threadIdx.x - 64;       // 0..255
+    // ------------------------------------------------------------ epilogue (warps 2..9)
     const int quarter = warp & 3;          // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;      // column half staged by this warp
+    const int half = (warp - 2) >> 2;      // 64-column half of the tile
     const int row_in_tile = quarter * 32 + lane;
-    uint32_t ju = 0;
-    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+    const int sw = row_in_tile & 7;        // 128-byte swizzle phase of this row
+    uint32_t ju = 0, i = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       const Unit un = units[u];
       const MatMeta& mt = p.meta[un.t];
       const int64_t m = mt.m, n = mt.n;
-      float* gh = p.tab.ghat[un.t];
-      const int64_t row0 = (int64_t)un.tile * BM, col0 = (int64_t)un.kb0 * DEC_NT;
+      const int64_t row = (int64_t)un.tile * BM + row_in_tile;
+      const int64_t colh = (int64_t)un.kb0 * DEC_NT + half * 64;
       const bool skipped = p.skip[mt.b] != 0;
+      float gv[64];
       if (!skipped) {
         const int acc = ju & 1;
-        if (!mbar_wait(&sm.acc_full[acc], (ju >> 1) & 1, err)) sm.abort_flag = 1;
+        ok = mbar_wait(&sm.acc_full[acc], (ju >> 1) & 1, err);
+        if (!ok) break;
         tc_fence_after();
-        if (!sm.abort_flag) {
-          // G^ = acc * 2^-(14 + e) as exact power-of-two factors (one rounding at most)
-          const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[3]);
-          const int tsh = 14 + e;
-          const int t1 = tsh > 126 ? 126 : (tsh < -126 ? -126 : tsh);
-          const float f1 = __uint_as_float((uint32_t)(127 - t1) << 23);
-          const float f2 = __uint_as_float((uint32_t)(127 - (tsh - t1)) << 23);
-          const uint32_t t_row = tmem_base + (uint32_t)(acc * DEC_NT + half * 64) + ((uint32_t)(quarter * 32) << 16);
-          float* gs = sm.g + row_in_tile * GS_LD + half * 64;
-          for (int c = 0; c < 64; c += 16) {
-            float v[16];
-            tmem_ld16(t_row + c, v);
+        // G^ = acc * 2^-(14 + e) as exact power-of-two factors (one rounding at most)
+        const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[3]);
+        const int tsh = 14 + e;
+        const int t1 = tsh > 126 ? 126 : (tsh < -126 ? -126 : tsh);
+        const float f1 = __uint_as_float((uint32_t)(127 - t1) << 23);
+        const float f2 = __uint_as_float((uint32_t)(127 - (tsh - t1)) << 23);
+        const uint32_t t_row = tmem_base + (uint32_t)(acc * DEC_NT + half * 64) + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
-            for (int i = 0; i < 16; i += 4)
-              *reinterpret_cast<float4*>(gs + c + i) =
-                  make_float4((v[i] * f1) * f2, (v[i + 1] * f1) * f2, (v[i + 2] * f1) * f2, (v[i + 3] * f1) * f2);
+        for (int c = 0; c < 64; c += 32) {
+          float v0[16], v1[16];
+          tmem_ld16x2(t_row + c, t_row + c + 16, v0, v1);
+#pragma unroll
+          for (int i2 = 0; i2 < 16; ++i2) {
+            gv[c + i2] = (v0[i2] * f1) * f2;
+            gv[c + 16 + i2] = (v1[i2] * f1) * f2;
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
         ++ju;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) gv[c] = 0.f;
       }
-      epi_bar();  // staged tile complete (or an abort recorded)
-      if (sm.abort_flag) break;
+      // G^ (this row's 64 columns; n is a multiple of 8)
+      if (row < m) {
+        float* gp = p.tab.ghat[un.t] + row * n + colh;
+#pragma unroll
+        for (int c = 0; c < 64; c += 4)
+          if (colh + c < n) *reinterpret_cast<float4*>(gp + c) = make_float4(gv[c], gv[c + 1], gv[c + 2], gv[c + 3]);
+      }
+      if (skipped) continue;
       TE* mbase = static_cast<TE*>(mt.mscr);
-      const size_t wstride = (size_t)m * n;
       // a rescaled bf16 M scratch holds M * 2^sh: undo it exactly, and restore M
       const int msh = reinterpret_cast<const int*>(mt.scal)[SC_MSHIFT];
       const float munscale = __uint_as_float((uint32_t)(127 - msh) << 23);
-      // 128 rows x 16 segments of 8 columns; thread et takes segments et + 256 k
-#pragma unroll 1
-      for (int k = 0; k < 8; k += 2) {
-        int64_t rowk[2], colk[2];
-        bool val[2];
-        float gv[2][8];
+      for (int w = 0; w < p.W; ++w) {
+        const int s = (int)(i % DEC_MSTAGES);
+        ok = mbar_wait(&sm.mfull[s], (i / DEC_MSTAGES) & 1, err);
+        if (!ok) break;
+        uint8_t* tile = sm.mt[s] + half * A_BYTES + row_in_tile * 128;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int sg = et + 256 * (k + q);
-          const int rl = sg >> 4, cs = (sg & 15) * 8;
-          rowk[q] = row0 + rl;
-          colk[q] = col0 + cs;
-          val[q] = rowk[q] < m && colk[q] < n;
-          if (skipped) {
+        for (int j = 0; j < 8; ++j) {
+          uint4* cp = reinterpret_cast<uint4*>(tile + ((j ^ sw) << 4));
+          const uint4 mv = *cp;
+          const TE* mx = reinterpret_cast<const TE*>(&mv);
+          __align__(16) TE ev[8], mr[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) gv[q][i] = 0.f;
-          } else {
-            const float4 a = *reinterpret_cast<const float4*>(sm.g + rl * GS_LD + cs);
-            const float4 b = *reinterpret_cast<const float4*>(sm.g + rl * GS_LD + cs + 4);
-            gv[q][0] = a.x; gv[q][1] = a.y; gv[q][2] = a.z; gv[q][3] = a.w;
-            gv[q][4] = b.x; gv[q][5] = b.y; gv[q][6] = b.z; gv[q][7] = b.w;
+          for (int e8 = 0; e8 < 8; ++e8) {
+            const float mval = to_f(mx[e8]) * munscale;  // exact: a power of two
+            ev[e8] = add_to<TE>(mval, -gv[j * 8 + e8]);
+            mr[e8] = from_f<TE>(mval);
           }
-          if (val[q]) {
-            float* gp = gh + rowk[q] * n + colk[q];
-            *reinterpret_cast<float4*>(gp) = make_float4(gv[q][0], gv[q][1], gv[q][2], gv[q][3]);
-            *reinterpret_cast<float4*>(gp + 4) = make_float4(gv[q][4], gv[q][5], gv[q][6], gv[q][7]);
-          }
+          *cp = *reinterpret_cast<const uint4*>(ev);
+          if (msh != 0 && row < m && colh + j * 8 < n)
+            *reinterpret_cast<uint4*>(mbase + (size_t)w * m * n + row * n + colh + j * 8) =
+                *reinterpret_cast<const uint4*>(mr);
         }
-        if (skipped) continue;
-        for (int w0 = 0; w0 < p.W; w0 += 8) {
-          uint4 mv[2][8];
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              if (val[q] && w0 + kk < p.W)
-                mv[q][kk] = __ldcs(reinterpret_cast<const uint4*>(mbase + (size_t)(w0 + kk) * wstride + rowk[q] * n + colk[q]));
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              if (!val[q] || w0 + kk >= p.W) continue;
-              const TE* mx = reinterpret_cast<const TE*>(&mv[q][kk]);
-              __align__(16) TE ev[8], mr[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float mval = to_f(mx[i]) * munscale;  // exact: a power of two
-                ev[i] = add_to<TE>(mval, -gv[q][i]);
-                mr[i] = from_f<TE>(mval);
-              }
-              TE* ep = static_cast<TE*>(p.tab.e[(size_t)un.t * p.W + w0 + kk]) + rowk[q] * n + colk[q];
-              __stcs(reinterpret_cast<uint4*>(ep), *reinterpret_cast<const uint4*>(ev));
-              if (msh != 0)
-                *reinterpret_cast<uint4*>(mbase + (size_t)(w0 + kk) * wstride + rowk[q] * n + colk[q]) =
-                    *reinterpret_cast<const uint4*>(mr);
-            }
-        }
+        fence_proxy_async_smem();  // E in shared memory, visible to the tensor store
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.mdone[s]);
+        ++i;
       }
-      epi_bar();  // the staged tile may be overwritten by the next unit
     }
   }
   tc_fence_before();
@@ -1068,7 +1098,7 @@ bool make_map(CUtensorMap* out, void* base, int rank, const uint64_t* dims, cons
   CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, (cuuint32_t)rank, base, d, s, b, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -1163,7 +1193,8 @@ size_t tc_ge_maps_bytes(const psgd_config* cfg) {
   return 2 * sizeof(CUtensorMap) * (size_t)cfg->num_blocks * cfg->mats_per_block * cfg->num_workers;
 }
 
-// TMA maps of each (matrix, worker) G and E: 2D {n, m}, 128 x 64 boxes, no swizzle.
+// TMA maps of each (matrix, worker) G and E: 2D {n, m}, 128 x 64 boxes, 128-byte swizzle
+// (the fused ingest reads G/E tiles through them; the decompression stores E tiles).
 bool tc_encode_ge_maps(const Handle& h, const void* const* grads, void* const* errs, void* out) {
   CUtensorMap* maps = static_cast<CUtensorMap*>(out);
   for (int t = 0; t < h.B * h.J; ++t) {
@@ -1172,8 +1203,8 @@ bool tc_encode_ge_maps(const Handle& h, const void* const* grads, void* const* e
     uint32_t box[2] = {64, 128};
     for (int w = 0; w < h.W; ++w) {
       const size_t slot = (size_t)t * h.W + w;
-      if (!make_map(&maps[2 * slot], const_cast<void*>(grads[slot]), 2, d, st, box, false)) return false;
-      if (!make_map(&maps[2 * slot + 1], errs[slot], 2, d, st, box, false)) return false;
+      if (!make_map(&maps[2 * slot], const_cast<void*>(grads[slot]), 2, d, st, box)) return false;
+      if (!make_map(&maps[2 * slot + 1], errs[slot], 2, d, st, box)) return false;
     }
   }
   return true;
@@ -1377,8 +1408,8 @@ cudaError_t launch_decomp_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   dim3 g((unsigned)h.max_ntiles128 * 4, p.B * p.J);
   k_qdec<<<g, 256, 0, s>>>(p, tp->kp);
   const int grid = std::min(tp->grid, tp->nd);
-  if (h.edt == DT_BF16) k_decomp_tc<__nv_bfloat16><<<grid, 320, dec_smem(), s>>>(p, tp->d_maps, tp->d_dunits, tp->nd, tp->kp);
-  else k_decomp_tc<__half><<<grid, 320, dec_smem(), s>>>(p, tp->d_maps, tp->d_dunits, tp->nd, tp->kp);
+  if (h.edt == DT_BF16) k_decomp_tc<__nv_bfloat16><<<grid, DEC_THREADS, dec_smem(), s>>>(p, tp->d_maps, tp->d_dunits, tp->nd, tp->kp);
+  else k_decomp_tc<__half><<<grid, DEC_THREADS, dec_smem(), s>>>(p, tp->d_maps, tp->d_dunits, tp->nd, tp->kp);
   h.launches += 2;
   return cudaGetLastError();
 }
