@@ -45,12 +45,12 @@ constexpr int PCHUNK_KB = 4;           // P GEMM: k-blocks of 64 columns per uni
 // accumulator per chained MMA, and those losses add up (they do not cancel like
 // round-to-nearest errors). So no accumulator chains more than a few MMAs: after each
 // segment of (k-block, worker) steps the epilogue adds the accumulator into a running sum
-// with round-to-nearest fp32 adds. The separate GEMMs keep that sum in registers and
-// close a segment every kGemmSegSteps steps (16 MMAs per column set). The fused ingest kernel keeps it
-// in TMEM, next to two accumulators of rp columns: there each K step issues one MMA per
-// split term of Q into the same accumulator, and a segment of kIngSegSteps steps chains
-// 8 (fp16) or 12 (bf16) MMAs per step.
-constexpr int kGemmSegSteps = 4;
+// with round-to-nearest fp32 adds. In both GEMM kernels each K step issues one MMA per
+// split term of the fp32 operand into the same accumulator of rp columns, so a step
+// chains 8 (fp16) or 12 (bf16) MMAs. The separate GEMMs keep the running sum in
+// registers and rotate four accumulators; the fused ingest kernel keeps it in TMEM next
+// to two accumulators.
+constexpr int kGemmSegSteps = 2;
 constexpr int kIngSegSteps = 2;
 constexpr int QSLICE_ROWS = 512;       // Q GEMM: rows of m per unit (matches Qpart slices)
 constexpr int DEC_NT = 128;            // G^ tile columns
@@ -284,10 +284,11 @@ __global__ void __launch_bounds__(256) k_qdec(Plan p, int kp) {
 // Shared memory, carved at run time: a_stages A tiles (16 KB each), B_STAGES B tiles of
 // b_stage bytes (1 KB multiples), then the barriers and the TMEM address slot.
 constexpr int kMaxAStages = 12;
+constexpr int kGemmAccs = 4;  // TMEM accumulators of the separate GEMMs
 struct GemmBars {
   uint64_t full_a[kMaxAStages], empty_a[kMaxAStages];
   uint64_t full_b[B_STAGES], empty_b[B_STAGES];
-  uint64_t acc_full[2], acc_empty[2], done;
+  uint64_t acc_full[kGemmAccs], acc_empty[kGemmAccs], done;
   uint32_t tmem;
 };
 struct GemmSmem {
@@ -321,8 +322,13 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
   const int A_STAGES = a_stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int TERMS = BF16 ? 3 : 2;
-  const int rp = p.rp, N = TERMS * rp;          // B rows = MMA N in total
-  const int NACC = N <= 256 ? 2 : 1;            // TMEM accumulators (512 columns)
+  const int rp = p.rp, N = TERMS * rp;          // B rows: the split terms, rp rows each
+  // The split terms go along K into one accumulator of rp <= 128 columns, so four
+  // accumulators fit in TMEM's 512 columns: the MMA can run three segments ahead of the
+  // epilogue's drain.
+  constexpr int NACC = kGemmAccs;
+  constexpr uint32_t kAccCols = 128;
+  static_assert(NACC * kAccCols <= 512 && kAccCols >= kMaxRank, "accumulators fit in TMEM");
   const int NBOX = N <= 256 ? 1 : 2;            // TMA boxes per B tile (<= 256 rows each)
   const uint32_t b_bytes = (uint32_t)N * BK * 2;
   int* err = p.err_word;
@@ -330,7 +336,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
   if (threadIdx.x == 0) {
     for (int i = 0; i < A_STAGES; ++i) { mbar_init(&sm.full_a[i], 1); mbar_init(&sm.empty_a[i], 1); }
     for (int i = 0; i < B_STAGES; ++i) { mbar_init(&sm.full_b[i], 1); mbar_init(&sm.empty_b[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&sm.acc_full[i], 1); mbar_init(&sm.acc_empty[i], kGemmEpiWarps); }
+    for (int i = 0; i < kGemmAccs; ++i) { mbar_init(&sm.acc_full[i], 1); mbar_init(&sm.acc_empty[i], kGemmEpiWarps); }
     mbar_init(&sm.done, 1);
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -387,9 +393,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const int n0 = N <= 256 ? N : 256;        // MMA pieces: [0, n0) and [n0, N)
-      const uint32_t idesc0 = idesc_f16(BM, n0, BF16, MN_A, false);
-      const uint32_t idesc1 = idesc_f16(BM, N > 256 ? N - 256 : 16, BF16, MN_A, false);
+      const uint32_t idesc = idesc_f16(BM, rp, BF16, MN_A, false);
       uint32_t ia = 0, ib = 0, ju = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
@@ -410,7 +414,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
               ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
               if (!ok) break;
               tc_fence_after();
-              d_tmem = tmem_base + (uint32_t)(acc * 256);
+              d_tmem = tmem_base + (uint32_t)acc * kAccCols;
               accum = 0;
             }
             const int sa = ia % A_STAGES;
@@ -422,10 +426,12 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
             for (int k = 0; k < BK / 16; ++k) {
               const uint64_t adesc = MN_A ? smem_desc(a_addr + k * 2048, A_BYTES / 2, 1024)
                                           : smem_desc(a_addr + k * 32, 16, 1024);
-              umma_f16(d_tmem, adesc, smem_desc(b_addr + k * 32, 16, 1024), idesc0, accum);
-              if (N > 256)
-                umma_f16(d_tmem + 256, adesc, smem_desc(b_addr + 256 * 128 + k * 32, 16, 1024), idesc1, accum);
-              accum = 1;
+#pragma unroll
+              for (int tm = 0; tm < TERMS; ++tm) {  // B rows [tm rp, (tm + 1) rp): term tm
+                umma_f16(d_tmem, adesc, smem_desc(b_addr + tm * rp * 128 + k * 32, 16, 1024), idesc,
+                         accum);
+                accum = 1;
+              }
             }
             umma_commit(&sm.empty_a[sa]);
             ++ia;
@@ -464,22 +470,18 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
         ok = mbar_wait(&sm.acc_full[acc], (ju / NACC) & 1, err);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t t_row = tmem_base + (uint32_t)(acc * 256) + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t t_row = tmem_base + (uint32_t)acc * kAccCols + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
-        for (int cc = 0; cc < kMaxRank / 32; ++cc) {
+        for (int cc = 0; cc < kMaxRank / 32; cc += 2) {  // chunks in pairs, one wait a pair
           if (ch0 + cc < ch1) {
             const int c = (ch0 + cc) * 16;
-            float t0[16], t1[16];  // split terms hi and lo (bf16: then the third, lo2)
-            tmem_ld16x2(t_row + c, t_row + rp + c, t0, t1);
+            const bool pair = ch0 + cc + 1 < ch1;
+            float t0[16], t1[16];
+            tmem_ld16x2(t_row + c, t_row + (pair ? c + 16 : c), t0, t1);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float x = sg == 0 ? t0[i] : __fadd_rn(run[cc * 16 + i], t0[i]);
-              run[cc * 16 + i] = __fadd_rn(x, t1[i]);
-            }
-            if (TERMS == 3) {
-              tmem_ld16(t_row + 2 * rp + c, t0);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) run[cc * 16 + i] = __fadd_rn(run[cc * 16 + i], t0[i]);
+              run[cc * 16 + i] = sg == 0 ? t0[i] : __fadd_rn(run[cc * 16 + i], t0[i]);
+              if (pair) run[cc * 16 + 16 + i] = sg == 0 ? t1[i] : __fadd_rn(run[cc * 16 + 16 + i], t1[i]);
             }
           }
         }
@@ -543,7 +545,10 @@ struct IngBars {
   uint32_t tmem;
 };
 
-// Walk the (unit, k-block, worker) tile sequence of this CTA.
+// Walk the (unit, worker, k-block) tile sequence of this CTA. The k-blocks of one worker
+// come back to back: a 128-byte tile row of G or E that starts off a 128-byte line (any
+// n * 2 not a multiple of 128) shares its second line with the next k-block's row, which
+// then still finds it in L2.
 struct TileIter {
   int u, kb, w;
   bool valid;
@@ -554,9 +559,10 @@ struct TileIter {
     if (valid) { un = units[u]; kb = un.kb0; }
   }
   __device__ void next(const Unit* units, int nunits, int W) {
+    if (++kb < un.kb1) return;
+    kb = un.kb0;
     if (++w < W) return;
     w = 0;
-    if (++kb < un.kb1) return;
     u += gridDim.x;
     valid = u < nunits;
     if (valid) { un = units[u]; kb = un.kb0; }
@@ -611,15 +617,16 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const Unit un = units[u];
         const CUtensorMap* mb = maps + (size_t)un.t * NMAPS + MAP_QS;
-        for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
-          const int sb = ib % B_STAGES;
-          ok = mbar_wait(&sm.empty_b[sb], ((ib / B_STAGES) & 1) ^ 1, err);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&sm.full_b[sb], b_bytes);
-          for (int x = 0; x < NBOX; ++x)
-            tma_load_2d(b0 + (size_t)sb * b_stage + x * (N / NBOX) * BK * 2, mb, kb * BK, x * (N / NBOX), &sm.full_b[sb]);
-          ++ib;
-        }
+        for (int w = 0; w < p.W && ok; ++w)  // one Q tile per (worker, k-block) step
+          for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
+            const int sb = ib % B_STAGES;
+            ok = mbar_wait(&sm.empty_b[sb], ((ib / B_STAGES) & 1) ^ 1, err);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&sm.full_b[sb], b_bytes);
+            for (int x = 0; x < NBOX; ++x)
+              tma_load_2d(b0 + (size_t)sb * b_stage + x * (N / NBOX) * BK * 2, mb, kb * BK, x * (N / NBOX), &sm.full_b[sb]);
+            ++ib;
+          }
       }
       for (uint32_t k = (ib > B_STAGES ? ib - B_STAGES : 0); k < ib; ++k)
         mbar_wait(&sm.full_b[k % B_STAGES], (k / B_STAGES) & 1, err, 1u << 20);
@@ -658,13 +665,13 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
         const int nsteps = (un.kb1 - un.kb0) * p.W;
         int step = 0, acc = 0;
         uint32_t d_tmem = tmem_base, accum = 0;
-        for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
-          const int sb = ib % B_STAGES;
-          ok = mbar_wait(&sm.full_b[sb], (ib / B_STAGES) & 1, err);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t b_addr = smem_u32(b0 + (size_t)sb * b_stage);
-          for (int w = 0; w < p.W; ++w) {
+        for (int w = 0; w < p.W && ok; ++w) {
+          for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
+            const int sb = ib % B_STAGES;
+            ok = mbar_wait(&sm.full_b[sb], (ib / B_STAGES) & 1, err);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t b_addr = smem_u32(b0 + (size_t)sb * b_stage);
             if (step % seg == 0) {  // open an accumulator segment
               acc = (int)(ju % NACC);
               ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
@@ -689,14 +696,14 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
               }
             }
             umma_commit(&sm.empty_a[sa]);
+            umma_commit(&sm.empty_b[sb]);
             ++ia;
+            ++ib;
             if (++step % seg == 0 || step == nsteps) {  // close the segment
               umma_commit(&sm.acc_full[acc]);
               ++ju;
             }
           }
-          umma_commit(&sm.empty_b[sb]);
-          ++ib;
         }
       }
       umma_commit(&sm.done);
