@@ -49,6 +49,52 @@ def parse():
     return ap.parse_args()
 
 
+# The dominant phase's kernel, its committed ncu summary and the file that holds its source.
+PROFILED = {"ingest": ("k_ingest_p", "profiles/k_ingest_p_resblock_shard.md"),
+            "decomp": ("k_decomp_tc", "profiles/k_decomp_tc_resblock_shard.md"),
+            "qgemm": ("k_gemm", "profiles/k_gemm_qgemm_resblock_shard.md")}
+KERNEL_SRC = "rank_gradient_compression_gb300/csrc/tc.cu"
+
+
+def kernel_source_hash(path: str, name: str):
+    """sha256 of a kernel's text, from its name to the closing brace of its body."""
+    import hashlib
+    try:
+        s = open(os.path.join(ROOT, path)).read()
+        i = s.index("\n" + name + "(")
+        j = s.index("{", i)
+    except (OSError, ValueError):
+        return None
+    depth = 0
+    for k in range(j, len(s)):
+        if s[k] == "{":
+            depth += 1
+        elif s[k] == "}":
+            depth -= 1
+            if depth == 0:
+                return hashlib.sha256(s[i:k + 1].encode()).hexdigest()
+    return None
+
+
+def profiled_traffic(phase: str):
+    """DRAM bytes per launch from the phase kernel's committed ncu summary, or None when
+    there is no summary or the kernel's source has changed since it was captured."""
+    if phase not in PROFILED:
+        return None, None
+    kname, md = PROFILED[phase]
+    try:
+        text = open(os.path.join(ROOT, md)).read()
+    except OSError:
+        return None, None
+    fields = dict(l.split(": ", 1) for l in text.splitlines() if ": " in l and not l.startswith(("|", "#")))
+    if fields.get("source_sha256", "").strip() != kernel_source_hash(KERNEL_SRC, kname):
+        return None, md
+    try:
+        return int(fields["traffic_bytes_per_launch"]), md
+    except (KeyError, ValueError):
+        return None, md
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -268,8 +314,10 @@ def run_ours(args):
     sm_clock = clk.get("sm_mhz") or float(pk.get("sm_max_mhz", 2070.0))
     if alg_bytes.get(dom, 0) and (ps.engine == "tcgen05" or dom in ("ingest", "decomp")):
         ach = alg_bytes[dom] / (d_ms * 1e-3) / 1e9
+        traffic, prof = profiled_traffic(dom)
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "traffic": None, "kernel": dom, "peak_kind": pk_kind}
+                "traffic": traffic, "kernel": dom, "peak_kind": pk_kind, "profile": prof,
+                "alg_bytes": alg_bytes[dom]}
     else:
         ach = flops.get(dom, 0) / (d_ms * 1e-3) / 1e12
         peak = SMS * FP32_LANES * 2 * float(pk.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
