@@ -44,9 +44,11 @@ __device__ __forceinline__ bool pass_skipped(const Plan& p, const MatMeta& mt, i
   return false;
 }
 
-// Gram partial sums over a row chunk: Gpart[c] = X_c^T X_c (rp x rp, r <= 128).
-// grid = (max C, B*J).
-__global__ void __launch_bounds__(kT) k_gram(Plan p, int pass) {
+// Gram partial sums over a row chunk: the upper triangle of Gpart[c] = X_c^T X_c
+// (rp x rp, r <= 128) in 8 x 8 blocks, one block (bi <= bj) per thread; the lower
+// triangle is neither written nor read. grid = (max C, B*J), block kGramThreads.
+constexpr int kGramThreads = 160;  // >= 16 * 17 / 2 = 136 upper-triangle blocks
+__global__ void __launch_bounds__(kGramThreads) k_gram(Plan p, int pass) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if ((int)blockIdx.x >= mt.C || pass_skipped(p, mt, pass)) return;
   const int64_t m = mt.m;
@@ -56,49 +58,58 @@ __global__ void __launch_bounds__(kT) k_gram(Plan p, int pass) {
   const int64_t rows_per = ((m + mt.C - 1) / mt.C + 31) / 32 * 32;
   const int64_t rbeg = (int64_t)blockIdx.x * rows_per, rend = min(m, rbeg + rows_per);
   __shared__ __align__(16) float Xs[32][128];
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int tid = threadIdx.x;
+  // this thread's block (bi, bj), bi <= bj, of the nb x nb block grid
+  const int nb = (r + 7) / 8;
+  int bi = 0, rem = tid;
+  while (bi < nb && rem >= nb - bi) { rem -= nb - bi; ++bi; }
+  const bool live = bi < nb;
+  const int bj = bi + rem;
   float acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
   for (int64_t k0 = rbeg; k0 < rend; k0 += 32) {
-    const int kk = tid >> 3, c = (tid & 7) * 16;
-    const int64_t row = k0 + kk;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      Xs[kk][c + i] = (row < rend && c + i < r) ? X[row * rp + c + i] * sc : 0.f;
+    for (int idx = tid; idx < 32 * 128; idx += kGramThreads) {
+      const int kk = idx >> 7, c = idx & 127;
+      const int64_t row = k0 + kk;
+      Xs[kk][c] = (row < rend && c < r) ? X[row * rp + c] * sc : 0.f;
+    }
     __syncthreads();
+    if (live) {
 #pragma unroll 4
-    for (int q = 0; q < 32; ++q) {
-      float a[8], b[8];
-      const float4 a0 = *reinterpret_cast<const float4*>(&Xs[q][ty * 8]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&Xs[q][ty * 8 + 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Xs[q][tx * 8]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Xs[q][tx * 8 + 4]);
-      a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w; a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
-      b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w; b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+      for (int q = 0; q < 32; ++q) {
+        float a[8], b[8];
+        const float4 a0 = *reinterpret_cast<const float4*>(&Xs[q][bi * 8]);
+        const float4 a1 = *reinterpret_cast<const float4*>(&Xs[q][bi * 8 + 4]);
+        const float4 b0 = *reinterpret_cast<const float4*>(&Xs[q][bj * 8]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&Xs[q][bj * 8 + 4]);
+        a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w; a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+        b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w; b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
     }
     __syncthreads();
   }
+  if (!live) return;
   float* out = mt.Gpart + (size_t)blockIdx.x * rp * rp;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int ii = ty * 8 + i;
+    const int ii = bi * 8 + i;
     if (ii >= r) continue;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int jj = tx * 8 + j;
-      if (jj < r) out[ii * rp + jj] = acc[i][j];
+      const int jj = bj * 8 + j;
+      if (jj < r && jj >= ii) out[ii * rp + jj] = acc[i][j];
     }
   }
 }
 
-// G = sum_c Gpart[c] into slot C of Gpart. Eight threads share an entry: thread k sums
+// G = sum_c Gpart[c] into slot C of Gpart (upper triangle). Eight threads share an entry: thread k sums
 // the partials c = k, k+8, ... in order, then the eight sums are added in a fixed tree
 // order (deterministic). grid = (ceil(rp*rp/32), B*J).
 __global__ void __launch_bounds__(kT) k_gsum(Plan p, int pass) {
@@ -107,7 +118,7 @@ __global__ void __launch_bounds__(kT) k_gsum(Plan p, int pass) {
   const int rp = p.rp;
   const int idx = blockIdx.x * (kT / 8) + (threadIdx.x >> 3);
   const int part = threadIdx.x & 7;
-  const bool live = idx < rp * rp;
+  const bool live = idx < rp * rp && idx % rp >= idx / rp;  // upper triangle only
   const float* src = mt.Gpart + (live ? idx : 0);
   float s = 0.f;
   if (live) {
@@ -167,7 +178,7 @@ __device__ __forceinline__ void load_gram_regs(const MatMeta& mt, int r, int rp,
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int j = lane + 32 * q;
-      float v = (i < r && j < r) ? src[(size_t)i * rp + j] : 0.f;
+      float v = (i < r && j < r && j >= i) ? src[(size_t)i * rp + j] : 0.f;  // upper triangle
       if (i == j && i < r) {
         if (record) S.diag0[i] = v;
         v += shift;
@@ -391,9 +402,12 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   const float* X = pass == 0 ? mt.P : buf_ptr(mt, mt.ostate[(pass - 1) * 4 + 1]);
   float* Y = buf_ptr(mt, mt.ostate[pass * 4 + 1]);
   const float sc = pass == 0 ? p_scale(mt) : 1.0f;
-  __shared__ float As[32][64 + 4];
+  __shared__ __align__(16) float As[32][64 + 4];
   __shared__ __align__(16) float Bs[32][128];
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  // A warp owns a 16-column strip (tx = column block of 8, ty = group of 4 rows), so the
+  // chunks of R^-1 below its strip (rows k > its last column: zero) are skipped whole.
+  const int tid = threadIdx.x, tx = tid >> 4, ty = tid & 15;
+  const int warp_last_col = (tid >> 5) * 16 + 15;
   float acc[4][8];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -419,9 +433,10 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
     __syncthreads();
 #pragma unroll 8
     for (int kk = 0; kk < 32; ++kk) {
+      if (k0 > warp_last_col) break;  // warp-uniform: R^-1 rows k0.. are zero in this strip
       float a[4], b[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+      const float4 av = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      a[0] = av.x; a[1] = av.y; a[2] = av.z; a[3] = av.w;
       const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 8]);
       const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 8 + 4]);
       b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
@@ -453,7 +468,7 @@ cudaError_t launch_orth(const Handle& h, const Plan& p, cudaStream_t s) {
   cudaFuncSetAttribute(k_chol, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCholSmem);
   const int BJ = p.B * p.J;
   for (int pass = 0; pass < kMaxPasses; ++pass) {
-    k_gram<<<dim3(h.max_C, BJ), kT, 0, s>>>(p, pass);
+    k_gram<<<dim3(h.max_C, BJ), kGramThreads, 0, s>>>(p, pass);
     k_gsum<<<dim3((p.rp * p.rp + kT / 8 - 1) / (kT / 8), BJ), kT, 0, s>>>(p, pass);
     k_chol<<<BJ, kCholThreads, kCholSmem, s>>>(p, pass);
     k_apply<<<dim3(h.max_mtiles64, BJ), kT, 0, s>>>(p, pass);
@@ -467,7 +482,7 @@ cudaError_t launch_orth_one(const Plan& p, int C, int mtiles64, cudaStream_t s) 
                                        (int)kCholSmem);
   if (e != cudaSuccess) return e;
   for (int pass = 0; pass < kMaxPasses; ++pass) {
-    k_gram<<<dim3(C, 1), kT, 0, s>>>(p, pass);
+    k_gram<<<dim3(C, 1), kGramThreads, 0, s>>>(p, pass);
     k_gsum<<<dim3((p.rp * p.rp + kT / 8 - 1) / (kT / 8), 1), kT, 0, s>>>(p, pass);
     k_chol<<<1, kCholThreads, kCholSmem, s>>>(p, pass);
     k_apply<<<dim3(mtiles64, 1), kT, 0, s>>>(p, pass);

@@ -532,9 +532,14 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
 // K-major layout. The MMA thread multiplies M_w by each split term of Q (Q_hi, Q_lo
 // [, Q_lo2]) into one accumulator, over every worker and k-block of the unit, in
 // segments; the epilogue sums the segments and writes the unit's P partial sums.
-// Warps: 0 TMA (Q split tiles), 1 MMA, 2..5 epilogue, 6..13 ingest, 14 TMA (G/E tiles).
+// Warps: 0 TMA (Q split tiles), 1 MMA, 2..5 epilogue, then kIngWarps ingest warps, then
+// the TMA warp of the G/E tiles (kIngGeWarp).
 // The ingest warps also record max|M| per matrix (for the bf16 subnormal rescale).
-constexpr int kIngWarps = 8;
+constexpr int kIngWarps = 16;                       // ingest warps: 8 or 16 (a divisor of 32)
+constexpr int kIngGeWarp = 6 + kIngWarps;           // the G/E TMA warp, after the ingest warps
+constexpr int kIngThreads = 32 * (kIngGeWarp + 1);
+constexpr int kIngRowsPerPass = 4 * kIngWarps;      // tile rows the ingest warps cover at once
+static_assert(128 % kIngRowsPerPass == 0, "ingest rows");
 constexpr int GE_BYTES = 2 * A_BYTES;  // one staged G tile + one E tile
 constexpr int kMaxGeStages = 4;
 struct IngBars {
@@ -570,7 +575,7 @@ struct TileIter {
 };
 
 template <typename TE>
-__global__ void __launch_bounds__(480, 1)
+__global__ void __launch_bounds__(kIngThreads, 1)
 k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
            int a_stages, int ge_stages, uint32_t b_stage, int seg) {
   extern __shared__ uint8_t smem_raw[];
@@ -631,7 +636,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
       for (uint32_t k = (ib > B_STAGES ? ib - B_STAGES : 0); k < ib; ++k)
         mbar_wait(&sm.full_b[k % B_STAGES], (k / B_STAGES) & 1, err, 1u << 20);
     }
-  } else if (warp == 14) {
+  } else if (warp == kIngGeWarp) {
     // ------------------------------------------------------------ TMA: G/E tiles
     if (lane == 0) {
       const CUtensorMap* gem = static_cast<const CUtensorMap*>(p.tab.ge_maps);
@@ -758,10 +763,10 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
       }
     }
   } else {
-    // ------------------------------------------------------------ ingest (warps 6..13)
-    const int it = threadIdx.x - 6 * 32;          // 0..255
+    // ------------------------------------------------------------ ingest (warps 6 ..)
+    const int it = threadIdx.x - 6 * 32;          // 0 .. 32 kIngWarps - 1
     const int cq = it & 7;                        // 16-byte chunk within the 128-byte row
-    const int rq = it >> 3;                       // first row (0..31); rows rq + 32k
+    const int rq = it >> 3;                       // first row; rows rq + kIngRowsPerPass k
     TileIter ti;
     ti.start(units, nunits);
     uint32_t ia = 0, ig = 0;
@@ -780,8 +785,8 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
       int cnt = 0;
       unsigned mmax = 0u;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int rl = rq + 32 * k;
+      for (int k = 0; k < 128 / kIngRowsPerPass; ++k) {
+        const int rl = rq + kIngRowsPerPass * k;
         const int64_t row = (int64_t)ti.un.tile * BM + rl;
         uint4 mv = make_uint4(0u, 0u, 0u, 0u);
         if (row < mt.m && col < mt.n) {
@@ -1380,8 +1385,8 @@ cudaError_t launch_ingest_p(const Handle& h, const Plan& p, cudaStream_t s) {
   size_t sm;
   ingest_stages(h.edt, bst, &ast, &gst, &sm);
   const int seg = kIngSegSteps;
-  if (h.edt == DT_BF16) k_ingest_p<__nv_bfloat16><<<grid, 480, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst, seg);
-  else k_ingest_p<__half><<<grid, 480, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst, seg);
+  if (h.edt == DT_BF16) k_ingest_p<__nv_bfloat16><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst, seg);
+  else k_ingest_p<__half><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst, seg);
   h.launches += 1;
   return cudaGetLastError();
 }

@@ -169,14 +169,11 @@ def test_stack64_sampled_blocks():
 def test_spectrum_rank_sweep(rank):
     """3968x15872 fp16 gradient with singular values c/k, W = 8 identical copies.
 
-    After a warm start, P has condition number about r^2. On the GPU each entry of P is a
-    chain of L = 4 k-blocks x 4 MMAs x 8 workers = 128 fp32 accumulations, then B = 62
-    partial sums. Each entry of the new Q is a chain of 256, then 8. A blocked fp32 sum of
-    terms a_j leaves an error of about u32 (sqrt(L/2) + sqrt(B/2)) sqrt(sum a_j^2), so
-    c = 14. In the small singular directions of a decaying spectrum the terms are kappa
-    times the result. The bar for G-hat and E is therefore max(1e-4, 4x the oracle's
-    own change under that modelled accumulation error), computed every step from the
-    same state. Both numbers are printed."""
+    After a warm start, P has condition number about r^2 (2.3e4 at r = 112), so rounding
+    in P is amplified into the span of P^. The bar is the plain 1e-4 on G-hat and on E
+    before storage. Also printed is the oracle's own change when its two GEMMs carry a
+    modelled fp32 accumulation error (u32 times the root sum of squared terms times 14).
+    That change is the size of difference that fp32 accumulation alone would explain."""
     import copy
     wl = synth.spectrum(rank=rank, steps=2)
     g = GpuRun(wl)
@@ -192,10 +189,9 @@ def test_spectrum_rank_sweep(rank):
         pert = oracle.block_step(grads, before, wl.scale(0), wl.err_dtype, accum_noise=14.0)
         sens_g = rel_err(pert.g_hat[0], res[0].g_hat[0])
         sens_e = rel_err(pert.e_pre[0][0], res[0].e_pre[0][0])
-        tol = {"g": max(TOL, 4 * sens_g), "e": max(TOL, 4 * sens_e)}
-        errs = compare_step(g, res, o, tol=lambda kind, b, j: tol[kind])
+        errs = compare_step(g, res, o, tol=TOL)
         print(f"rank {rank} step {t}: GPU (G-hat, E, stored E) {errs}; "
-              f"sensitivity to modelled fp32 accumulation (G-hat, E) ({sens_g:.2e}, {sens_e:.2e})")
+              f"oracle sensitivity to modelled fp32 accumulation (G-hat, E) ({sens_g:.2e}, {sens_e:.2e})")
 
 
 # ------------------------------------------------------------------ properties
