@@ -204,7 +204,7 @@ __device__ void cholesky_panels(float a[kPanel][4], int r, float dead_tol, CholS
           const float d0 = S.diag0[k];
           const bool bad = !(d > dead_tol * d0) || !isfinite(d) || !(d0 > 0.f);
           const float rkk = bad ? 1.f : sqrtf(d);
-          const float inv = 1.f / rkk;
+          const float inv = __frcp_rn(rkk);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int j = lane + 32 * q;
@@ -212,7 +212,7 @@ __device__ void cholesky_panels(float a[kPanel][4], int r, float dead_tol, CholS
           }
           if (lane == 0) {
             S.dead[k] = bad;
-            S.ratio[k] = bad ? 0.f : d / d0;
+            S.ratio[k] = bad ? 0.f : __fdividef(d, d0);  // statistics only
           }
           // the rows below k in this panel
 #pragma unroll
@@ -268,7 +268,7 @@ __device__ void inverse_panels(float a[kPanel][4], int r, CholSmem& S) {
       for (int t = kPanel - 1; t >= 0; --t) {
         const int k = k0 + t;
         if (k < r) {
-          const float inv = 1.f / S.R[k * kRsLd + k];
+          const float inv = __frcp_rn(S.R[k * kRsLd + k]);
 #pragma unroll
           for (int q = 0; q < 4; ++q) a[t][q] *= inv;
 #pragma unroll
@@ -318,10 +318,18 @@ __global__ void __launch_bounds__(kCholThreads) k_chol(Plan p, int pass) {
   const int src = pass == 0 ? 0 : mt.ostate[(pass - 1) * 4 + 1];
 
   float a[kPanel][4];
+  __shared__ float s_trace;
   load_gram_regs(mt, r, rp, a, 0.f, S, true);
   __syncthreads();
-  float trace = 0.f;
-  for (int k = 0; k < r; ++k) trace += S.diag0[k];  // same order in every thread
+  if (warp == 0) {  // trace: fixed-order warp reduction
+    float t = 0.f;
+    for (int k = lane; k < r; k += 32) t += S.diag0[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) s_trace = t;
+  }
+  __syncthreads();
+  const float trace = s_trace;
   bool shifted = false;
   if (!(trace > 0.f) || !isfinite(trace)) {
     for (int k = threadIdx.x; k < r; k += blockDim.x) { S.dead[k] = 1; S.ratio[k] = 0.f; }
@@ -413,22 +421,55 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  // 16-byte loads and stores when the row pitch and the buffers allow them (always in
+  // the step: pitch rp a multiple of 16, workspace buffers 256-byte aligned); scalar ones
+  // otherwise (a caller's 4-byte-aligned matrix in the one-matrix entry point).
+  const bool vec = (rp & 3) == 0 &&
+                   ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Y) |
+                     reinterpret_cast<uintptr_t>(mt.Rinv)) & 15) == 0;
   for (int k0 = 0; k0 < r; k0 += 32) {
     {
       const int rr = tid >> 2, kk = (tid & 3) * 8;
       const int64_t row = row0 + rr;
+      float x[8];
+      if (vec) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int k = k0 + kk + i;
-        As[kk + i][rr] = (row < m && k < r) ? X[row * rp + k] * sc : 0.f;
+        for (int h = 0; h < 2; ++h) {
+          const int k = k0 + kk + 4 * h;
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (row < m && k < rp) v = *reinterpret_cast<const float4*>(X + row * rp + k);
+          x[4 * h] = v.x; x[4 * h + 1] = v.y; x[4 * h + 2] = v.z; x[4 * h + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = (row < m && k0 + kk + i < r) ? X[row * rp + k0 + kk + i] : 0.f;
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) As[kk + i][rr] = (k0 + kk + i < r) ? x[i] * sc : 0.f;
     }
     {
       const int kk = tid >> 3, c = (tid & 7) * 16;
       const int k = k0 + kk;
+      const float* rrow = mt.Rinv + (size_t)k * rp;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        Bs[kk][c + i] = (k < r && c + i < r) ? mt.Rinv[k * rp + c + i] : 0.f;
+      for (int h = 0; h < 4; ++h) {
+        const int cc = c + 4 * h;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < r) {
+          if (vec) {
+            if (cc < rp) v = *reinterpret_cast<const float4*>(rrow + cc);
+          } else {
+            v.x = cc < r ? rrow[cc] : 0.f;
+            v.y = cc + 1 < r ? rrow[cc + 1] : 0.f;
+            v.z = cc + 2 < r ? rrow[cc + 2] : 0.f;
+            v.w = cc + 3 < r ? rrow[cc + 3] : 0.f;
+          }
+        }
+        Bs[kk][cc] = cc < r ? v.x : 0.f;
+        Bs[kk][cc + 1] = cc + 1 < r ? v.y : 0.f;
+        Bs[kk][cc + 2] = cc + 2 < r ? v.z : 0.f;
+        Bs[kk][cc + 3] = cc + 3 < r ? v.w : 0.f;
+      }
     }
     __syncthreads();
 #pragma unroll 8
@@ -452,10 +493,20 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   for (int i = 0; i < 4; ++i) {
     const int64_t row = row0 + ty * 4 + i;
     if (row >= m) continue;
+    float y[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = tx * 8 + j;
-      if (c < rp) Y[row * rp + c] = c < r ? acc[i][j] : 0.f;
+    for (int j = 0; j < 8; ++j) y[j] = tx * 8 + j < r ? acc[i][j] : 0.f;
+    if (vec) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = tx * 8 + 4 * h;
+        if (c < rp)
+          *reinterpret_cast<float4*>(Y + row * rp + c) = make_float4(y[4 * h], y[4 * h + 1], y[4 * h + 2], y[4 * h + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (tx * 8 + j < rp) Y[row * rp + tx * 8 + j] = y[j];
     }
   }
 }

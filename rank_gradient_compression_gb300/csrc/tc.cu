@@ -49,9 +49,11 @@ constexpr int PCHUNK_KB = 4;           // P GEMM: k-blocks of 64 columns per uni
 // split term of the fp32 operand into the same accumulator of rp columns, so a step
 // chains 8 (fp16) or 12 (bf16) MMAs. The separate GEMMs keep the running sum in
 // registers and rotate four accumulators; the fused ingest kernel keeps it in TMEM next
-// to two accumulators.
-constexpr int kGemmSegSteps = 2;
-constexpr int kIngSegSteps = 2;
+// to two accumulators. P's segments are shorter than Q's: errors in P are amplified by
+// cond(P) in the span of P^ (up to ~2e4 for a decaying spectrum at r = 112), errors in
+// Q reach G^ and E directly.
+constexpr int kGemmSegSteps = 16;
+constexpr int kIngSegSteps = 4;
 constexpr int QSLICE_ROWS = 512;       // Q GEMM: rows of m per unit (matches Qpart slices)
 constexpr int DEC_NT = 128;            // G^ tile columns
 constexpr int NMAPS = 6;               // tensor maps per matrix

@@ -130,3 +130,24 @@ def test_static_orth_rejects_sizes_beyond_the_limit():
     with pytest.raises(psgd.PSGDError) as ex:
         psgd.psgd_orthonormalize_static(0, b, 16, 4, _stream())
     assert ex.value.status == psgd.PSGD_EINVAL
+
+
+def test_static_orth_accepts_4_byte_aligned_pointers():
+    """The entry point promises only 4-byte alignment. With both pointers 4 bytes off a
+    16-byte boundary (r a multiple of 4, so only the pointers rule out 16-byte accesses),
+    the result equals the one from aligned buffers bit for bit."""
+    psgd = _psgd()
+    m, r = 1000, 40
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    p = torch.randn((m, r), generator=gen, device="cuda")
+    ref = _static(psgd, p)
+    pbuf = torch.zeros(m * r + 4, device="cuda")
+    obuf = torch.full((m * r + 4,), float("nan"), device="cuda")
+    pv = pbuf[1:1 + m * r]
+    pv.copy_(p.reshape(-1))
+    ov = obuf[1:1 + m * r]
+    psgd.psgd_orthonormalize_static(pv.data_ptr(), ov.data_ptr(), m, r, _stream())
+    torch.cuda.synchronize()
+    assert pv.data_ptr() % 16 == 4 and ov.data_ptr() % 16 == 4
+    assert torch.equal(ov.view(m, r), ref)
