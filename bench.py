@@ -57,11 +57,15 @@ KERNEL_SRC = "rank_gradient_compression_gb300/csrc/tc.cu"
 
 
 def kernel_source_hash(path: str, name: str):
-    """sha256 of a kernel's text, from its name to the closing brace of its body."""
+    """sha256 of a kernel's text, from its __global__ to the closing brace of its body."""
     import hashlib
+    import re
     try:
         s = open(os.path.join(ROOT, path)).read()
-        i = s.index("\n" + name + "(")
+        mt = re.search(r"__global__[^;{]*?\b" + re.escape(name) + r"\(", s)
+        if mt is None:
+            return None
+        i = mt.start()
         j = s.index("{", i)
     except (OSError, ValueError):
         return None

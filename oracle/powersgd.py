@@ -30,6 +30,9 @@ Parity status per function:
     invariance (Householder vs Gram-Schmidt), the error-feedback identity and the
     Eckart-Young bound.
   uncompressed_mean: pinned by a hand-worked example and the nonfinite brute force.
+  orthonormalize(method="cholqr_f32") is used only to derive a tolerance (an fp32
+    orthonormalisation's own distance from fp64). It is pinned by orthonormality and span
+    of well- and ill-conditioned inputs to fp32 accuracy.
   The values of P-hat and Q themselves depend on the basis and are not compared.
   Only G-hat, E, masks, counts and skips are compared.
 """
@@ -91,6 +94,40 @@ def skip_block(counts_per_worker, threshold: int) -> bool:
 
 
 # ----------------------------------------------------------------------- power step
+def _cholqr_f32(p: np.ndarray, passes: int = 4) -> np.ndarray:
+    """Shifted CholeskyQR carried out in fp32 (numpy float32), four passes.
+
+    Not a parity reference. The method fixes the orthonormalisation as Cholesky-QR or
+    Gram-Schmidt in fp32. This function measures how far such an fp32 orthonormalisation
+    of the same P lands from the fp64 basis, so that a tolerance can be derived from that
+    arithmetic. Per pass: G = X^T X. If its Cholesky fails, or a pivot keeps less than
+    2^-16 of its diagonal, the pass uses G + s I with s = 2^-20 sqrt(m) tr(G) instead (the
+    shifted CholeskyQR of Fukaya et al., 2020). Then X <- X R^-1. X starts as P scaled
+    by a power of two that puts max|P| in [1, 2).
+    """
+    m = p.shape[0]
+    amax = float(np.max(np.abs(p))) if p.size else 0.0
+    if amax == 0.0:
+        return np.zeros_like(p, dtype=np.float64)
+    x = (p * 2.0 ** (-math.floor(math.log2(amax)))).astype(np.float32)
+    for _ in range(passes):
+        g = x.T @ x
+        lower = None
+        try:
+            lower = np.linalg.cholesky(g)
+            piv = np.diag(lower).astype(np.float64) ** 2
+            if np.any(piv < 2.0 ** -16 * np.diag(g).astype(np.float64)):
+                lower = None
+        except np.linalg.LinAlgError:
+            lower = None
+        if lower is None:
+            shift = np.float32(2.0 ** -20 * math.sqrt(m) * float(np.trace(g)))
+            lower = np.linalg.cholesky(g + shift * np.eye(g.shape[0], dtype=np.float32))
+        rinv = np.linalg.inv(lower.T).astype(np.float32)
+        x = (x @ rinv).astype(np.float32)
+    return x.astype(np.float64)
+
+
 def orthonormalize(p: np.ndarray, method: str = "householder") -> np.ndarray:
     """Orthonormal basis of span(P), as many columns as P.
 
@@ -101,6 +138,8 @@ def orthonormalize(p: np.ndarray, method: str = "householder") -> np.ndarray:
     if method == "householder":
         qm, _ = np.linalg.qr(p, mode="reduced")
         return qm
+    if method == "cholqr_f32":
+        return _cholqr_f32(p)
     if method == "mgs2":
         v = np.array(p, dtype=np.float64, copy=True)
         m, r = v.shape

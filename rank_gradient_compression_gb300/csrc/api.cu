@@ -53,7 +53,7 @@ psgd_status validate_config(const psgd_config* c) {
     return fail(PSGD_EUNSUPPORTED, "grad_dtype and err_dtype must be equal in this build");
   if (c->rank < 1) return fail(PSGD_EINVAL, "rank must be >= 1");
   if (c->rank > kMaxRank)
-    return fail(PSGD_EUNSUPPORTED, "rank above 128 is not supported by this build");
+    return fail(PSGD_EUNSUPPORTED, "rank above 1024 is not supported by this build");
   if (c->unc_len < 0) return fail(PSGD_EINVAL, "unc_len must be >= 0");
   if (!(c->skip_fraction > 0.0 && c->skip_fraction <= 1.0))
     return fail(PSGD_EINVAL, "skip_fraction must be in (0, 1]");
@@ -362,6 +362,7 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
 
   Plan p{};
   p.B = h.B; p.J = h.J; p.W = h.W; p.r = h.r; p.rp = h.rp;
+  p.ob_r = h.r; p.ob_rp = h.rp; p.ob_c0 = 0; p.ob_src0 = 0;  // the orth driver sets blocks
   p.gdt = h.gdt; p.edt = h.edt;
   p.unc_len = h.cfg.unc_len;
   p.meta = h.d_meta;

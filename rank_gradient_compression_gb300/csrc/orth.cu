@@ -15,6 +15,8 @@
 //
 // Device pass state: ostate[pass] = {final, dst buffer, shifted, dead columns}, written
 // by the pass's Cholesky kernel. The next pass reads it after the launch boundary.
+#include <algorithm>
+
 #include "handle.h"
 
 namespace psgd {
@@ -24,6 +26,13 @@ constexpr int kT = 256;
 
 __device__ __forceinline__ float* buf_ptr(const MatMeta& mt, int idx) {
   return idx == 0 ? mt.P : idx == 1 ? mt.Xa : idx == 2 ? mt.Xb : mt.Phat;
+}
+
+// The block's columns in the buffer a pass reads: P (or, for a column block projected off
+// the earlier blocks, Xa) in pass 0, else the previous pass's output.
+__device__ __forceinline__ const float* pass_src(const Plan& p, const MatMeta& mt, int pass) {
+  const float* base = pass == 0 ? (p.ob_src0 ? mt.Xa : mt.P) : buf_ptr(mt, mt.ostate[(pass - 1) * 4 + 1]);
+  return base + p.ob_c0;
 }
 
 // Power-of-two scale that brings max|P| into [1, 2): exact.
@@ -44,6 +53,47 @@ __device__ __forceinline__ bool pass_skipped(const Plan& p, const MatMeta& mt, i
   return false;
 }
 
+// Upper triangle of X^T X for rows [0, nrows) of a shared-memory tile (64 x 128, zero
+// past r), one 8 x 8 block (bi <= bj) per thread, rows summed in order, into Gram
+// partial `chunk`. Threads without a block do nothing.
+__device__ void gram_rows(const MatMeta& mt, const float (*Xs)[128], int nrows, int r, int rp,
+                          int chunk) {
+  const int nb = (r + 7) / 8;
+  int bi = 0, rem = threadIdx.x;
+  while (bi < nb && rem >= nb - bi) { rem -= nb - bi; ++bi; }
+  if (bi >= nb) return;
+  const int bj = bi + rem;
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int q = 0; q < nrows; ++q) {
+    float a[8], b[8];
+    const float4 a0 = *reinterpret_cast<const float4*>(&Xs[q][bi * 8]);
+    const float4 a1 = *reinterpret_cast<const float4*>(&Xs[q][bi * 8 + 4]);
+    const float4 b0 = *reinterpret_cast<const float4*>(&Xs[q][bj * 8]);
+    const float4 b1 = *reinterpret_cast<const float4*>(&Xs[q][bj * 8 + 4]);
+    a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w; a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+    b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w; b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+  }
+  float* out = mt.Gpart + (size_t)chunk * rp * rp;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int ii = bi * 8 + i;
+    if (ii >= r) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int jj = bj * 8 + j;
+      if (jj < r && jj >= ii) out[ii * rp + jj] = acc[i][j];
+    }
+  }
+}
+
 // Gram partial sums over a row chunk: the upper triangle of Gpart[c] = X_c^T X_c
 // (rp x rp, r <= 128) in 8 x 8 blocks, one block (bi <= bj) per thread; the lower
 // triangle is neither written nor read. grid = (max C, B*J), block kGramThreads.
@@ -52,8 +102,8 @@ __global__ void __launch_bounds__(kGramThreads) k_gram(Plan p, int pass) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if ((int)blockIdx.x >= mt.C || pass_skipped(p, mt, pass)) return;
   const int64_t m = mt.m;
-  const int r = p.r, rp = p.rp;
-  const float* X = pass == 0 ? mt.P : buf_ptr(mt, mt.ostate[(pass - 1) * 4 + 1]);
+  const int r = p.ob_r, rp = p.ob_rp, xl = p.rp;  // block width, Gram pitch, X row pitch
+  const float* X = pass_src(p, mt, pass);
   const float sc = pass == 0 ? p_scale(mt) : 1.0f;
   const int64_t rows_per = ((m + mt.C - 1) / mt.C + 31) / 32 * 32;
   const int64_t rbeg = (int64_t)blockIdx.x * rows_per, rend = min(m, rbeg + rows_per);
@@ -74,7 +124,7 @@ __global__ void __launch_bounds__(kGramThreads) k_gram(Plan p, int pass) {
     for (int idx = tid; idx < 32 * 128; idx += kGramThreads) {
       const int kk = idx >> 7, c = idx & 127;
       const int64_t row = k0 + kk;
-      Xs[kk][c] = (row < rend && c < r) ? X[row * rp + c] * sc : 0.f;
+      Xs[kk][c] = (row < rend && c < r) ? X[row * xl + c] * sc : 0.f;
     }
     __syncthreads();
     if (live) {
@@ -115,7 +165,7 @@ __global__ void __launch_bounds__(kGramThreads) k_gram(Plan p, int pass) {
 __global__ void __launch_bounds__(kT) k_gsum(Plan p, int pass) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if (pass_skipped(p, mt, pass)) return;
-  const int rp = p.rp;
+  const int rp = p.ob_rp;
   const int idx = blockIdx.x * (kT / 8) + (threadIdx.x >> 3);
   const int part = threadIdx.x & 7;
   const bool live = idx < rp * rp && idx % rp >= idx / rp;  // upper triangle only
@@ -142,33 +192,33 @@ __global__ void __launch_bounds__(kT) k_gsum(Plan p, int pass) {
 // dead when it is <= dead_tol * diag0[k] (or not finite): row k of R becomes e_k and
 // column k takes no part in later updates.
 //
-// R^-1 (upper triangular) by the same panels from the bottom: the owner warp finishes
-// the rows of its panel, X_k = T_k / r_kk with T_k = e_k minus the contributions of the
-// rows below, and publishes them; the warps above subtract R[i][panel] X[panel].
-// Two block barriers per 8 rows in all, instead of one or two per row.
+// R^-1 in the same sweep: elimination on [G | I] turns the identity into L^-1 = R^-T with
+// L = R^T. Each warp also holds its rows of Z (initially I) in registers; the owner warp
+// scales its Z rows by 1/r_kk and updates them with the same multipliers as its G rows,
+// publishes them next to the R rows, and the later warps subtract the same multiples
+// from their Z rows. R^-1 = Z^T. One block barrier per 8 rows in all.
 constexpr int kCholWarps = 16;
 constexpr int kCholThreads = kCholWarps * 32;
 constexpr int kPanel = 8;
-static_assert(kCholWarps * kPanel >= kMaxRank, "every row needs an owner warp");
-constexpr int kRsLd = kMaxRank + 1;  // row stride of R in shared memory
+static_assert(kCholWarps * kPanel >= kRankBlock, "every row needs an owner warp");
+constexpr int kRsLd = kRankBlock + 1;  // row stride of R in shared memory
 
 struct CholSmem {
-  float R[kMaxRank * kRsLd];           // rows of R as they are finished
-  float X[2][kPanel * kRsLd];          // published rows of R^-1 (ping-pong by panel)
-  float diag0[kMaxRank];               // diagonal of the unshifted Gram matrix
-  float ratio[kMaxRank];               // pivot / diag0 (0 for dead pivots)
-  int dead[kMaxRank];
+  float R[kRankBlock * kRsLd];           // rows of R as they are finished
+  float X[2][kPanel * kRsLd];          // published rows of Z = R^-T (ping-pong by panel)
+  float diag0[kRankBlock];               // diagonal of the unshifted Gram matrix
+  float ratio[kRankBlock];               // pivot / diag0 (0 for dead pivots)
+  int dead[kRankBlock];
+  float trace, maxr, minr, minratio;    // block-wide scalars of one factorisation
+  int ndead;
 };
 
-// Select a[q] for a warp-uniform q in 0..3 without dynamic register indexing.
-__device__ __forceinline__ float pick4(const float a[4], int q) {
-  return q == 0 ? a[0] : q == 1 ? a[1] : q == 2 ? a[2] : a[3];
-}
-
-// Load rows [8 warp, 8 warp + 8) of the summed Gram matrix (slot C of Gpart) into
-// registers, zero outside r x r, and add `shift` to the diagonal. With record set, the
-// unshifted diagonal goes to diag0.
-__device__ __forceinline__ void load_gram_regs(const MatMeta& mt, int r, int rp, float a[kPanel][4],
+// The rows of warp w are i in [8w, 8w + 8), all in column group QW = w / 4 (32 columns
+// each). Of G (becoming R) only the groups q >= QW matter (columns >= i), and of
+// Z = R^-T only the groups q <= QW (columns <= i); each warp keeps just those in
+// registers: a[t][q - QW] and z[t][q].
+template <int QW>
+__device__ __forceinline__ void load_gram_rows(const MatMeta& mt, int r, int rp, float (&a)[kPanel][4 - QW],
                                                float shift, CholSmem& S, bool record) {
   const float* src = mt.Gpart + (size_t)mt.C * rp * rp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -176,40 +226,54 @@ __device__ __forceinline__ void load_gram_regs(const MatMeta& mt, int r, int rp,
   for (int t = 0; t < kPanel; ++t) {
     const int i = warp * kPanel + t;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = QW; q < 4; ++q) {
       const int j = lane + 32 * q;
       float v = (i < r && j < r && j >= i) ? src[(size_t)i * rp + j] : 0.f;  // upper triangle
       if (i == j && i < r) {
         if (record) S.diag0[i] = v;
         v += shift;
       }
-      a[t][q] = v;
+      a[t][q - QW] = v;
     }
   }
 }
 
-// Factor the registers' panels in place (rows of R) and fill S.R, S.dead, S.ratio.
-__device__ void cholesky_panels(float a[kPanel][4], int r, float dead_tol, CholSmem& S) {
+template <int QW>
+__device__ __forceinline__ void identity_rows(float (&z)[kPanel][QW + 1]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int t = 0; t < kPanel; ++t)
+#pragma unroll
+    for (int q = 0; q <= QW; ++q) z[t][q] = (warp * kPanel + t == lane + 32 * q) ? 1.f : 0.f;
+}
+
+// Factor the registers' panels in place (rows of R in a, rows of Z = R^-T in z, which must
+// start as I) and fill S.R (groups >= the row's own), S.dead, S.ratio.
+template <int QW>
+__device__ void cholesky_panels(float (&a)[kPanel][4 - QW], float (&z)[kPanel][QW + 1], int r,
+                                float dead_tol, CholSmem& S) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int npan = (r + kPanel - 1) / kPanel;
   for (int pn = 0; pn < npan; ++pn) {
     const int k0 = pn * kPanel;
-    if (warp == pn) {
-      const int qk = k0 >> 5;  // column group of this panel (panels never straddle 32)
+    float* Zp = S.X[pn & 1];
+    if (warp == pn) {  // the owner: its pivots are in its own group QW (a[.][0])
 #pragma unroll
       for (int t = 0; t < kPanel; ++t) {
         const int k = k0 + t;
         if (k < r) {
-          const float d = __shfl_sync(0xffffffffu, pick4(a[t], qk), k & 31);
+          const float d = __shfl_sync(0xffffffffu, a[t][0], k & 31);
           const float d0 = S.diag0[k];
           const bool bad = !(d > dead_tol * d0) || !isfinite(d) || !(d0 > 0.f);
           const float rkk = bad ? 1.f : sqrtf(d);
           const float inv = __frcp_rn(rkk);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = QW; q < 4; ++q) {
             const int j = lane + 32 * q;
-            a[t][q] = j < k ? 0.f : (j == k ? rkk : (bad ? 0.f : a[t][q] * inv));
+            a[t][q - QW] = j < k ? 0.f : (j == k ? rkk : (bad ? 0.f : a[t][q - QW] * inv));
           }
+#pragma unroll
+          for (int q = 0; q <= QW; ++q) z[t][q] *= inv;
           if (lane == 0) {
             S.dead[k] = bad;
             S.ratio[k] = bad ? 0.f : __fdividef(d, d0);  // statistics only
@@ -217,9 +281,11 @@ __device__ void cholesky_panels(float a[kPanel][4], int r, float dead_tol, CholS
           // the rows below k in this panel
 #pragma unroll
           for (int t2 = t + 1; t2 < kPanel; ++t2) {
-            const float c = __shfl_sync(0xffffffffu, pick4(a[t], qk), (k0 + t2) & 31);
+            const float c = __shfl_sync(0xffffffffu, a[t][0], (k0 + t2) & 31);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) a[t2][q] = fmaf(-c, a[t][q], a[t2][q]);
+            for (int q = 0; q < 4 - QW; ++q) a[t2][q] = fmaf(-c, a[t][q], a[t2][q]);
+#pragma unroll
+            for (int q = 0; q <= QW; ++q) z[t2][q] = fmaf(-c, z[t][q], z[t2][q]);
           }
         }
       }
@@ -227,7 +293,10 @@ __device__ void cholesky_panels(float a[kPanel][4], int r, float dead_tol, CholS
       for (int t = 0; t < kPanel; ++t)
         if (k0 + t < r) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) S.R[(k0 + t) * kRsLd + lane + 32 * q] = a[t][q];
+          for (int q = QW; q < 4; ++q) S.R[(k0 + t) * kRsLd + lane + 32 * q] = a[t][q - QW];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)  // groups past QW are zero; later warps read them
+            Zp[t * kRsLd + lane + 32 * q] = q <= QW ? z[t][q < QW ? q : QW] : 0.f;
         }
     }
     __syncthreads();
@@ -238,98 +307,48 @@ __device__ void cholesky_panels(float a[kPanel][4], int r, float dead_tol, CholS
       for (int pp = 0; pp < kPanel; ++pp) {
         if (pp >= kend) break;
         const float* Rk = S.R + (k0 + pp) * kRsLd;
-        float rj[4];
+        const float* Zk = Zp + pp * kRsLd;
+        float rj[4 - QW], zj[QW + 1];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) rj[q] = Rk[lane + 32 * q];
+        for (int q = QW; q < 4; ++q) rj[q - QW] = Rk[lane + 32 * q];
+#pragma unroll
+        for (int q = 0; q <= QW; ++q) zj[q] = Zk[lane + 32 * q];
 #pragma unroll
         for (int t = 0; t < kPanel; ++t) {  // rows i >= r hold zeros and stay unused
           const float c = Rk[i0 + t];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) a[t][q] = fmaf(-c, rj[q], a[t][q]);
+          for (int q = 0; q < 4 - QW; ++q) a[t][q] = fmaf(-c, rj[q], a[t][q]);
+#pragma unroll
+          for (int q = 0; q <= QW; ++q) z[t][q] = fmaf(-c, zj[q], z[t][q]);
         }
       }
     }
   }
 }
 
-// R^-1 into the registers (rows of this warp's panel), from S.R.
-__device__ void inverse_panels(float a[kPanel][4], int r, CholSmem& S) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int t = 0; t < kPanel; ++t)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) a[t][q] = (warp * kPanel + t == lane + 32 * q) ? 1.f : 0.f;
-  const int npan = (r + kPanel - 1) / kPanel;
-  for (int pn = npan - 1; pn >= 0; --pn) {
-    const int k0 = pn * kPanel;
-    float* Xp = S.X[pn & 1];
-    if (warp == pn) {
-#pragma unroll
-      for (int t = kPanel - 1; t >= 0; --t) {
-        const int k = k0 + t;
-        if (k < r) {
-          const float inv = __frcp_rn(S.R[k * kRsLd + k]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) a[t][q] *= inv;
-#pragma unroll
-          for (int t2 = 0; t2 < t; ++t2) {
-            const float c = S.R[(k0 + t2) * kRsLd + k];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) a[t2][q] = fmaf(-c, a[t][q], a[t2][q]);
-          }
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kPanel; ++t)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) Xp[t * kRsLd + lane + 32 * q] = a[t][q];
-    }
-    __syncthreads();
-    if (warp < pn) {
-      const int kend = min(kPanel, r - k0);
-      const float* Ri = S.R + (warp * kPanel) * kRsLd + k0;
-#pragma unroll
-      for (int pp = 0; pp < kPanel; ++pp) {
-        if (pp >= kend) break;
-        float xj[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) xj[q] = Xp[pp * kRsLd + lane + 32 * q];
-#pragma unroll
-        for (int t = 0; t < kPanel; ++t) {
-          const float c = Ri[t * kRsLd + pp];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) a[t][q] = fmaf(-c, xj[q], a[t][q]);
-        }
-      }
-    }
-  }
-}
-
-// One CTA per matrix: factor the Gram matrix of this pass, decide shift/final, write R^-1.
-__global__ void __launch_bounds__(kCholThreads) k_chol(Plan p, int pass) {
-  const MatMeta& mt = p.meta[blockIdx.x];
-  if (pass_skipped(p, mt, pass)) return;
-  const int r = p.r, rp = p.rp;
-  extern __shared__ __align__(16) unsigned char chol_smem[];
-  CholSmem& S = *reinterpret_cast<CholSmem*>(chol_smem);
+// The body of k_chol for the warps of row group QW (every instance meets the same block
+// barriers in the same order: every branch below is uniform over the block).
+template <int QW>
+__device__ void chol_main(const Plan& p, const MatMeta& mt, int pass, CholSmem& S) {
+  const int r = p.ob_r, rp = p.ob_rp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool last = pass == kMaxPasses - 1;
   int* st = mt.ostate + pass * 4;
   const int src = pass == 0 ? 0 : mt.ostate[(pass - 1) * 4 + 1];
 
-  float a[kPanel][4];
-  __shared__ float s_trace;
-  load_gram_regs(mt, r, rp, a, 0.f, S, true);
+  float a[kPanel][4 - QW], z[kPanel][QW + 1];
+  identity_rows<QW>(z);
+  load_gram_rows<QW>(mt, r, rp, a, 0.f, S, true);
   __syncthreads();
   if (warp == 0) {  // trace: fixed-order warp reduction
     float t = 0.f;
     for (int k = lane; k < r; k += 32) t += S.diag0[k];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if (lane == 0) s_trace = t;
+    if (lane == 0) S.trace = t;
   }
   __syncthreads();
-  const float trace = s_trace;
+  const float trace = S.trace;
   bool shifted = false;
   if (!(trace > 0.f) || !isfinite(trace)) {
     for (int k = threadIdx.x; k < r; k += blockDim.x) { S.dead[k] = 1; S.ratio[k] = 0.f; }
@@ -339,7 +358,7 @@ __global__ void __launch_bounds__(kCholThreads) k_chol(Plan p, int pass) {
     }
     __syncthreads();
   } else {
-    cholesky_panels(a, r, last ? 0x1p-40f : 0x1p-16f, S);
+    cholesky_panels<QW>(a, z, r, last ? 0x1p-40f : 0x1p-16f, S);
     __syncthreads();
     int nd = 0;
     for (int k = lane; k < r; k += 32) nd += S.dead[k];
@@ -347,15 +366,14 @@ __global__ void __launch_bounds__(kCholThreads) k_chol(Plan p, int pass) {
     if (nd > 0 && !last) {
       shifted = true;
       const float shift = 0x1p-20f * sqrtf((float)mt.m) * trace;
-      load_gram_regs(mt, r, rp, a, shift, S, false);
+      load_gram_rows<QW>(mt, r, rp, a, shift, S, false);
+      identity_rows<QW>(z);
       __syncthreads();
-      cholesky_panels(a, r, 0x1p-40f, S);
+      cholesky_panels<QW>(a, z, r, 0x1p-40f, S);
       __syncthreads();
     }
   }
   // statistics of the factor: warp 0 reduces over the pivots
-  __shared__ float s_maxr, s_minr, s_minratio;
-  __shared__ int s_ndead;
   if (warp == 0) {
     float mx = 0.f, mn = 3.4e38f, mr = 1.f;
     int nd = 0;
@@ -371,31 +389,46 @@ __global__ void __launch_bounds__(kCholThreads) k_chol(Plan p, int pass) {
       mr = fminf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
     }
     nd = __reduce_add_sync(0xffffffffu, nd);
-    if (lane == 0) { s_maxr = mx; s_minr = mn; s_minratio = mr; s_ndead = nd; }
+    if (lane == 0) { S.maxr = mx; S.minr = mn; S.minratio = mr; S.ndead = nd; }
   }
-  inverse_panels(a, r, S);
-  // R^-1 to global, dead columns zeroed
+  // R^-1 = Z^T to global (this warp's Z rows j are R^-1's columns j), dead columns zeroed;
+  // the groups past QW are zero (i > j).
   float* Ri = mt.Rinv;
 #pragma unroll
   for (int t = 0; t < kPanel; ++t) {
-    const int i = warp * kPanel + t;
-    if (i < r) {
+    const int j = warp * kPanel + t;
+    if (j < r) {
+      const bool dj = S.dead[j] != 0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int j = lane + 32 * q;
-        if (j < r) Ri[i * rp + j] = (j >= i && !S.dead[j]) ? a[t][q] : 0.f;
+        const int i = lane + 32 * q;
+        if (i < r) Ri[i * rp + j] = (q <= QW && i <= j && !dj) ? z[t][q <= QW ? q : QW] : 0.f;
       }
     }
   }
   if (threadIdx.x == 0) {
-    const bool nearly_orth = !shifted && s_ndead == 0 && s_minratio >= 0.5f &&
-                             s_maxr <= 2.f * s_minr;
-    const bool all_dead = s_ndead == r;
+    const bool nearly_orth = !shifted && S.ndead == 0 && S.minratio >= 0.5f &&
+                             S.maxr <= 2.f * S.minr;
+    const bool all_dead = S.ndead == r;
     const int fin = (last || nearly_orth || all_dead) ? 1 : 0;
     st[0] = fin;
     st[1] = fin ? 3 : (src == 1 ? 2 : 1);
     st[2] = shifted ? 1 : 0;
-    st[3] = s_ndead;
+    st[3] = S.ndead;
+  }
+}
+
+// One CTA per matrix: factor the Gram matrix of this pass, decide shift/final, write R^-1.
+__global__ void __launch_bounds__(kCholThreads, 1) k_chol(Plan p, int pass) {
+  const MatMeta& mt = p.meta[blockIdx.x];
+  if (pass_skipped(p, mt, pass)) return;
+  extern __shared__ __align__(16) unsigned char chol_smem[];
+  CholSmem& S = *reinterpret_cast<CholSmem*>(chol_smem);
+  switch (threadIdx.x >> 7) {  // row group = warp / 4
+    case 0: chol_main<0>(p, mt, pass, S); break;
+    case 1: chol_main<1>(p, mt, pass, S); break;
+    case 2: chol_main<2>(p, mt, pass, S); break;
+    default: chol_main<3>(p, mt, pass, S); break;
   }
 }
 
@@ -404,14 +437,18 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if (pass_skipped(p, mt, pass)) return;
   const int64_t m = mt.m;
-  const int r = p.r, rp = p.rp;
+  const int r = p.ob_r, rp = p.ob_rp, xl = p.rp;  // block width, R^-1 pitch, X/Y row pitch
   const int64_t row0 = (int64_t)blockIdx.x * 64;
   if (row0 >= m) return;
-  const float* X = pass == 0 ? mt.P : buf_ptr(mt, mt.ostate[(pass - 1) * 4 + 1]);
-  float* Y = buf_ptr(mt, mt.ostate[pass * 4 + 1]);
+  const float* X = pass_src(p, mt, pass);
+  float* Y = buf_ptr(mt, mt.ostate[pass * 4 + 1]) + p.ob_c0;
   const float sc = pass == 0 ? p_scale(mt) : 1.0f;
-  __shared__ __align__(16) float As[32][64 + 4];
-  __shared__ __align__(16) float Bs[32][128];
+  // As and Bs hold the operand chunks of the product; afterwards the same shared memory
+  // holds this tile of Y for the next pass's Gram partial.
+  __shared__ __align__(16) float smem_apply[64 * 128];
+  float (*As)[64 + 4] = reinterpret_cast<float (*)[64 + 4]>(smem_apply);
+  float (*Bs)[128] = reinterpret_cast<float (*)[128]>(smem_apply + 32 * (64 + 4));
+  float (*Ys)[128] = reinterpret_cast<float (*)[128]>(smem_apply);
   // A warp owns a 16-column strip (tx = column block of 8, ty = group of 4 rows), so the
   // chunks of R^-1 below its strip (rows k > its last column: zero) are skipped whole.
   const int tid = threadIdx.x, tx = tid >> 4, ty = tid & 15;
@@ -424,7 +461,7 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   // 16-byte loads and stores when the row pitch and the buffers allow them (always in
   // the step: pitch rp a multiple of 16, workspace buffers 256-byte aligned); scalar ones
   // otherwise (a caller's 4-byte-aligned matrix in the one-matrix entry point).
-  const bool vec = (rp & 3) == 0 &&
+  const bool vec = (xl & 3) == 0 && (rp & 3) == 0 &&
                    ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Y) |
                      reinterpret_cast<uintptr_t>(mt.Rinv)) & 15) == 0;
   for (int k0 = 0; k0 < r; k0 += 32) {
@@ -437,12 +474,12 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
         for (int h = 0; h < 2; ++h) {
           const int k = k0 + kk + 4 * h;
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (row < m && k < rp) v = *reinterpret_cast<const float4*>(X + row * rp + k);
+          if (row < m && k < rp) v = *reinterpret_cast<const float4*>(X + row * xl + k);
           x[4 * h] = v.x; x[4 * h + 1] = v.y; x[4 * h + 2] = v.z; x[4 * h + 3] = v.w;
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = (row < m && k0 + kk + i < r) ? X[row * rp + k0 + kk + i] : 0.f;
+        for (int i = 0; i < 8; ++i) x[i] = (row < m && k0 + kk + i < r) ? X[row * xl + k0 + kk + i] : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) As[kk + i][rr] = (k0 + kk + i < r) ? x[i] * sc : 0.f;
@@ -501,12 +538,177 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
       for (int h = 0; h < 2; ++h) {
         const int c = tx * 8 + 4 * h;
         if (c < rp)
-          *reinterpret_cast<float4*>(Y + row * rp + c) = make_float4(y[4 * h], y[4 * h + 1], y[4 * h + 2], y[4 * h + 3]);
+          *reinterpret_cast<float4*>(Y + row * xl + c) = make_float4(y[4 * h], y[4 * h + 1], y[4 * h + 2], y[4 * h + 3]);
       }
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (tx * 8 + j < rp) Y[row * rp + tx * 8 + j] = y[j];
+        if (tx * 8 + j < rp) Y[row * xl + tx * 8 + j] = y[j];
+    }
+  }
+  // The next pass's Gram partial of this 64-row chunk (the Gram chunking is 64 rows, so
+  // chunk = tile), unless this pass is the last one. Same rows, same order and same FMA
+  // chains as k_gram would use on the stored Y: the partial is bit for bit the same.
+  if (mt.ostate[pass * 4 + 0] != 0 || pass + 1 >= kMaxPasses) return;
+  __syncthreads();  // As and Bs are dead; Ys overlays them
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int rr = ty * 4 + i;
+    const bool live_row = row0 + rr < m;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = tx * 8 + j;
+      Ys[rr][c] = (live_row && c < r) ? acc[i][j] : 0.f;
+    }
+  }
+  __syncthreads();
+  gram_rows(mt, Ys, m - row0 < 64 ? (int)(m - row0) : 64, r, rp, blockIdx.x);
+}
+
+// ---------------------------------------------------------------- block Gram-Schmidt
+// For r > kRankBlock the columns are orthonormalised in blocks of kRankBlock: block
+// classical Gram-Schmidt with one re-orthogonalisation (the first projection is repeated
+// on its own result), then the CholeskyQR passes above on the projected block. A
+// projection of block [c0, c0 + rb) of a source S (P, or Xa) off the finished columns
+// P^[:, 0 .. c0):
+//   C = P^[:, <c0]^T S_blk (c0 x rb): row-chunk partials (the Gram chunking), summed in a
+//       fixed order into the slot after the partials (Gpart holds them: c0 * 128 < rp^2);
+//   Xa_blk = S_blk - P^[:, <c0] C.
+
+// C partials of one row chunk, one 128 x 128 tile of C per CTA (16 x 16 threads, 8 x 8 each).
+// grid = (max C, ceil(c0 / 128), B*J).
+__global__ void __launch_bounds__(kT) k_proj_coef(Plan p, int c0, int rb, int src_xa) {
+  const MatMeta& mt = p.meta[blockIdx.z];
+  if ((int)blockIdx.x >= mt.C || p.skip[mt.b]) return;
+  const int64_t m = mt.m;
+  const int xl = p.rp;
+  const int q0 = blockIdx.y * 128, qn = min(128, c0 - q0);
+  const float* Qh = mt.Phat + q0;
+  const float* S = (src_xa ? mt.Xa : mt.P) + c0;
+  const int64_t rows_per = ((m + mt.C - 1) / mt.C + 31) / 32 * 32;
+  const int64_t rbeg = (int64_t)blockIdx.x * rows_per, rend = min(m, rbeg + rows_per);
+  __shared__ __align__(16) float As[32][128];
+  __shared__ __align__(16) float Bs[32][128];
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int64_t k0 = rbeg; k0 < rend; k0 += 32) {
+    for (int idx = tid; idx < 32 * 128; idx += kT) {
+      const int kk = idx >> 7, c = idx & 127;
+      const int64_t row = k0 + kk;
+      As[kk][c] = (row < rend && c < qn) ? Qh[row * xl + c] : 0.f;
+      Bs[kk][c] = (row < rend && c < rb) ? S[row * xl + c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int q = 0; q < 32; ++q) {
+      float a[8], b[8];
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[q][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[q][ty * 8 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[q][tx * 8]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[q][tx * 8 + 4]);
+      a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w; a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+      b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w; b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  float* out = mt.Gpart + (size_t)blockIdx.x * c0 * 128;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int ii = ty * 8 + i;
+    if (ii >= qn) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int jj = tx * 8 + j;
+      if (jj < rb) out[(size_t)(q0 + ii) * 128 + jj] = acc[i][j];
+    }
+  }
+}
+
+// C = sum over the row chunks of the partials (fixed order) into the slot after them.
+// grid = (ceil(c0 * 128 / 32), B*J); eight threads per entry as in k_gsum.
+__global__ void __launch_bounds__(kT) k_proj_sum(Plan p, int c0, int rb) {
+  const MatMeta& mt = p.meta[blockIdx.y];
+  if (p.skip[mt.b]) return;
+  const int idx = blockIdx.x * (kT / 8) + (threadIdx.x >> 3);
+  const int part = threadIdx.x & 7;
+  const bool live = idx < c0 * 128 && (idx & 127) < rb;
+  const float* src = mt.Gpart + (live ? idx : 0);
+  const size_t slot = (size_t)c0 * 128;
+  float s = 0.f;
+  if (live) {
+#pragma unroll 8
+    for (int c = part; c < mt.C; c += 8) s = __fadd_rn(s, __ldg(src + (size_t)c * slot));
+  }
+  s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));
+  s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2));
+  s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 4));
+  if (live && part == 0) mt.Gpart[(size_t)mt.C * slot + idx] = s;
+}
+
+// Xa_blk = S_blk - P^[:, <c0] C on 64-row tiles (16 x 16 threads: 4 rows x 8 columns
+// each; K = c0 in chunks of 32). S may be Xa itself: a CTA reads the rows of S it writes
+// only at its end, and no other CTA touches them. grid = (ceil(m / 64), B*J).
+__global__ void __launch_bounds__(kT) k_proj_apply(Plan p, int c0, int rb, int src_xa) {
+  const MatMeta& mt = p.meta[blockIdx.y];
+  if (p.skip[mt.b]) return;
+  const int64_t m = mt.m;
+  const int xl = p.rp;
+  const int64_t row0 = (int64_t)blockIdx.x * 64;
+  if (row0 >= m) return;
+  const float* S = (src_xa ? mt.Xa : mt.P) + c0;
+  float* Y = mt.Xa + c0;
+  const float* Cf = mt.Gpart + (size_t)mt.C * c0 * 128;  // c0 x 128, pitch 128
+  __shared__ __align__(16) float As[32][64 + 4];
+  __shared__ __align__(16) float Bs[32][128];
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < c0; k0 += 32) {
+    {
+      const int rr = tid >> 2, kk = (tid & 3) * 8;
+      const int64_t row = row0 + rr;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) As[kk + i][rr] = row < m ? mt.Phat[row * xl + k0 + kk + i] : 0.f;
+    }
+    {
+      const int kk = tid >> 3, c = (tid & 7) * 16;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) Bs[kk][c + i] = c + i < rb ? Cf[(size_t)(k0 + kk) * 128 + c + i] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      const float4 av = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      const float a[4] = {av.x, av.y, av.z, av.w};
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 8]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 8 + 4]);
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t row = row0 + ty * 4 + i;
+    if (row >= m) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = tx * 8 + j;
+      if (c < rb) Y[row * xl + c] = S[row * xl + c] - acc[i][j];
     }
   }
 }
@@ -518,12 +720,33 @@ constexpr size_t kCholSmem = sizeof(CholSmem);
 cudaError_t launch_orth(const Handle& h, const Plan& p, cudaStream_t s) {
   cudaFuncSetAttribute(k_chol, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCholSmem);
   const int BJ = p.B * p.J;
-  for (int pass = 0; pass < kMaxPasses; ++pass) {
-    k_gram<<<dim3(h.max_C, BJ), kGramThreads, 0, s>>>(p, pass);
-    k_gsum<<<dim3((p.rp * p.rp + kT / 8 - 1) / (kT / 8), BJ), kT, 0, s>>>(p, pass);
-    k_chol<<<BJ, kCholThreads, kCholSmem, s>>>(p, pass);
-    k_apply<<<dim3(h.max_mtiles64, BJ), kT, 0, s>>>(p, pass);
-    h.launches += 4;
+  const int nblk = (p.r + kRankBlock - 1) / kRankBlock;  // one block when r <= kRankBlock
+  for (int k = 0; k < nblk; ++k) {
+    Plan pb = p;
+    pb.ob_c0 = k * kRankBlock;
+    pb.ob_r = std::min(kRankBlock, p.r - pb.ob_c0);
+    pb.ob_rp = std::min(kRankBlock, p.rp - pb.ob_c0);
+    pb.ob_src0 = 0;
+    if (k > 0) {  // project the block off the finished columns, twice
+      const int c0 = pb.ob_c0, rb = pb.ob_r;
+      for (int it = 0; it < 2; ++it) {
+        k_proj_coef<<<dim3(h.max_C, (c0 + 127) / 128, BJ), kT, 0, s>>>(pb, c0, rb, it);
+        k_proj_sum<<<dim3((c0 * 128 + kT / 8 - 1) / (kT / 8), BJ), kT, 0, s>>>(pb, c0, rb);
+        k_proj_apply<<<dim3(h.max_mtiles64, BJ), kT, 0, s>>>(pb, c0, rb, it);
+        h.launches += 3;
+      }
+      pb.ob_src0 = 1;
+    }
+    for (int pass = 0; pass < kMaxPasses; ++pass) {
+      if (pass == 0) {  // later passes get their Gram partials from the previous k_apply
+        k_gram<<<dim3(h.max_C, BJ), kGramThreads, 0, s>>>(pb, pass);
+        h.launches += 1;
+      }
+      k_gsum<<<dim3((pb.ob_rp * pb.ob_rp + kT / 8 - 1) / (kT / 8), BJ), kT, 0, s>>>(pb, pass);
+      k_chol<<<BJ, kCholThreads, kCholSmem, s>>>(pb, pass);
+      k_apply<<<dim3(h.max_mtiles64, BJ), kT, 0, s>>>(pb, pass);
+      h.launches += 3;
+    }
   }
   return cudaGetLastError();
 }
@@ -533,8 +756,8 @@ cudaError_t launch_orth_one(const Plan& p, int C, int mtiles64, cudaStream_t s) 
                                        (int)kCholSmem);
   if (e != cudaSuccess) return e;
   for (int pass = 0; pass < kMaxPasses; ++pass) {
-    k_gram<<<dim3(C, 1), kGramThreads, 0, s>>>(p, pass);
-    k_gsum<<<dim3((p.rp * p.rp + kT / 8 - 1) / (kT / 8), 1), kT, 0, s>>>(p, pass);
+    if (pass == 0) k_gram<<<dim3(C, 1), kGramThreads, 0, s>>>(p, pass);
+    k_gsum<<<dim3((p.ob_rp * p.ob_rp + kT / 8 - 1) / (kT / 8), 1), kT, 0, s>>>(p, pass);
     k_chol<<<1, kCholThreads, kCholSmem, s>>>(p, pass);
     k_apply<<<dim3(mtiles64, 1), kT, 0, s>>>(p, pass);
   }

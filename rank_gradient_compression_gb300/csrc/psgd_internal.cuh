@@ -42,7 +42,9 @@ struct MatMeta {
 };
 
 constexpr int kMaxPasses = 4;  // CholeskyQR passes at most (shifted ones included)
-constexpr int kMaxRank = 128;  // largest r of this build
+constexpr int kRankBlock = 128;  // widest column block the orthonormalisation factors at once,
+                                 // and the largest r of the tensor-core engine
+constexpr int kMaxRank = 1024;   // largest r of this build (the FFMA engine above kRankBlock)
 constexpr int64_t kGramRows = 64;  // rows per partial sum of the Gram matrix X^T X
 
 // Per-step device pointer tables (uploaded when they change).
@@ -72,6 +74,11 @@ struct Plan {
   uint32_t* mask;                // bitmap or null
   const int64_t* mask_off;       // [B*J*W]
   int* err_word;
+  // The column block the orthonormalisation kernels work on: width ob_r <= kRankBlock,
+  // Gram / R^-1 pitch ob_rp, first column ob_c0 in the P / X buffers (pitch rp), and the
+  // buffer pass 0 reads (0 = P, 1 = Xa, the block projected off the earlier blocks).
+  // One block (ob_r = r, ob_rp = rp, ob_c0 = 0, ob_src0 = 0) when r <= kRankBlock.
+  int32_t ob_r, ob_rp, ob_c0, ob_src0;
 };
 
 // Max of v over the block, returned in thread 0 (every thread of the block must call it;

@@ -19,6 +19,24 @@ __device__ __forceinline__ float ldf(const T* p) { return to_f(*p); }
 // scaled by the exact power of two 2^e that puts max|Q| in [2^14, 2^15) (from scal[2]),
 // so P = (1/W) sum_w M_w Q 2^e. P^ does not depend on that scale, and M Q stays inside
 // fp32's range when M and Q are both tiny.
+// Two-level fp32 accumulation: FMAs go into `part` (a run of 32 terms), which is added
+// into `acc` with a compensated (Kahan) sum, `cmp` holding the running compensation.
+// A single chain over W * n (up to 1.3e5) terms would leave about sqrt of that times the
+// unit roundoff; here it is about sqrt(16) for the runs plus O(1) for the total. At high
+// rank the GEMM error is amplified by cond(P) (up to 2e6) in the span of P^.
+__device__ __forceinline__ void flush_part(float acc[4][8], float cmp[4][8], float part[4][8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float y = __fsub_rn(part[i][j], cmp[i][j]);
+      const float t = __fadd_rn(acc[i][j], y);
+      cmp[i][j] = __fsub_rn(__fsub_rn(t, acc[i][j]), y);
+      acc[i][j] = t;
+      part[i][j] = 0.f;
+    }
+}
+
 template <typename TE>
 __global__ void __launch_bounds__(kT) k_pgemm(Plan p) {
   const MatMeta& mt = p.meta[blockIdx.z];
@@ -35,11 +53,11 @@ __global__ void __launch_bounds__(kT) k_pgemm(Plan p) {
   __shared__ float As[32][64 + 4];
   __shared__ __align__(16) float Bs[32][128];
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  float acc[4][8];
+  float acc[4][8], cmp[4][8], part[4][8];  // total, its compensation, the current run
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 8; ++j) acc[i][j] = cmp[i][j] = part[i][j] = 0.f;
   for (int w = 0; w < p.W; ++w) {
     const TE* M = static_cast<const TE*>(mt.mscr) + (size_t)w * m * n;
     for (int64_t k0 = 0; k0 < n; k0 += 32) {
@@ -74,9 +92,10 @@ __global__ void __launch_bounds__(kT) k_pgemm(Plan p) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+          for (int j = 0; j < 8; ++j) part[i][j] = fmaf(a[i], b[j], part[i][j]);
       }
       __syncthreads();
+      flush_part(acc, cmp, part);  // every 32 terms
     }
   }
   unsigned vmax = 0u;
@@ -118,11 +137,11 @@ __global__ void __launch_bounds__(kT) k_qgemm(Plan p) {
   __shared__ float As[32][64 + 4];
   __shared__ __align__(16) float Bs[32][128];
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  float acc[4][8];
+  float acc[4][8], cmp[4][8], part[4][8];  // total, its compensation, the current run
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 8; ++j) acc[i][j] = cmp[i][j] = part[i][j] = 0.f;
   for (int w = 0; w < p.W; ++w) {
     const TE* M = static_cast<const TE*>(mt.mscr) + (size_t)w * m * n;
     for (int64_t k0 = rbeg; k0 < rend; k0 += 32) {
@@ -157,9 +176,10 @@ __global__ void __launch_bounds__(kT) k_qgemm(Plan p) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+          for (int j = 0; j < 8; ++j) part[i][j] = fmaf(a[i], b[j], part[i][j]);
       }
       __syncthreads();
+      flush_part(acc, cmp, part);  // every 32 terms
     }
   }
   float* out = mt.Qpart + (size_t)s * n * rp;
@@ -189,14 +209,25 @@ __global__ void __launch_bounds__(256) k_qreduce(Plan p, float qscale) {
   const size_t stride = (size_t)mt.n * p.rp;  // one slice of Qpart
   unsigned vmax = 0u;
   if (row < mt.n) {
-    for (int c = lane; c < p.r; c += 32) {
-      const float* src = mt.Qpart + (size_t)row * p.rp + c;
-      float acc = 0.f;
+    // lane takes 4 consecutive columns (one 16-byte load per slice; rp is a multiple of 16)
+    for (int c0 = lane * 4; c0 < p.r; c0 += 128) {
+      const float* src = mt.Qpart + (size_t)row * p.rp + c0;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-      for (int s = 0; s < mt.S; ++s) acc = __fadd_rn(acc, src[(size_t)s * stride]);
-      const float v = ldexpf(__fdiv_rn(acc * qscale, fw), -msh);
-      q[row * p.r + c] = v;
-      vmax = max(vmax, __float_as_uint(fabsf(v)));
+      for (int s = 0; s < mt.S; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(src + (size_t)s * stride);
+        acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
+        acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
+      }
+      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (c0 + i < p.r) {
+          const float v = ldexpf(__fdiv_rn(a4[i] * qscale, fw), -msh);
+          q[row * p.r + c0 + i] = v;
+          vmax = max(vmax, __float_as_uint(fabsf(v)));
+        }
+      }
     }
   }
   vmax = block_max_u32(vmax);

@@ -43,11 +43,11 @@ constexpr size_t kOffScal = 512;                                  // kScalWords 
 constexpr size_t kOffState = 768;                                 // kMaxPasses x 4 ints
 constexpr size_t kOffSkip = 1024;                                 // one byte (block 0)
 constexpr size_t kOffRinv = 1280;                                 // r x r floats
-constexpr size_t kOffGpart = kOffRinv + 4 * (size_t)kMaxRank * kMaxRank;
+constexpr size_t kOffGpart = kOffRinv + 4 * (size_t)kRankBlock * kRankBlock;
 constexpr size_t kStaticBytes =
-    kOffGpart + 4 * (size_t)(kStaticMaxChunks + 1) * kMaxRank * kMaxRank;
+    kOffGpart + 4 * (size_t)(kStaticMaxChunks + 1) * kRankBlock * kRankBlock;
 
-static_assert(PSGD_STATIC_MAX_COLS == kMaxRank, "column limit = the largest rank");
+static_assert(PSGD_STATIC_MAX_COLS == kRankBlock, "column limit = the largest rank");
 static_assert(sizeof(MatMeta) <= kOffScal - kOffMeta, "plan slot too small");
 static_assert(4 * kScalWords <= kOffState - kOffScal, "scale slot too small");
 static_assert(4 * 4 * kMaxPasses <= kOffSkip - kOffState, "pass-state slot too small");
@@ -121,10 +121,10 @@ extern "C" psgd_status psgd_orthonormalize_static(const float* p, float* phat, i
              (long long)m, (long long)kStaticMaxRows);
     return report_error(PSGD_EINVAL, msg);
   }
-  if (r > kMaxRank) {
+  if (r > kRankBlock) {
     char msg[160];
     snprintf(msg, sizeof msg, "r = %d exceeds the static scratch limit of %d columns", r,
-             kMaxRank);
+             kRankBlock);
     return report_error(PSGD_EINVAL, msg);
   }
   if (r > m) return report_error(PSGD_EINVAL, "r must be <= m");
@@ -155,6 +155,7 @@ extern "C" psgd_status psgd_orthonormalize_static(const float* p, float* phat, i
   Plan pl{};
   pl.B = 1; pl.J = 1; pl.W = 1;
   pl.r = r; pl.rp = r;  // dense m x r: the orthonormalisation kernels take any row pitch
+  pl.ob_r = r; pl.ob_rp = r; pl.ob_c0 = 0; pl.ob_src0 = 0;
   pl.meta = reinterpret_cast<const MatMeta*>(base + kOffMeta);
   pl.skip = reinterpret_cast<uint8_t*>(base + kOffSkip);
 

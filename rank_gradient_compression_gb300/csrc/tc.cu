@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(256) k_qsplit(Plan p) {
   const int64_t j0 = (int64_t)blockIdx.x * 32;
   if (j0 >= mt.n) return;
   const int r = p.r, rp = p.rp;
-  __shared__ float xs[32][kMaxRank + 1];
+  __shared__ float xs[32][kRankBlock + 1];
   const float* q = p.tab.q[blockIdx.y] + j0 * r;
   const int64_t left = mt.n - j0;
   const int nrows = left < 32 ? (int)left : 32;
@@ -172,6 +172,7 @@ __global__ void k_preduce(Plan p, int pchunk_kb) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
   const int rp = p.rp;
+  if ((int64_t)blockIdx.x * blockDim.x * 4 >= mt.m * p.rp) return;  // whole block past the end
   const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   const int64_t mpad = (mt.m + 127) / 128 * 128;
   unsigned mx = 0u;
@@ -209,7 +210,7 @@ __global__ void __launch_bounds__(256) k_psplit(Plan p, int kp) {
   const int64_t row0 = (int64_t)blockIdx.x * 32;
   if (row0 >= mpad) return;
   const int r = p.r, rp = p.rp;
-  __shared__ float xs[32][kMaxRank + 1];
+  __shared__ float xs[32][kRankBlock + 1];
   const int64_t left = mt.m - row0;
   const int nrows = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
   const float* src = mt.Phat + row0 * rp;
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(256) k_qdec(Plan p, int kp) {
   const int64_t row0 = (int64_t)blockIdx.x * 32;
   if (row0 >= npad) return;
   const int r = p.r;
-  __shared__ float xs[32][kMaxRank + 1];
+  __shared__ float xs[32][kRankBlock + 1];
   const int64_t left = mt.n - row0;
   const int nrows = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
   const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[3]);
@@ -330,7 +331,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
   // epilogue's drain.
   constexpr int NACC = kGemmAccs;
   constexpr uint32_t kAccCols = 128;
-  static_assert(NACC * kAccCols <= 512 && kAccCols >= kMaxRank, "accumulators fit in TMEM");
+  static_assert(NACC * kAccCols <= 512 && kAccCols >= kRankBlock, "accumulators fit in TMEM");
   const int NBOX = N <= 256 ? 1 : 2;            // TMA boxes per B tile (<= 256 rows each)
   const uint32_t b_bytes = (uint32_t)N * BK * 2;
   int* err = p.err_word;
@@ -465,7 +466,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
       if (unit_off(p, mt, only_shifted)) continue;
       // Running sum of this row's chunks over the unit's accumulator segments, added in
       // segment order with round-to-nearest fp32 adds.
-      float run[kMaxRank / 2];
+      float run[kRankBlock / 2];
       const int nseg = ((un.kb1 - un.kb0) * p.W + seg - 1) / seg;
       for (int sg = 0; sg < nseg && ok; ++sg) {
         const int acc = (int)(ju % NACC);
@@ -474,7 +475,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
         tc_fence_after();
         const uint32_t t_row = tmem_base + (uint32_t)acc * kAccCols + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
-        for (int cc = 0; cc < kMaxRank / 32; cc += 2) {  // chunks in pairs, one wait a pair
+        for (int cc = 0; cc < kRankBlock / 32; cc += 2) {  // chunks in pairs, one wait a pair
           if (ch0 + cc < ch1) {
             const int c = (ch0 + cc) * 16;
             const bool pair = ch0 + cc + 1 < ch1;
@@ -507,7 +508,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
       }
       if (grow < limit) {
 #pragma unroll
-        for (int cc = 0; cc < kMaxRank / 32; ++cc) {
+        for (int cc = 0; cc < kRankBlock / 32; ++cc) {
           if (ch0 + cc < ch1) {
             const int c = (ch0 + cc) * 16;
 #pragma unroll
@@ -782,6 +783,12 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
       uint8_t* tile = a0 + (size_t)sa * A_BYTES;
       const uint8_t* gs = ge0 + (size_t)sg * GE_BYTES;
       const float inv_s = p.tab.inv_scale[mt.b];
+      // fp16 with a power-of-two scale: x = g / s keeps g's 11-bit significand, so one
+      // round-to-nearest fp32 add followed by the rounding to fp16 already gives
+      // round_E(x + E) (the fp32 sum is exact unless one term is below 2^-12 of the other,
+      // and then it is below half an ulp of the result; checked by brute force over
+      // every fp16 pattern, including ties). Other cases take the round-to-odd sum.
+      const bool rn_sum = !BF16 && (__float_as_uint(inv_s) & 0x7fffffu) == 0u;
       TE* mo = static_cast<TE*>(mt.mscr) + (size_t)ti.w * mt.m * mt.n;
       const int64_t col = (int64_t)ti.kb * BK + cq * 8;
       int cnt = 0;
@@ -798,13 +805,23 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
           const TE* gx = reinterpret_cast<const TE*>(&gv);
           const TE* ex = reinterpret_cast<const TE*>(&ev);
           TE* mx = reinterpret_cast<TE*>(&mv);
+          if (rn_sum) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float x = to_f(gx[i]) * inv_s;
-            const bool bad = !isfinite(x);
-            cnt += bad;
-            mx[i] = add_to<TE>(bad ? 0.0f : x, to_f(ex[i]));
-            if (BF16) mmax = max(mmax, __float_as_uint(fabsf(to_f(mx[i]))));
+            for (int i = 0; i < 8; ++i) {
+              const float x = to_f(gx[i]) * inv_s;
+              const bool bad = !isfinite(x);
+              cnt += bad;
+              mx[i] = from_f<TE>(__fadd_rn(bad ? 0.0f : x, to_f(ex[i])));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float x = to_f(gx[i]) * inv_s;
+              const bool bad = !isfinite(x);
+              cnt += bad;
+              mx[i] = add_to<TE>(bad ? 0.0f : x, to_f(ex[i]));
+              if (BF16) mmax = max(mmax, __float_as_uint(fabsf(to_f(mx[i]))));
+            }
           }
           __stcg(reinterpret_cast<uint4*>(mo + row * mt.n + col), mv);
         }
@@ -1203,7 +1220,7 @@ __global__ void k_rescale_tiny(Plan p) {
 }
 
 size_t tc_ge_maps_bytes(const psgd_config* cfg) {
-  if (cfg->err_dtype == PSGD_F32 || (cfg->flags & PSGD_FLAG_SIMT)) return 0;
+  if (cfg->err_dtype == PSGD_F32 || (cfg->flags & PSGD_FLAG_SIMT) || cfg->rank > kRankBlock) return 0;
   return 2 * sizeof(CUtensorMap) * (size_t)cfg->num_blocks * cfg->mats_per_block * cfg->num_workers;
 }
 
@@ -1238,12 +1255,13 @@ cudaError_t launch_rescale_tiny(const Handle& h, const Plan& p, cudaStream_t s) 
 }
 
 size_t tc_workspace_bytes(const psgd_config* cfg) {
-  if (cfg->err_dtype == PSGD_F32 || (cfg->flags & PSGD_FLAG_SIMT)) return 0;
+  if (cfg->err_dtype == PSGD_F32 || (cfg->flags & PSGD_FLAG_SIMT) || cfg->rank > kRankBlock) return 0;
   return tc_layout(cfg).total;
 }
 
 bool tc_supported(const psgd_config* cfg, std::string* why) {
   if (cfg->err_dtype == PSGD_F32) { if (why) *why = "fp32 gradients use the FFMA engine"; return false; }
+  if (cfg->rank > kRankBlock) { if (why) *why = "ranks above 128 use the FFMA engine"; return false; }
   int dev = 0, major = 0, minor = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);

@@ -50,7 +50,7 @@ def test_strerror(psgd):
     (dict(shapes=[(0, 32)], dtype="f16"), "positive"),
     (dict(shapes=[(64, 32)], dtype="f16", workers=0), ">= 1"),
     (dict(shapes=[(64, 32)], dtype="f16", skip_fraction=0.0), "skip_fraction"),
-    (dict(shapes=[(512, 512)], dtype="f16", rank=200), "above 128"),
+    (dict(shapes=[(2048, 2048)], dtype="f16", rank=1100), "above 1024"),
 ])
 def test_invalid_configs_are_rejected(psgd, kw, msg):
     args = dict(blocks=1, workers=2, rank=4, unc_len=0, skip_fraction=1.0)
@@ -59,6 +59,13 @@ def test_invalid_configs_are_rejected(psgd, kw, msg):
                               args.pop("dtype"), args["unc_len"], args["skip_fraction"])
     assert psgd.psgd_workspace_size(cfg) == 0
     assert msg in psgd.lib.psgd_last_error().decode()
+
+
+def test_ranks_above_128_are_planned(psgd):
+    """Ranks above the tensor engine's 128 (up to 1024) get a workspace: the FFMA engine
+    runs them, with the orthonormalisation in 128-column blocks."""
+    cfg, _ = psgd.make_config([(1024, 2048)], 1, 2, 896, "f16")
+    assert psgd.psgd_workspace_size(cfg) > 0
 
 
 def test_workspace_and_mask_layout(psgd):

@@ -165,17 +165,21 @@ def test_stack64_sampled_blocks():
     run_parity(wl, oracle_blocks=[0, 5, 6, 17, 30, 35, 36, 63])
 
 
-@pytest.mark.parametrize("rank", [16, 112])
+@pytest.mark.parametrize("rank", [16, 32, 64, 112, 256, 640, 896])
 def test_spectrum_rank_sweep(rank):
-    """3968x15872 fp16 gradient with singular values c/k, W = 8 identical copies.
+    """3968x15872 fp16 gradient with singular values c/k, W = 8 identical copies, 5 steps.
+    Ranks above 128 run on the FFMA engine with the orthonormalisation in 128-column
+    blocks (block Gram-Schmidt with re-orthogonalisation, CholeskyQR within a block).
 
-    After a warm start, P has condition number about r^2 (2.3e4 at r = 112), so rounding
-    in P is amplified into the span of P^. The bar is the plain 1e-4 on G-hat and on E
-    before storage. Also printed is the oracle's own change when its two GEMMs carry a
-    modelled fp32 accumulation error (u32 times the root sum of squared terms times 14).
-    That change is the size of difference that fp32 accumulation alone would explain."""
+    After a warm start, P has condition number about r^2 (up to 2e6 at r = 896), and
+    rounding in P is amplified into the span of P^. G-hat is held to the plain 1e-4. E is
+    held to max(1e-4, 4 s). Here s is the distance from the fp64 oracle of the same step
+    done with fp32 arithmetic where the method prescribes fp32: the orthonormalisation in
+    fp32 (shifted CholeskyQR), and the two GEMMs with modelled fp32 accumulation error.
+    At high rank E is only 2-4% of M, and s alone exceeds 1e-4 there (1.7e-4 for the
+    orthonormalisation at r = 896)."""
     import copy
-    wl = synth.spectrum(rank=rank, steps=2)
+    wl = synth.spectrum(rank=rank, steps=5)
     g = GpuRun(wl)
     o = OracleRun(wl, [0])
     for t in range(wl.steps):
@@ -186,12 +190,14 @@ def test_spectrum_rank_sweep(rank):
         torch.cuda.synchronize()
         res = o.step(t)
         grads = [[synth.grad(wl, t, 0, 0, w).double().numpy() for w in range(wl.workers)]]
-        pert = oracle.block_step(grads, before, wl.scale(0), wl.err_dtype, accum_noise=14.0)
+        pert = oracle.block_step(grads, copy.deepcopy(before), wl.scale(0), wl.err_dtype,
+                                 orth="cholqr_f32", accum_noise=14.0)
         sens_g = rel_err(pert.g_hat[0], res[0].g_hat[0])
         sens_e = rel_err(pert.e_pre[0][0], res[0].e_pre[0][0])
-        errs = compare_step(g, res, o, tol=TOL)
-        print(f"rank {rank} step {t}: GPU (G-hat, E, stored E) {errs}; "
-              f"oracle sensitivity to modelled fp32 accumulation (G-hat, E) ({sens_g:.2e}, {sens_e:.2e})")
+        tol = {"g": TOL, "e": max(TOL, 4 * sens_e)}
+        errs = compare_step(g, res, o, tol=lambda kind, b, j: tol[kind])
+        print(f"rank {rank} step {t}: GPU (G-hat, E, stored E) {errs}; fp32-method "
+              f"sensitivity (G-hat, E) ({sens_g:.2e}, {sens_e:.2e}); E bar {tol['e']:.2e}")
 
 
 # ------------------------------------------------------------------ properties

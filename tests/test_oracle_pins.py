@@ -366,3 +366,21 @@ def test_parameter_count_is_12B():
     "12B" of the pages ([card] 计算设置)."""
     assert 64 * 12 * 3968 ** 2 == 12_092_178_432
     assert 64 * sum(m * n for m, n in synth.SHARD_SHAPES) * 8 == 64 * 12 * 3968 ** 2
+
+
+def test_fp32_cholesky_qr_orthonormal_basis_of_span():
+    """The fp32 shifted CholeskyQR (used only to derive a tolerance) returns an
+    orthonormal basis of span(P) to fp32 accuracy: on a well-conditioned P, and on a P
+    with condition number 1e6 (the shift path), where the columns stay orthonormal and
+    the span of P's dominant part is kept."""
+    rng = np.random.default_rng(3)
+    p = rng.standard_normal((300, 24))
+    x = oracle.orthonormalize(p, "cholqr_f32")
+    assert np.abs(x.T @ x - np.eye(24)).max() < 1e-5
+    assert np.linalg.norm(x @ (x.T @ p) - p) / np.linalg.norm(p) < 1e-5
+    u = np.linalg.qr(rng.standard_normal((400, 32)))[0]
+    v = np.linalg.qr(rng.standard_normal((32, 32)))[0]
+    p = (u * np.logspace(0, -6, 32)) @ v.T
+    x = oracle.orthonormalize(p, "cholqr_f32")
+    assert np.abs(x.T @ x - np.eye(32)).max() < 1e-5
+    assert np.linalg.norm(x @ (x.T @ p) - p) / np.linalg.norm(p) < 1e-5
