@@ -53,22 +53,21 @@ __device__ __forceinline__ bool pass_skipped(const Plan& p, const MatMeta& mt, i
   return false;
 }
 
-// Upper triangle of X^T X for rows [0, nrows) of a shared-memory tile (64 x 128, zero
-// past r), one 8 x 8 block (bi <= bj) per thread, rows summed in order, into Gram
-// partial `chunk`. Threads without a block do nothing.
-__device__ void gram_rows(const MatMeta& mt, const float (*Xs)[128], int nrows, int r, int rp,
-                          int chunk) {
-  const int nb = (r + 7) / 8;
-  int bi = 0, rem = threadIdx.x;
-  while (bi < nb && rem >= nb - bi) { rem -= nb - bi; ++bi; }
-  if (bi >= nb) return;
-  const int bj = bi + rem;
-  float acc[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  for (int q = 0; q < nrows; ++q) {
+// Block b (0 <= b < nb (nb + 1) / 2) of the upper triangle of an nb x nb grid of 8 x 8
+// blocks, numbered row by row: (bi, bj) with bi <= bj.
+__device__ __forceinline__ void block_coords(int b, int nb, int& bi, int& bj) {
+  int i = 0, rem = b;
+  while (i < nb && rem >= nb - i) { rem -= nb - i; ++i; }
+  bi = i;
+  bj = i + rem;
+}
+
+// acc += rows [q0, q0 + 32) of Xs restricted to columns 8 bi.. x columns 8 bj.., row by
+// row in order.
+__device__ __forceinline__ void gram_block_rows(const float (*Xs)[128], int bi, int bj, int q0,
+                                                float (&acc)[8][8]) {
+#pragma unroll 4
+  for (int q = q0; q < q0 + 32; ++q) {
     float a[8], b[8];
     const float4 a0 = *reinterpret_cast<const float4*>(&Xs[q][bi * 8]);
     const float4 a1 = *reinterpret_cast<const float4*>(&Xs[q][bi * 8 + 4]);
@@ -81,7 +80,10 @@ __device__ void gram_rows(const MatMeta& mt, const float (*Xs)[128], int nrows, 
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
   }
-  float* out = mt.Gpart + (size_t)chunk * rp * rp;
+}
+
+__device__ __forceinline__ void gram_block_store(float* out, const float (&acc)[8][8], int bi,
+                                                 int bj, int r, int rp) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int ii = bi * 8 + i;
@@ -94,91 +96,139 @@ __device__ void gram_rows(const MatMeta& mt, const float (*Xs)[128], int nrows, 
   }
 }
 
-// Gram partial sums over a row chunk: the upper triangle of Gpart[c] = X_c^T X_c
-// (rp x rp, r <= 128) in 8 x 8 blocks, one block (bi <= bj) per thread; the lower
-// triangle is neither written nor read. grid = (max C, B*J), block kGramThreads.
-constexpr int kGramThreads = 160;  // >= 16 * 17 / 2 = 136 upper-triangle blocks
+// Upper triangle of X^T X for one 64-row chunk held in shared memory (Xs: 64 x 128, zero
+// past r and past the end of the matrix) into Gram partial `chunk`, in 8 x 8 blocks
+// (nb = ceil(r / 8), nb (nb + 1) / 2 <= 136 blocks). All kT = 256 threads of the block call
+// it (it holds block barriers). Thread t takes block t mod 128 and sums rows
+// [32 h, 32 h + 32) of the chunk in order, h = t / 128; the upper half's sums are added to
+// the lower half's through `red` (32 x 128 floats), four rows of the block at a time.
+// Blocks 128 and up (r > 120 only) are summed over all 64 rows by the upper half alone.
+// The partial is a fixed function of the chunk, whichever kernel calls this.
+constexpr int kGramThreads = kT;
+__device__ void gram_tile(const MatMeta& mt, const float (*Xs)[128], float* red, int r, int rp,
+                          int chunk) {
+  const int nb = (r + 7) / 8, nblk = nb * (nb + 1) / 2;
+  const int tid = threadIdx.x, h = tid >> 7, b = tid & 127;
+  float* out = mt.Gpart + (size_t)chunk * rp * rp;
+  const bool live = b < nblk;
+  int bi = 0, bj = 0;
+  if (live) block_coords(b, nb, bi, bj);
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  if (live) gram_block_rows(Xs, bi, bj, 32 * h, acc);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    if (h == 1 && live) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) red[(i * 8 + j) * 128 + b] = acc[4 * half + i][j];
+    }
+    __syncthreads();
+    if (h == 0 && live) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          acc[4 * half + i][j] = __fadd_rn(acc[4 * half + i][j], red[(i * 8 + j) * 128 + b]);
+    }
+    __syncthreads();
+  }
+  if (h == 0 && live) gram_block_store(out, acc, bi, bj, r, rp);
+  if (h == 1 && 128 + b < nblk) {
+    block_coords(128 + b, nb, bi, bj);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    gram_block_rows(Xs, bi, bj, 0, acc);
+    gram_block_rows(Xs, bi, bj, 32, acc);
+    gram_block_store(out, acc, bi, bj, r, rp);
+  }
+}
+
+// Gram partial of one 64-row chunk: Gpart[c] = X_c^T X_c (upper triangle; the lower one
+// is neither written nor read). The chunk is staged in shared memory with all of a
+// thread's loads issued before its stores. grid = (max C, B*J), block kGramThreads.
+static_assert(kGramRows == 64, "gram_tile sums 64-row chunks");
 __global__ void __launch_bounds__(kGramThreads) k_gram(Plan p, int pass) {
+  pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   if ((int)blockIdx.x >= mt.C || pass_skipped(p, mt, pass)) return;
   const int64_t m = mt.m;
   const int r = p.ob_r, rp = p.ob_rp, xl = p.rp;  // block width, Gram pitch, X row pitch
   const float* X = pass_src(p, mt, pass);
   const float sc = pass == 0 ? p_scale(mt) : 1.0f;
-  const int64_t rows_per = ((m + mt.C - 1) / mt.C + 31) / 32 * 32;
-  const int64_t rbeg = (int64_t)blockIdx.x * rows_per, rend = min(m, rbeg + rows_per);
-  __shared__ __align__(16) float Xs[32][128];
+  const int64_t row0 = (int64_t)blockIdx.x * kGramRows;
+  __shared__ __align__(16) float Xs[kGramRows][128];
+  __shared__ __align__(16) float red[32 * 128];
   const int tid = threadIdx.x;
-  // this thread's block (bi, bj), bi <= bj, of the nb x nb block grid
-  const int nb = (r + 7) / 8;
-  int bi = 0, rem = tid;
-  while (bi < nb && rem >= nb - bi) { rem -= nb - bi; ++bi; }
-  const bool live = bi < nb;
-  const int bj = bi + rem;
-  float acc[8][8];
+  if ((xl & 3) == 0 && (reinterpret_cast<uintptr_t>(X) & 15) == 0) {
+    float4 v[8];  // 64 rows x 32 float4
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  for (int64_t k0 = rbeg; k0 < rend; k0 += 32) {
-    for (int idx = tid; idx < 32 * 128; idx += kGramThreads) {
-      const int kk = idx >> 7, c = idx & 127;
-      const int64_t row = k0 + kk;
-      Xs[kk][c] = (row < rend && c < r) ? X[row * xl + c] * sc : 0.f;
+    for (int u = 0; u < 8; ++u) {
+      const int f = tid + kGramThreads * u, rr = f >> 5, c = (f & 31) * 4;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row0 + rr < m && c < r) v[u] = __ldg(reinterpret_cast<const float4*>(X + (row0 + rr) * xl + c));
     }
-    __syncthreads();
-    if (live) {
-#pragma unroll 4
-      for (int q = 0; q < 32; ++q) {
-        float a[8], b[8];
-        const float4 a0 = *reinterpret_cast<const float4*>(&Xs[q][bi * 8]);
-        const float4 a1 = *reinterpret_cast<const float4*>(&Xs[q][bi * 8 + 4]);
-        const float4 b0 = *reinterpret_cast<const float4*>(&Xs[q][bj * 8]);
-        const float4 b1 = *reinterpret_cast<const float4*>(&Xs[q][bj * 8 + 4]);
-        a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w; a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
-        b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w; b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-      }
+    for (int u = 0; u < 8; ++u) {
+      const int f = tid + kGramThreads * u, rr = f >> 5, c = (f & 31) * 4;
+      *reinterpret_cast<float4*>(&Xs[rr][c]) =
+          make_float4(c < r ? v[u].x * sc : 0.f, c + 1 < r ? v[u].y * sc : 0.f,
+                      c + 2 < r ? v[u].z * sc : 0.f, c + 3 < r ? v[u].w * sc : 0.f);
     }
-    __syncthreads();
-  }
-  if (!live) return;
-  float* out = mt.Gpart + (size_t)blockIdx.x * rp * rp;
+  } else {
+    float v[32];  // 64 rows x 128 floats
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int ii = bi * 8 + i;
-    if (ii >= r) continue;
+    for (int u = 0; u < 32; ++u) {
+      const int f = tid + kGramThreads * u, rr = f >> 7, c = f & 127;
+      v[u] = (row0 + rr < m && c < r) ? __ldg(X + (row0 + rr) * xl + c) : 0.f;
+    }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int jj = bj * 8 + j;
-      if (jj < r && jj >= ii) out[ii * rp + jj] = acc[i][j];
+    for (int u = 0; u < 32; ++u) {
+      const int f = tid + kGramThreads * u;
+      Xs[f >> 7][f & 127] = v[u] * sc;
     }
   }
+  __syncthreads();
+  gram_tile(mt, Xs, red, r, rp, blockIdx.x);
 }
 
-// G = sum_c Gpart[c] into slot C of Gpart (upper triangle). Eight threads share an entry: thread k sums
-// the partials c = k, k+8, ... in order, then the eight sums are added in a fixed tree
-// order (deterministic). grid = (ceil(rp*rp/32), B*J).
+// G = sum_c Gpart[c] into slot C of Gpart (upper triangle). A block takes 32 consecutive
+// entries of one row of G; warp w sums the partials c = w, w + 8, ... in order (one
+// 128-byte load per partial), and the eight warp sums are added in warp order.
+// grid = (rp * ceil(rp / 32), B*J).
 __global__ void __launch_bounds__(kT) k_gsum(Plan p, int pass) {
+  pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   if (pass_skipped(p, mt, pass)) return;
   const int rp = p.ob_rp;
-  const int idx = blockIdx.x * (kT / 8) + (threadIdx.x >> 3);
-  const int part = threadIdx.x & 7;
-  const bool live = idx < rp * rp && idx % rp >= idx / rp;  // upper triangle only
-  const float* src = mt.Gpart + (live ? idx : 0);
+  const int nseg = (rp + 31) / 32;
+  const int i = blockIdx.x / nseg, j0 = (blockIdx.x - i * nseg) * 32;
+  if (i >= rp || j0 + 31 < i) return;  // wholly below the diagonal
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = j0 + lane;
+  const bool live = j < rp && j >= i;
+  const size_t slot = (size_t)rp * rp;
+  const float* src = mt.Gpart + (size_t)i * rp + j;
   float s = 0.f;
   if (live) {
 #pragma unroll 8
-    for (int c = part; c < mt.C; c += 8) s = __fadd_rn(s, __ldg(src + (size_t)c * rp * rp));
+    for (int c = warp; c < mt.C; c += 8) s = __fadd_rn(s, __ldg(src + (size_t)c * slot));
   }
-  s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));
-  s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2));
-  s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 4));
-  if (live && part == 0) mt.Gpart[(size_t)mt.C * rp * rp + idx] = s;
+  __shared__ float part[8][32];
+  part[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && live) {
+    float t = part[0][lane];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) t = __fadd_rn(t, part[w][lane]);
+    mt.Gpart[(size_t)mt.C * slot + (size_t)i * rp + j] = t;
+  }
 }
 
 // ---------------------------------------------------------------- Cholesky + R^-1
@@ -223,17 +273,20 @@ __device__ __forceinline__ void load_gram_rows(const MatMeta& mt, int r, int rp,
   const float* src = mt.Gpart + (size_t)mt.C * rp * rp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-  for (int t = 0; t < kPanel; ++t) {
+  for (int t = 0; t < kPanel; ++t) {  // all loads first (upper triangle)
     const int i = warp * kPanel + t;
 #pragma unroll
     for (int q = QW; q < 4; ++q) {
       const int j = lane + 32 * q;
-      float v = (i < r && j < r && j >= i) ? src[(size_t)i * rp + j] : 0.f;  // upper triangle
-      if (i == j && i < r) {
-        if (record) S.diag0[i] = v;
-        v += shift;
-      }
-      a[t][q - QW] = v;
+      a[t][q - QW] = (i < r && j < r && j >= i) ? __ldg(src + (size_t)i * rp + j) : 0.f;
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kPanel; ++t) {  // then the diagonal: group QW, lane i mod 32
+    const int i = warp * kPanel + t;
+    if (i < r && lane == (i & 31)) {
+      if (record) S.diag0[i] = a[t][0];
+      a[t][0] += shift;
     }
   }
 }
@@ -420,6 +473,7 @@ __device__ void chol_main(const Plan& p, const MatMeta& mt, int pass, CholSmem& 
 
 // One CTA per matrix: factor the Gram matrix of this pass, decide shift/final, write R^-1.
 __global__ void __launch_bounds__(kCholThreads, 1) k_chol(Plan p, int pass) {
+  pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.x];
   if (pass_skipped(p, mt, pass)) return;
   extern __shared__ __align__(16) unsigned char chol_smem[];
@@ -434,6 +488,7 @@ __global__ void __launch_bounds__(kCholThreads, 1) k_chol(Plan p, int pass) {
 
 // X <- X R^-1 on 64-row tiles (R^-1 upper triangular, r <= 128). grid = (ceil(m/64), B*J).
 __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
+  pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   if (pass_skipped(p, mt, pass)) return;
   const int64_t m = mt.m;
@@ -446,6 +501,7 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   // As and Bs hold the operand chunks of the product; afterwards the same shared memory
   // holds this tile of Y for the next pass's Gram partial.
   __shared__ __align__(16) float smem_apply[64 * 128];
+  __shared__ __align__(16) float red_apply[32 * 128];  // gram_tile's reduction buffer
   float (*As)[64 + 4] = reinterpret_cast<float (*)[64 + 4]>(smem_apply);
   float (*Bs)[128] = reinterpret_cast<float (*)[128]>(smem_apply + 32 * (64 + 4));
   float (*Ys)[128] = reinterpret_cast<float (*)[128]>(smem_apply);
@@ -464,51 +520,49 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   const bool vec = (xl & 3) == 0 && (rp & 3) == 0 &&
                    ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Y) |
                      reinterpret_cast<uintptr_t>(mt.Rinv)) & 15) == 0;
-  for (int k0 = 0; k0 < r; k0 += 32) {
-    {
-      const int rr = tid >> 2, kk = (tid & 3) * 8;
-      const int64_t row = row0 + rr;
-      float x[8];
-      if (vec) {
+  // One 32-wide k chunk: this thread's 8 entries of X (row xr, columns k0 + xk ..) and 16
+  // of R^-1 (row k0 + bk, columns bc ..). The next chunk's loads go out before the FMAs
+  // of the current one, and every load of a chunk before its shared-memory stores.
+  const int xr = tid >> 2, xk = (tid & 3) * 8, bk = tid >> 3, bc = (tid & 7) * 16;
+  const int64_t xrow = row0 + xr;
+  float xv[8], bv[16];
+  auto load_chunk = [&](int k0) {
+    const int k = k0 + bk;
+    const float* rrow = mt.Rinv + (size_t)k * rp;
+    if (vec) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int k = k0 + kk + 4 * h;
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (row < m && k < rp) v = *reinterpret_cast<const float4*>(X + row * xl + k);
-          x[4 * h] = v.x; x[4 * h + 1] = v.y; x[4 * h + 2] = v.z; x[4 * h + 3] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = (row < m && k0 + kk + i < r) ? X[row * xl + k0 + kk + i] : 0.f;
+      for (int h = 0; h < 2; ++h) {
+        const int kx = k0 + xk + 4 * h;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (xrow < m && kx < rp) v = *reinterpret_cast<const float4*>(X + xrow * xl + kx);
+        xv[4 * h] = v.x; xv[4 * h + 1] = v.y; xv[4 * h + 2] = v.z; xv[4 * h + 3] = v.w;
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) As[kk + i][rr] = (k0 + kk + i < r) ? x[i] * sc : 0.f;
-    }
-    {
-      const int kk = tid >> 3, c = (tid & 7) * 16;
-      const int k = k0 + kk;
-      const float* rrow = mt.Rinv + (size_t)k * rp;
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        const int cc = c + 4 * h;
+        const int cc = bc + 4 * h;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (k < r) {
-          if (vec) {
-            if (cc < rp) v = *reinterpret_cast<const float4*>(rrow + cc);
-          } else {
-            v.x = cc < r ? rrow[cc] : 0.f;
-            v.y = cc + 1 < r ? rrow[cc + 1] : 0.f;
-            v.z = cc + 2 < r ? rrow[cc + 2] : 0.f;
-            v.w = cc + 3 < r ? rrow[cc + 3] : 0.f;
-          }
-        }
-        Bs[kk][cc] = cc < r ? v.x : 0.f;
-        Bs[kk][cc + 1] = cc + 1 < r ? v.y : 0.f;
-        Bs[kk][cc + 2] = cc + 2 < r ? v.z : 0.f;
-        Bs[kk][cc + 3] = cc + 3 < r ? v.w : 0.f;
+        if (k < r && cc < rp) v = __ldg(reinterpret_cast<const float4*>(rrow + cc));
+        bv[4 * h] = v.x; bv[4 * h + 1] = v.y; bv[4 * h + 2] = v.z; bv[4 * h + 3] = v.w;
       }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        xv[i] = (xrow < m && k0 + xk + i < r) ? X[xrow * xl + k0 + xk + i] : 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) bv[i] = (k < r && bc + i < r) ? __ldg(rrow + bc + i) : 0.f;
     }
+  };
+  auto store_chunk = [&](int k0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) As[xk + i][xr] = (k0 + xk + i < r) ? xv[i] * sc : 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Bs[bk][bc + i] = bc + i < r ? bv[i] : 0.f;
+  };
+  load_chunk(0);
+  for (int k0 = 0; k0 < r; k0 += 32) {
+    store_chunk(k0);
     __syncthreads();
+    if (k0 + 32 < r) load_chunk(k0 + 32);
 #pragma unroll 8
     for (int kk = 0; kk < 32; ++kk) {
       if (k0 > warp_last_col) break;  // warp-uniform: R^-1 rows k0.. are zero in this strip
@@ -562,7 +616,7 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
     }
   }
   __syncthreads();
-  gram_rows(mt, Ys, m - row0 < 64 ? (int)(m - row0) : 64, r, rp, blockIdx.x);
+  gram_tile(mt, Ys, red_apply, r, rp, blockIdx.x);
 }
 
 // ---------------------------------------------------------------- block Gram-Schmidt
@@ -714,6 +768,8 @@ __global__ void __launch_bounds__(kT) k_proj_apply(Plan p, int c0, int rb, int s
 }
 
 constexpr size_t kCholSmem = sizeof(CholSmem);
+// k_gsum: one block per 32-entry segment of a row of G.
+unsigned gsum_blocks(int rp) { return (unsigned)(rp * ((rp + 31) / 32)); }
 
 }  // namespace
 
@@ -739,12 +795,12 @@ cudaError_t launch_orth(const Handle& h, const Plan& p, cudaStream_t s) {
     }
     for (int pass = 0; pass < kMaxPasses; ++pass) {
       if (pass == 0) {  // later passes get their Gram partials from the previous k_apply
-        k_gram<<<dim3(h.max_C, BJ), kGramThreads, 0, s>>>(pb, pass);
+        launch_pdl(k_gram, dim3(h.max_C, BJ), dim3(kGramThreads), 0, s, pb, pass);
         h.launches += 1;
       }
-      k_gsum<<<dim3((pb.ob_rp * pb.ob_rp + kT / 8 - 1) / (kT / 8), BJ), kT, 0, s>>>(pb, pass);
-      k_chol<<<BJ, kCholThreads, kCholSmem, s>>>(pb, pass);
-      k_apply<<<dim3(h.max_mtiles64, BJ), kT, 0, s>>>(pb, pass);
+      launch_pdl(k_gsum, dim3(gsum_blocks(pb.ob_rp), BJ), dim3(kT), 0, s, pb, pass);
+      launch_pdl(k_chol, dim3(BJ), dim3(kCholThreads), kCholSmem, s, pb, pass);
+      launch_pdl(k_apply, dim3(h.max_mtiles64, BJ), dim3(kT), 0, s, pb, pass);
       h.launches += 3;
     }
   }
@@ -756,10 +812,10 @@ cudaError_t launch_orth_one(const Plan& p, int C, int mtiles64, cudaStream_t s) 
                                        (int)kCholSmem);
   if (e != cudaSuccess) return e;
   for (int pass = 0; pass < kMaxPasses; ++pass) {
-    if (pass == 0) k_gram<<<dim3(C, 1), kGramThreads, 0, s>>>(p, pass);
-    k_gsum<<<dim3((p.ob_rp * p.ob_rp + kT / 8 - 1) / (kT / 8), 1), kT, 0, s>>>(p, pass);
-    k_chol<<<1, kCholThreads, kCholSmem, s>>>(p, pass);
-    k_apply<<<dim3(mtiles64, 1), kT, 0, s>>>(p, pass);
+    if (pass == 0) launch_pdl(k_gram, dim3(C, 1), dim3(kGramThreads), 0, s, p, pass);
+    launch_pdl(k_gsum, dim3(gsum_blocks(p.ob_rp), 1), dim3(kT), 0, s, p, pass);
+    launch_pdl(k_chol, dim3(1), dim3(kCholThreads), kCholSmem, s, p, pass);
+    launch_pdl(k_apply, dim3(mtiles64, 1), dim3(kT), 0, s, p, pass);
   }
   return cudaGetLastError();
 }

@@ -81,6 +81,30 @@ struct Plan {
   int32_t ob_r, ob_rp, ob_c0, ob_src0;
 };
 
+// Programmatic dependent launch. A kernel launched by launch_pdl may be scheduled while
+// the kernel before it in the stream is still finishing; it calls pdl_wait() first, which
+// returns once that kernel has completed and its memory operations are visible, so none
+// of its reads or writes can overlap its predecessor's. Launched without the attribute,
+// pdl_wait() returns at once. What the overlap saves is the launch latency between the
+// short kernels of the step.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Max of v over the block, returned in thread 0 (every thread of the block must call it;
 // blockDim.x a multiple of 32). One atomic per block instead of one per warp: atomics on
 // one address serialise at its L2 slice.
@@ -96,6 +120,33 @@ __device__ __forceinline__ unsigned block_max_u32(unsigned v) {
     r = __reduce_max_sync(0xffffffffu, r);
   }
   return r;
+}
+
+// Stages the first `count` floats of a contiguous run src[0 .. count) into a 32-row
+// shared-memory tile xs (`len` entries per row, row stride kRankBlock + 1, count <= 32 *
+// len, len <= kRankBlock) as xs[i / len][i % len] = f(src[i], i % len); every other entry
+// of rows 0..31, columns 0..len-1 gets 0. Each thread issues all of its loads before its
+// first store: interleaved, every load would wait for the shared-memory store before it,
+// since the compiler cannot rule out that src points into shared memory. src is read
+// through the read-only path (it is not written during the kernel).
+template <int kThreads, typename F>
+__device__ __forceinline__ void stage_rows(float (*xs)[kRankBlock + 1], const float* src,
+                                           int count, int len, F f) {
+  constexpr int kPer = (32 * kRankBlock + kThreads - 1) / kThreads;
+  float v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = (int)threadIdx.x + u * kThreads;
+    v[u] = i < count ? __ldg(src + i) : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = (int)threadIdx.x + u * kThreads;
+    if (i < 32 * len) {
+      const int rr = i / len, c = i - rr * len;
+      xs[rr][c] = i < count ? f(v[u], c) : 0.f;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- numerics helpers

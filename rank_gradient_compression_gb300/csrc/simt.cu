@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(kT) k_qgemm(Plan p) {
 // Q = (sum_s Qpart[s]) * qscale / W in slice order -> the caller's fp32 Q state (n x r),
 // and max|Q| -> scal[3]. qscale undoes the power-of-two scale of a split P^ (exact).
 __global__ void __launch_bounds__(256) k_qreduce(Plan p, float qscale) {
+  pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
   // one warp per row of Q; lane covers columns lane, lane + 32, ...
@@ -343,7 +344,7 @@ cudaError_t launch_qreduce(const Handle& h, const Plan& p, cudaStream_t s) {
   int64_t max_n = 0;
   for (const MatMeta& mt : h.meta) max_n = std::max<int64_t>(max_n, mt.n);
   dim3 grid((unsigned)((max_n + 7) / 8), p.B * p.J);
-  k_qreduce<<<grid, 256, 0, s>>>(p, h.tc ? 0x1p-14f : 1.0f);
+  launch_pdl(k_qreduce, dim3(grid), dim3(256), 0, s, p, h.tc ? 0x1p-14f : 1.0f);
   h.launches += 1;
   return cudaGetLastError();
 }

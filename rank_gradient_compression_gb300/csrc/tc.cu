@@ -110,9 +110,10 @@ __device__ __forceinline__ void split3(float xs, uint16_t& hi, uint16_t& mid, ui
 // Number of 16-bit terms the fp32 operand of the P and Q GEMMs is split into.
 template <typename T> __host__ __device__ constexpr int nterms() { return sizeof(T) == 2 && !std::is_same<T, __half>::value ? 3 : 2; }
 
-// max|Q| of the caller's Q state -> scal[2] (bits). grid = (64, B*J). This and k_qsplit
+// max|Q| of the caller's Q state -> scal[2] (bits). grid = (qmax_blocks, B*J). This and k_qsplit
 // run for every matrix: they can precede the skip decision of the step.
 __global__ void k_qmax(Plan p) {
+  pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   const float* q = p.tab.q[blockIdx.y];
   const int64_t total = mt.n * p.r;
@@ -130,6 +131,7 @@ __global__ void k_qmax(Plan p) {
 // of 8, so a group of 8 is wholly inside or outside the matrix). grid = (ceil(n/32), B*J).
 template <typename T>
 __global__ void __launch_bounds__(256) k_qsplit(Plan p) {
+  pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   const int64_t j0 = (int64_t)blockIdx.x * 32;
   if (j0 >= mt.n) return;
@@ -139,10 +141,7 @@ __global__ void __launch_bounds__(256) k_qsplit(Plan p) {
   const int64_t left = mt.n - j0;
   const int nrows = left < 32 ? (int)left : 32;
   const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[2]);
-  for (int idx = threadIdx.x; idx < nrows * r; idx += blockDim.x) {
-    const int rr = idx / r, c = idx - rr * r;
-    xs[rr][c] = ldexpf(q[idx], e);
-  }
+  stage_rows<256>(xs, q, nrows * r, r, [e](float v, int) { return ldexpf(v, e); });
   __syncthreads();
   for (int it = threadIdx.x; it < rp * 4; it += blockDim.x) {
     const int c = it >> 2, g = it & 3;
@@ -169,6 +168,7 @@ __global__ void __launch_bounds__(256) k_qsplit(Plan p) {
 // below fp32's range when both M and Q are tiny (deep blocks of the stack, M ~ Q ~ 2^-80).
 // grid = (ceil(m*rp / 256), B*J).
 __global__ void k_preduce(Plan p, int pchunk_kb) {
+  pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
   const int rp = p.rp;
@@ -204,6 +204,7 @@ __global__ void k_preduce(Plan p, int pchunk_kb) {
 // per 16-byte store. grid = (mpad / 32, B*J).
 template <typename T>
 __global__ void __launch_bounds__(256) k_psplit(Plan p, int kp) {
+  pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
   const int64_t mpad = (mt.m + 127) / 128 * 128;
@@ -214,10 +215,8 @@ __global__ void __launch_bounds__(256) k_psplit(Plan p, int kp) {
   const int64_t left = mt.m - row0;
   const int nrows = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
   const float* src = mt.Phat + row0 * rp;
-  for (int idx = threadIdx.x; idx < 32 * rp; idx += blockDim.x) {
-    const int rr = idx / rp, c = idx - rr * rp;
-    xs[rr][c] = (rr < nrows && c < r) ? src[idx] * 16384.0f : 0.f;  // * 2^14, exact
-  }
+  stage_rows<256>(xs, src, nrows * rp, rp,  // * 2^14, exact
+                  [r](float v, int c) { return c < r ? v * 16384.0f : 0.f; });
   __syncthreads();
   // pdec rows: [hi | lo | hi], kp / 8 groups of 8 columns per segment
   const int gpr = kp / 8;
@@ -253,6 +252,7 @@ __global__ void __launch_bounds__(256) k_psplit(Plan p, int kp) {
 // A block stages 32 rows of Q (n x r row-major) in shared memory and writes 8 columns
 // per 16-byte store. grid = (npad / 32, B*J).
 __global__ void __launch_bounds__(256) k_qdec(Plan p, int kp) {
+  pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
   const int64_t npad = (mt.n + DEC_NT - 1) / DEC_NT * DEC_NT;
@@ -264,10 +264,7 @@ __global__ void __launch_bounds__(256) k_qdec(Plan p, int kp) {
   const int nrows = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
   const int e = 14 - exp_of_max(reinterpret_cast<const unsigned*>(mt.scal)[3]);
   const float* q = p.tab.q[blockIdx.y] + row0 * r;
-  for (int idx = threadIdx.x; idx < nrows * r; idx += blockDim.x) {
-    const int rr = idx / r, c = idx - rr * r;
-    xs[rr][c] = ldexpf(q[idx], e);
-  }
+  stage_rows<256>(xs, q, nrows * r, r, [e](float v, int) { return ldexpf(v, e); });
   __syncthreads();
   const int gpr = kp / 8;
   for (int it = threadIdx.x; it < 32 * gpr; it += blockDim.x) {
@@ -317,6 +314,7 @@ template <bool MN_A, bool BF16>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
        int a_stages, uint32_t b_stage, int only_shifted, int seg) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   GemmSmem S{base, base + (size_t)a_stages * A_BYTES,
@@ -883,6 +881,7 @@ struct DecSmem {
 template <typename TE>
 __global__ void __launch_bounds__(DEC_THREADS, 1)
 k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits, int kp) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   DecSmem& sm = *reinterpret_cast<DecSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1249,7 +1248,7 @@ cudaError_t launch_rescale_tiny(const Handle& h, const Plan& p, cudaStream_t s) 
   const uint32_t bst = gemm_b_stage(h.edt, p.rp);
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
-  k_gemm<false, true><<<grid, kGemmThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 1, kGemmSegSteps);
+  launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 1, kGemmSegSteps);
   h.launches += 1;
   return cudaGetLastError();
 }
@@ -1365,18 +1364,22 @@ void tc_free(Handle& h) {
   h.tc_plan = nullptr;
 }
 
+// Blocks per matrix of k_qmax: about 2048 blocks in all (a few loads per thread for the
+// resblock-shard sizes), at least 8 per matrix.
+static unsigned qmax_blocks(int BJ) { return (unsigned)std::min(256, std::max(8, 2048 / std::max(BJ, 1))); }
+
 cudaError_t launch_qmax(const Handle& h, const Plan& p, cudaStream_t s) {
-  k_qmax<<<dim3(64, p.B * p.J), 256, 0, s>>>(p);
+  launch_pdl(k_qmax, dim3(qmax_blocks(p.B * p.J), p.B * p.J), dim3(256), 0, s, p);
   h.launches += 1;
   return cudaGetLastError();
 }
 
 cudaError_t launch_prep_q(const Handle& h, const Plan& p, cudaStream_t s) {
   const int BJ = p.B * p.J;
-  k_qmax<<<dim3(64, BJ), 256, 0, s>>>(p);
+  launch_pdl(k_qmax, dim3(qmax_blocks(BJ), BJ), dim3(256), 0, s, p);
   dim3 g((unsigned)((h.max_ntiles64 * 64 + 31) / 32), BJ);
-  if (h.edt == DT_BF16) k_qsplit<__nv_bfloat16><<<g, 256, 0, s>>>(p);
-  else k_qsplit<__half><<<g, 256, 0, s>>>(p);
+  if (h.edt == DT_BF16) launch_pdl(k_qsplit<__nv_bfloat16>, dim3(g), dim3(256), 0, s, p);
+  else launch_pdl(k_qsplit<__half>, dim3(g), dim3(256), 0, s, p);
   h.launches += 2;
   return cudaGetLastError();
 }
@@ -1388,11 +1391,11 @@ cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
   const int seg = kGemmSegSteps;
-  if (h.edt == DT_BF16) k_gemm<false, true><<<grid, kGemmThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg);
-  else k_gemm<false, false><<<grid, kGemmThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg);
+  if (h.edt == DT_BF16) launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg);
+  else launch_pdl(k_gemm<false, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg);
   int64_t maxe = 0;
   for (const MatMeta& mt : h.meta) maxe = std::max<int64_t>(maxe, mt.m * p.rp);
-  k_preduce<<<dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), 256, 0, s>>>(p, PCHUNK_KB);
+  launch_pdl(k_preduce, dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), dim3(256), 0, s, p, PCHUNK_KB);
   h.launches += 2;
   return cudaGetLastError();
 }
@@ -1414,7 +1417,7 @@ cudaError_t launch_ingest_p(const Handle& h, const Plan& p, cudaStream_t s) {
 cudaError_t launch_preduce(const Handle& h, const Plan& p, cudaStream_t s) {
   int64_t maxe = 0;
   for (const MatMeta& mt : h.meta) maxe = std::max<int64_t>(maxe, mt.m * p.rp);
-  k_preduce<<<dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), 256, 0, s>>>(p, PCHUNK_KB);
+  launch_pdl(k_preduce, dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), dim3(256), 0, s, p, PCHUNK_KB);
   h.launches += 1;
   return cudaGetLastError();
 }
@@ -1422,15 +1425,15 @@ cudaError_t launch_preduce(const Handle& h, const Plan& p, cudaStream_t s) {
 cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
   dim3 g((unsigned)h.max_mtiles * 4, p.B * p.J);
-  if (h.edt == DT_BF16) k_psplit<__nv_bfloat16><<<g, 256, 0, s>>>(p, tp->kp);
-  else k_psplit<__half><<<g, 256, 0, s>>>(p, tp->kp);
+  if (h.edt == DT_BF16) launch_pdl(k_psplit<__nv_bfloat16>, dim3(g), dim3(256), 0, s, p, tp->kp);
+  else launch_pdl(k_psplit<__half>, dim3(g), dim3(256), 0, s, p, tp->kp);
   const int grid = std::min(tp->grid, tp->nq);
   const uint32_t bst = gemm_b_stage(h.edt, p.rp);
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
   const int seg = kGemmSegSteps;
-  if (h.edt == DT_BF16) k_gemm<true, true><<<grid, kGemmThreads, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg);
-  else k_gemm<true, false><<<grid, kGemmThreads, sm, s>>>(p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg);
+  if (h.edt == DT_BF16) launch_pdl(k_gemm<true, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg);
+  else launch_pdl(k_gemm<true, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg);
   h.launches += 2;
   return cudaGetLastError();
 }
@@ -1438,10 +1441,10 @@ cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
 cudaError_t launch_decomp_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
   dim3 g((unsigned)h.max_ntiles128 * 4, p.B * p.J);
-  k_qdec<<<g, 256, 0, s>>>(p, tp->kp);
+  launch_pdl(k_qdec, dim3(g), dim3(256), 0, s, p, tp->kp);
   const int grid = std::min(tp->grid, tp->nd);
-  if (h.edt == DT_BF16) k_decomp_tc<__nv_bfloat16><<<grid, DEC_THREADS, dec_smem(), s>>>(p, tp->d_maps, tp->d_dunits, tp->nd, tp->kp);
-  else k_decomp_tc<__half><<<grid, DEC_THREADS, dec_smem(), s>>>(p, tp->d_maps, tp->d_dunits, tp->nd, tp->kp);
+  if (h.edt == DT_BF16) launch_pdl(k_decomp_tc<__nv_bfloat16>, dim3(grid), dim3(DEC_THREADS), dec_smem(), s, p, tp->d_maps, tp->d_dunits, tp->nd, tp->kp);
+  else launch_pdl(k_decomp_tc<__half>, dim3(grid), dim3(DEC_THREADS), dec_smem(), s, p, tp->d_maps, tp->d_dunits, tp->nd, tp->kp);
   h.launches += 2;
   return cudaGetLastError();
 }
