@@ -263,70 +263,77 @@ struct CholSmem {
   int ndead;
 };
 
-// The rows of warp w are i in [8w, 8w + 8), all in column group QW = w / 4 (32 columns
-// each). Of G (becoming R) only the groups q >= QW matter (columns >= i), and of
-// Z = R^-T only the groups q <= QW (columns <= i); each warp keeps just those in
-// registers: a[t][q - QW] and z[t][q].
-template <int QW>
-__device__ __forceinline__ void load_gram_rows(const MatMeta& mt, int r, int rp, float (&a)[kPanel][4 - QW],
-                                               float shift, CholSmem& S, bool record) {
+// Warp w holds rows i in [8w, 8w + 8) of G (becoming R) in a[t][q] and of Z = R^-T in
+// z[t][q], column j = lane + 32 q. One code body for every warp, with the loops that
+// only address shared memory kept rolled: a per-warp specialisation of the register
+// arrays would be smaller in arithmetic but overflows the instruction cache.
+__device__ __forceinline__ float sel4(const float (&v)[4], int q) {  // q warp-uniform
+  return q == 0 ? v[0] : q == 1 ? v[1] : q == 2 ? v[2] : v[3];
+}
+
+__device__ __forceinline__ void load_gram_rows(const MatMeta& mt, int r, int rp,
+                                               float (&a)[kPanel][4], float shift, CholSmem& S,
+                                               bool record) {
   const float* src = mt.Gpart + (size_t)mt.C * rp * rp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int t = 0; t < kPanel; ++t) {  // all loads first (upper triangle)
     const int i = warp * kPanel + t;
 #pragma unroll
-    for (int q = QW; q < 4; ++q) {
+    for (int q = 0; q < 4; ++q) {
       const int j = lane + 32 * q;
-      a[t][q - QW] = (i < r && j < r && j >= i) ? __ldg(src + (size_t)i * rp + j) : 0.f;
+      a[t][q] = (i < r && j < r && j >= i) ? __ldg(src + (size_t)i * rp + j) : 0.f;
     }
   }
+  const int qw = warp >> 2;  // the diagonal of row i sits in group i / 32 = warp / 4
 #pragma unroll
-  for (int t = 0; t < kPanel; ++t) {  // then the diagonal: group QW, lane i mod 32
+  for (int t = 0; t < kPanel; ++t) {
     const int i = warp * kPanel + t;
     if (i < r && lane == (i & 31)) {
-      if (record) S.diag0[i] = a[t][0];
-      a[t][0] += shift;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q == qw) {
+          if (record) S.diag0[i] = a[t][q];
+          a[t][q] += shift;
+        }
     }
   }
 }
 
-template <int QW>
-__device__ __forceinline__ void identity_rows(float (&z)[kPanel][QW + 1]) {
+__device__ __forceinline__ void identity_rows(float (&z)[kPanel][4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int t = 0; t < kPanel; ++t)
 #pragma unroll
-    for (int q = 0; q <= QW; ++q) z[t][q] = (warp * kPanel + t == lane + 32 * q) ? 1.f : 0.f;
+    for (int q = 0; q < 4; ++q) z[t][q] = (warp * kPanel + t == lane + 32 * q) ? 1.f : 0.f;
 }
 
-// Factor the registers' panels in place (rows of R in a, rows of Z = R^-T in z, which must
-// start as I) and fill S.R (groups >= the row's own), S.dead, S.ratio.
-template <int QW>
-__device__ void cholesky_panels(float (&a)[kPanel][4 - QW], float (&z)[kPanel][QW + 1], int r,
+// Factor the registers' panels in place (a: rows of G -> R; z: rows of I -> Z = R^-T) and
+// fill S.R, S.dead, S.ratio.
+__device__ void cholesky_panels(float (&a)[kPanel][4], float (&z)[kPanel][4], int r,
                                 float dead_tol, CholSmem& S) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int npan = (r + kPanel - 1) / kPanel;
   for (int pn = 0; pn < npan; ++pn) {
     const int k0 = pn * kPanel;
+    const int qg = pn >> 2;  // column group of this panel's pivots
     float* Zp = S.X[pn & 1];
-    if (warp == pn) {  // the owner: its pivots are in its own group QW (a[.][0])
+    if (warp == pn) {  // the owner
 #pragma unroll
       for (int t = 0; t < kPanel; ++t) {
         const int k = k0 + t;
         if (k < r) {
-          const float d = __shfl_sync(0xffffffffu, a[t][0], k & 31);
+          const float d = __shfl_sync(0xffffffffu, sel4(a[t], qg), k & 31);
           const float d0 = S.diag0[k];
           const bool bad = !(d > dead_tol * d0) || !isfinite(d) || !(d0 > 0.f);
           const float rkk = bad ? 1.f : sqrtf(d);
           const float inv = __frcp_rn(rkk);
 #pragma unroll
-          for (int q = QW; q < 4; ++q) {
+          for (int q = 0; q < 4; ++q) {
             const int j = lane + 32 * q;
-            a[t][q - QW] = j < k ? 0.f : (j == k ? rkk : (bad ? 0.f : a[t][q - QW] * inv));
+            a[t][q] = j < k ? 0.f : (j == k ? rkk : (bad ? 0.f : a[t][q] * inv));
+            z[t][q] *= inv;
           }
-#pragma unroll
-          for (int q = 0; q <= QW; ++q) z[t][q] *= inv;
           if (lane == 0) {
             S.dead[k] = bad;
             S.ratio[k] = bad ? 0.f : __fdividef(d, d0);  // statistics only
@@ -334,11 +341,12 @@ __device__ void cholesky_panels(float (&a)[kPanel][4 - QW], float (&z)[kPanel][Q
           // the rows below k in this panel
 #pragma unroll
           for (int t2 = t + 1; t2 < kPanel; ++t2) {
-            const float c = __shfl_sync(0xffffffffu, a[t][0], (k0 + t2) & 31);
+            const float c = __shfl_sync(0xffffffffu, sel4(a[t], qg), (k0 + t2) & 31);
 #pragma unroll
-            for (int q = 0; q < 4 - QW; ++q) a[t2][q] = fmaf(-c, a[t][q], a[t2][q]);
-#pragma unroll
-            for (int q = 0; q <= QW; ++q) z[t2][q] = fmaf(-c, z[t][q], z[t2][q]);
+            for (int q = 0; q < 4; ++q) {
+              a[t2][q] = fmaf(-c, a[t][q], a[t2][q]);
+              z[t2][q] = fmaf(-c, z[t][q], z[t2][q]);
+            }
           }
         }
       }
@@ -346,52 +354,55 @@ __device__ void cholesky_panels(float (&a)[kPanel][4 - QW], float (&z)[kPanel][Q
       for (int t = 0; t < kPanel; ++t)
         if (k0 + t < r) {
 #pragma unroll
-          for (int q = QW; q < 4; ++q) S.R[(k0 + t) * kRsLd + lane + 32 * q] = a[t][q - QW];
-#pragma unroll
-          for (int q = 0; q < 4; ++q)  // groups past QW are zero; later warps read them
-            Zp[t * kRsLd + lane + 32 * q] = q <= QW ? z[t][q < QW ? q : QW] : 0.f;
+          for (int q = 0; q < 4; ++q) {
+            S.R[(k0 + t) * kRsLd + lane + 32 * q] = a[t][q];
+            Zp[t * kRsLd + lane + 32 * q] = z[t][q];
+          }
         }
     }
     __syncthreads();
     if (warp > pn) {
       const int kend = min(kPanel, r - k0);
       const int i0 = warp * kPanel;
-#pragma unroll
-      for (int pp = 0; pp < kPanel; ++pp) {
-        if (pp >= kend) break;
+#pragma unroll 1
+      for (int pp = 0; pp < kend; ++pp) {
         const float* Rk = S.R + (k0 + pp) * kRsLd;
         const float* Zk = Zp + pp * kRsLd;
-        float rj[4 - QW], zj[QW + 1];
+        float rj[4], zj[4], c[kPanel];
 #pragma unroll
-        for (int q = QW; q < 4; ++q) rj[q - QW] = Rk[lane + 32 * q];
+        for (int q = 0; q < 4; ++q) { rj[q] = Rk[lane + 32 * q]; zj[q] = Zk[lane + 32 * q]; }
 #pragma unroll
-        for (int q = 0; q <= QW; ++q) zj[q] = Zk[lane + 32 * q];
+        for (int t = 0; t < kPanel; ++t) c[t] = Rk[i0 + t];
 #pragma unroll
         for (int t = 0; t < kPanel; ++t) {  // rows i >= r hold zeros and stay unused
-          const float c = Rk[i0 + t];
 #pragma unroll
-          for (int q = 0; q < 4 - QW; ++q) a[t][q] = fmaf(-c, rj[q], a[t][q]);
-#pragma unroll
-          for (int q = 0; q <= QW; ++q) z[t][q] = fmaf(-c, zj[q], z[t][q]);
+          for (int q = 0; q < 4; ++q) {
+            a[t][q] = fmaf(-c[t], rj[q], a[t][q]);
+            z[t][q] = fmaf(-c[t], zj[q], z[t][q]);
+          }
         }
       }
     }
   }
 }
 
-// The body of k_chol for the warps of row group QW (every instance meets the same block
-// barriers in the same order: every branch below is uniform over the block).
-template <int QW>
-__device__ void chol_main(const Plan& p, const MatMeta& mt, int pass, CholSmem& S) {
+// One CTA per matrix: factor the Gram matrix of this pass, decide shift/final, write R^-1.
+// Every branch that holds a block barrier is uniform over the block.
+__global__ void __launch_bounds__(kCholThreads, 1) k_chol(Plan p, int pass) {
+  pdl_wait();
+  const MatMeta& mt = p.meta[blockIdx.x];
+  if (pass_skipped(p, mt, pass)) return;
+  extern __shared__ __align__(16) unsigned char chol_smem[];
+  CholSmem& S = *reinterpret_cast<CholSmem*>(chol_smem);
   const int r = p.ob_r, rp = p.ob_rp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool last = pass == kMaxPasses - 1;
   int* st = mt.ostate + pass * 4;
   const int src = pass == 0 ? 0 : mt.ostate[(pass - 1) * 4 + 1];
 
-  float a[kPanel][4 - QW], z[kPanel][QW + 1];
-  identity_rows<QW>(z);
-  load_gram_rows<QW>(mt, r, rp, a, 0.f, S, true);
+  float a[kPanel][4], z[kPanel][4];
+  identity_rows(z);
+  load_gram_rows(mt, r, rp, a, 0.f, S, true);
   __syncthreads();
   if (warp == 0) {  // trace: fixed-order warp reduction
     float t = 0.f;
@@ -411,7 +422,7 @@ __device__ void chol_main(const Plan& p, const MatMeta& mt, int pass, CholSmem& 
     }
     __syncthreads();
   } else {
-    cholesky_panels<QW>(a, z, r, last ? 0x1p-40f : 0x1p-16f, S);
+    cholesky_panels(a, z, r, last ? 0x1p-40f : 0x1p-16f, S);
     __syncthreads();
     int nd = 0;
     for (int k = lane; k < r; k += 32) nd += S.dead[k];
@@ -419,10 +430,10 @@ __device__ void chol_main(const Plan& p, const MatMeta& mt, int pass, CholSmem& 
     if (nd > 0 && !last) {
       shifted = true;
       const float shift = 0x1p-20f * sqrtf((float)mt.m) * trace;
-      load_gram_rows<QW>(mt, r, rp, a, shift, S, false);
-      identity_rows<QW>(z);
+      load_gram_rows(mt, r, rp, a, shift, S, false);
+      identity_rows(z);
       __syncthreads();
-      cholesky_panels<QW>(a, z, r, 0x1p-40f, S);
+      cholesky_panels(a, z, r, 0x1p-40f, S);
       __syncthreads();
     }
   }
@@ -444,8 +455,7 @@ __device__ void chol_main(const Plan& p, const MatMeta& mt, int pass, CholSmem& 
     nd = __reduce_add_sync(0xffffffffu, nd);
     if (lane == 0) { S.maxr = mx; S.minr = mn; S.minratio = mr; S.ndead = nd; }
   }
-  // R^-1 = Z^T to global (this warp's Z rows j are R^-1's columns j), dead columns zeroed;
-  // the groups past QW are zero (i > j).
+  // R^-1 = Z^T to global (this warp's Z rows j are R^-1's columns j), dead columns zeroed.
   float* Ri = mt.Rinv;
 #pragma unroll
   for (int t = 0; t < kPanel; ++t) {
@@ -455,7 +465,7 @@ __device__ void chol_main(const Plan& p, const MatMeta& mt, int pass, CholSmem& 
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int i = lane + 32 * q;
-        if (i < r) Ri[i * rp + j] = (q <= QW && i <= j && !dj) ? z[t][q <= QW ? q : QW] : 0.f;
+        if (i < r) Ri[i * rp + j] = (i <= j && !dj) ? z[t][q] : 0.f;
       }
     }
   }
@@ -468,21 +478,6 @@ __device__ void chol_main(const Plan& p, const MatMeta& mt, int pass, CholSmem& 
     st[1] = fin ? 3 : (src == 1 ? 2 : 1);
     st[2] = shifted ? 1 : 0;
     st[3] = S.ndead;
-  }
-}
-
-// One CTA per matrix: factor the Gram matrix of this pass, decide shift/final, write R^-1.
-__global__ void __launch_bounds__(kCholThreads, 1) k_chol(Plan p, int pass) {
-  pdl_wait();
-  const MatMeta& mt = p.meta[blockIdx.x];
-  if (pass_skipped(p, mt, pass)) return;
-  extern __shared__ __align__(16) unsigned char chol_smem[];
-  CholSmem& S = *reinterpret_cast<CholSmem*>(chol_smem);
-  switch (threadIdx.x >> 7) {  // row group = warp / 4
-    case 0: chol_main<0>(p, mt, pass, S); break;
-    case 1: chol_main<1>(p, mt, pass, S); break;
-    case 2: chol_main<2>(p, mt, pass, S); break;
-    default: chol_main<3>(p, mt, pass, S); break;
   }
 }
 
