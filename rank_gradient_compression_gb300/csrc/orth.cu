@@ -217,8 +217,18 @@ __global__ void __launch_bounds__(kT) k_gsum(Plan p, int pass) {
   const float* src = mt.Gpart + (size_t)i * rp + j;
   float s = 0.f;
   if (live) {
-#pragma unroll 8
-    for (int c = warp; c < mt.C; c += 8) s = __fadd_rn(s, __ldg(src + (size_t)c * slot));
+    const int C = mt.C;
+    for (int c0 = warp; c0 < C; c0 += 8 * 16) {  // 16 loads in flight, then 16 adds in order
+      float v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int c = c0 + 8 * u;
+        v[u] = c < C ? __ldg(src + (size_t)c * slot) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (c0 + 8 * u < C) s = __fadd_rn(s, v[u]);
+    }
   }
   __shared__ float part[8][32];
   part[warp][lane] = s;
@@ -455,17 +465,32 @@ __global__ void __launch_bounds__(kCholThreads, 1) k_chol(Plan p, int pass) {
     nd = __reduce_add_sync(0xffffffffu, nd);
     if (lane == 0) { S.maxr = mx; S.minr = mn; S.minratio = mr; S.ndead = nd; }
   }
-  // R^-1 = Z^T to global (this warp's Z rows j are R^-1's columns j), dead columns zeroed.
+  // R^-1 = Z^T to global, dead columns zeroed: this warp's Z rows j = 8 warp + t are R^-1's
+  // columns j, so each thread holds 8 consecutive entries of R^-1 rows i = lane + 32 q,
+  // written as two 16-byte stores when the pitch and the base allow.
   float* Ri = mt.Rinv;
+  const int j0 = warp * kPanel;
+  if (j0 < r) {
+    bool live[kPanel];
 #pragma unroll
-  for (int t = 0; t < kPanel; ++t) {
-    const int j = warp * kPanel + t;
-    if (j < r) {
-      const bool dj = S.dead[j] != 0;
+    for (int t = 0; t < kPanel; ++t) live[t] = j0 + t < r && S.dead[j0 + t] == 0;
+    const bool vec = j0 + kPanel <= r && (rp & 3) == 0 &&
+                     (reinterpret_cast<uintptr_t>(Ri) & 15) == 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = lane + 32 * q;
-        if (i < r) Ri[i * rp + j] = (i <= j && !dj) ? z[t][q] : 0.f;
+    for (int q = 0; q < 4; ++q) {
+      const int i = lane + 32 * q;
+      if (i >= r) continue;
+      float v[kPanel];
+#pragma unroll
+      for (int t = 0; t < kPanel; ++t) v[t] = (i <= j0 + t && live[t]) ? z[t][q] : 0.f;
+      float* row = Ri + (size_t)i * rp + j0;
+      if (vec) {
+        *reinterpret_cast<float4*>(row) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(row + 4) = make_float4(v[4], v[5], v[6], v[7]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < kPanel; ++t)
+          if (j0 + t < r) row[t] = v[t];
       }
     }
   }
