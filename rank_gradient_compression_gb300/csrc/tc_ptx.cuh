@@ -53,9 +53,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
 }
 
 // ------------------------------------------------------------------ TMA
-__device__ __forceinline__ void tma_prefetch_desc(const void* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -77,14 +74,6 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
-// Wait until all but the n most recent committed bulk stores of this thread have finished
-// reading shared memory (n clamped to 0..3).
-__device__ __forceinline__ void bulk_wait_read_leq(int n) {
-  if (n <= 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-  else if (n == 1) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-  else if (n == 2) asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
-  else asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
-}
 // Wait until every committed bulk store of this thread is complete.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int x, int y, int z,
@@ -93,15 +82,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int x, i
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Untiled bulk copy global -> shared, completing on an mbarrier (16-byte aligned
-// addresses, size a multiple of 16 bytes).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 
