@@ -43,11 +43,12 @@ constexpr int B_STAGES = 2;
 constexpr int PCHUNK_KB = 4;           // P GEMM: k-blocks of 64 columns per unit
 // Accumulator segments. The tensor cores' fp32 accumulation loses about 2^-24 of the
 // accumulator per chained MMA, and those losses add up (they do not cancel like
-// round-to-nearest errors). So no accumulator chains more than a few MMAs: after each
+// round-to-nearest errors). So an accumulator chains a bounded number of MMAs: after each
 // segment of (k-block, worker) steps the epilogue adds the accumulator into a running sum
 // with round-to-nearest fp32 adds. In both GEMM kernels each K step issues one MMA per
 // split term of the fp32 operand into the same accumulator of rp columns, so a step
-// chains 8 (fp16) or 12 (bf16) MMAs. The separate GEMMs keep the running sum in
+// chains 8 (fp16) or 12 (bf16) MMAs: a Q GEMM segment of 16 steps chains 128 (fp16), a
+// fused P GEMM segment of 4 steps 32. The separate GEMMs keep the running sum in
 // registers and rotate four accumulators; the fused ingest kernel keeps it in TMEM next
 // to two accumulators. P's segments are shorter than Q's: errors in P are amplified by
 // cond(P) in the span of P^ (up to ~2e4 for a decaying spectrum at r = 112), errors in
