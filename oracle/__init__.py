@@ -9,13 +9,13 @@ from .numerics import (FORMATS, decode_bits, is_representable, max_finite, min_n
                        min_subnormal, round_to_format)
 from .powersgd import (BlockResult, BlockState, PowerStepResult, accumulate_error,
                        block_step, compressed_fraction, error_update, orthonormalize,
-                       power_step, skip_block, skip_threshold, uncompressed_mean,
-                       unscale_and_mask)
+                       power_step, scale_update, skip_block, skip_threshold,
+                       uncompressed_mean, unscale_and_mask)
 
 __all__ = [
     "FORMATS", "decode_bits", "is_representable", "max_finite", "min_normal",
     "min_subnormal", "round_to_format", "BlockResult", "BlockState", "PowerStepResult",
     "accumulate_error", "block_step", "compressed_fraction", "error_update",
-    "orthonormalize", "power_step", "skip_block", "skip_threshold", "uncompressed_mean",
-    "unscale_and_mask",
+    "orthonormalize", "power_step", "scale_update", "skip_block", "skip_threshold",
+    "uncompressed_mean", "unscale_and_mask",
 ]

@@ -30,6 +30,9 @@ Parity status per function:
     invariance (Householder vs Gram-Schmidt), the error-feedback identity and the
     Eckart-Young bound.
   uncompressed_mean: pinned by a hand-worked example and the nonfinite brute force.
+  scale_update: pinned by the closed form 2^(e0 + growths - backoffs) for power-of-two
+    factors over a long random finite/nonfinite sequence, by hand-worked sequences that
+    include a drop below 1, and by the fp32 product of a non-power-of-two factor.
   orthonormalize(method="cholqr_f32") is used only to derive a tolerance (an fp32
     orthonormalisation's own distance from fp64). It is pinned by orthonormality and span
     of well- and ill-conditioned inputs to fp32 accuracy.
@@ -91,6 +94,33 @@ def skip_threshold(fraction: float, workers: int, numel_block: int) -> int:
 
 def skip_block(counts_per_worker, threshold: int) -> bool:
     return int(np.sum(np.asarray(counts_per_worker, dtype=np.int64))) >= int(threshold)
+
+
+def scale_update(scale: float, streak: int, counts_per_worker, backoff: float, growth: float,
+                 interval: int):
+    """One update of a resblock's dynamic gradient scale S and its finite-step streak.
+
+    [amp] §3.2, the dynamic scaler: S becomes beta S when the scaled gradient holds an
+    Inf or NaN, gamma S after K consecutive finite steps, and otherwise stays; beta < 1
+    is the backoff, gamma > 1 the growth, K the interval. The page also notes that S is
+    not guaranteed to stay above 1. [card] 方法适配 gives every resblock its own scale, so
+    the rule runs per block. Here:
+    - "holds an Inf or NaN" means the block's nonfinite count, summed over every worker,
+      is > 0. That is the count the step reports, so every worker agrees ([amp] §6.2).
+    - The streak counts consecutive finite steps. It restarts at 0 after a growth and
+      after a backoff.
+    - S is fp32 state. Each update is one IEEE single multiply by the factor rounded to
+      fp32.
+
+    Returns (S', streak').
+    """
+    s = np.float32(scale)
+    if int(np.sum(np.asarray(counts_per_worker, dtype=np.int64))) > 0:
+        return np.float32(s * np.float32(backoff)), 0
+    streak = int(streak) + 1
+    if streak >= int(interval):
+        return np.float32(s * np.float32(growth)), 0
+    return s, streak
 
 
 # ----------------------------------------------------------------------- power step

@@ -384,3 +384,63 @@ def test_fp32_cholesky_qr_orthonormal_basis_of_span():
     x = oracle.orthonormalize(p, "cholqr_f32")
     assert np.abs(x.T @ x - np.eye(32)).max() < 1e-5
     assert np.linalg.norm(x @ (x.T @ p) - p) / np.linalg.norm(p) < 1e-5
+
+
+# ------------------------------------------------------------- dynamic scale ([amp] §3.2)
+def _run_scaler(s0, events, backoff, growth, interval):
+    s, k, trace = s0, 0, []
+    for nonfinite in events:
+        s, k = oracle.scale_update(s, k, [0, 1] if nonfinite else [0, 0], backoff, growth,
+                                   interval)
+        trace.append((float(s), k))
+    return trace
+
+
+def test_scale_update_hand_worked_sequence_drops_below_one():
+    """S0 = 1, backoff 1/2, growth 2, interval 2, events N F F N N F (N: the block held an
+    Inf/NaN). By the rule: 1/2 (streak 0), 1/2 (1), 1 (grown, 0), 1/2, 1/4, 1/4 (1). The
+    scale goes below 1, which the page says can happen."""
+    assert _run_scaler(1.0, [1, 0, 0, 1, 1, 0], 0.5, 2.0, 2) == [
+        (0.5, 0), (0.5, 1), (1.0, 0), (0.5, 0), (0.25, 0), (0.25, 1)]
+
+
+def test_scale_update_counts_any_worker():
+    """One nonfinite entry on any worker backs the block off; zero counts everywhere do
+    not."""
+    assert oracle.scale_update(8.0, 3, [0, 0, 0, 1], 0.5, 2.0, 100) == (4.0, 0)
+    assert oracle.scale_update(8.0, 3, [0, 0, 0, 0], 0.5, 2.0, 100) == (8.0, 4)
+
+
+def test_scale_update_closed_form_over_random_events():
+    """With power-of-two factors every product is exact, so after any event sequence
+    S = 2^(e0 + growths - backoffs). The counts come from a run-length reading of the
+    sequence, not from the update: every event N is one backoff; a run of L finite
+    events after a reset gives floor(L / K) growths and leaves L mod K in the streak."""
+    rng = np.random.default_rng(11)
+    events = (rng.random(600) < 0.25).astype(int)
+    K = 3
+    trace = _run_scaler(2.0 ** 5, events, 0.5, 2.0, K)
+    backoffs = int(events.sum())
+    runs, cur = [], 0
+    for ev in events:
+        if ev:
+            runs.append(cur)
+            cur = 0
+        else:
+            cur += 1
+    runs.append(cur)
+    growths = sum(L // K for L in runs)
+    e = 5 + growths - backoffs
+    assert -120 < e < 120  # stays in fp32's normal range for this seed
+    assert trace[-1] == (2.0 ** e, runs[-1] % K)
+
+
+def test_scale_update_rounds_each_product_to_fp32():
+    """Backoff 0.3 is not a power of two. fp32(0.3) = 0.300000011920928955078125, so
+    1000 * fp32(0.3) = 300.0000119209..., which is within half an fp32 ulp (2^-16 at 300)
+    of 300: S' = 300 exactly. A second backoff: 300 * fp32(0.3) = 90.0000035762...,
+    which rounds to 90 (half an ulp there is 2^-18 = 3.8e-6)."""
+    s, _ = oracle.scale_update(1000.0, 0, [1], 0.3, 2.0, 4)
+    assert s == np.float32(300.0) and s.dtype == np.float32
+    s, _ = oracle.scale_update(s, 0, [1], 0.3, 2.0, 4)
+    assert s == np.float32(90.0)
