@@ -94,7 +94,8 @@ typedef struct {
   float* const* q_state;        /* [B*J] Q_{b,j}, fp32 n x r row-major; the caller
                                    writes Q0 before the first step; updated in place */
   const float* scales;          /* [B] host: s_b, finite and >= 1 (powers of two give
-                                   a bit-exact M) */
+                                   a bit-exact M). May be NULL when scales_device is
+                                   given; ignored then. */
   float* const* ghat;           /* [B*J] G^_{b,j}, fp32 m x n (written; 0 when skipped) */
   const float* const* unc_in;   /* [B*W] raw gains/biases, fp32 unc_len (NULL if none) */
   float* const* unc_out;        /* [B] mean gains/biases, fp32 unc_len (NULL if none) */
@@ -105,6 +106,11 @@ typedef struct {
                                    bit per matrix entry, LSB-first in 32-bit words,
                                    row-major; matrix (b,j,w) starts at word
                                    psgd_mask_offset(cfg, b, j, w) */
+  const float* scales_device;   /* [B] device, or NULL: s_b read on the device (the state
+                                   psgd_scale_update keeps), so no host round trip sits
+                                   between steps. Each s_b must be > 0; it may be below 1
+                                   (then 1/s_b > 1, and a product that overflows counts
+                                   as nonfinite). Nothing checks the values on the host. */
 } psgd_step_args;
 
 /* Bytes of device workspace psgd_init needs for this configuration (0 on error). */
@@ -122,6 +128,27 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes,
 
 /* Enqueue one PowerSGD step on `stream` (see the top of this file). */
 psgd_status psgd_step(psgd_handle* h, const psgd_step_args* args, void* stream);
+
+/* Dynamic per-resblock gradient scale ("AIGC 基本功|混合精度与数值稳定性", §3.2, the
+ * dynamic scaler rule, applied per resblock as "Zero-Shot Text-to-Image Generation -
+ * 中文验证版" §方法适配 gives each resblock its own scale). From the nonfinite counts a
+ * finished psgd_step left in `counts`, for every block b:
+ *   if sum_w counts[b*W + w] > 0:  scale[b] = fp32(scale[b] * fp32(backoff)), streak[b] = 0
+ *   else: streak[b] += 1; if streak[b] >= interval:
+ *                                   scale[b] = fp32(scale[b] * fp32(growth)), streak[b] = 0
+ *   num_blocks  B >= 1, num_workers W >= 1
+ *   counts      device int64 [B*W] (psgd_step's counts), read
+ *   scale       device fp32 [B], read and written (pass it to the next step as
+ *               psgd_step_args.scales_device)
+ *   streak      device int32 [B], read and written; the caller starts it at 0
+ *   backoff     in (0, 1); growth > 1 (both finite); interval >= 1
+ *   stream      cudaStream_t (NULL: the legacy default stream); asynchronous.
+ * Returns PSGD_EINVAL, before any launch, for a NULL pointer, a pointer that is not
+ * aligned to its element size, or a factor or size out of range. Needs no handle and
+ * allocates nothing. */
+psgd_status psgd_scale_update(int32_t num_blocks, int32_t num_workers, const int64_t* counts,
+                              float* scale, int32_t* streak, double backoff, double growth,
+                              int32_t interval, void* stream);
 
 /* Wait for `stream`, then report a device-side error raised by an earlier step
  * (PSGD_ETIMEOUT for an expired bounded wait), and clear it. */

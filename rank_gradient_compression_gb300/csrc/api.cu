@@ -34,6 +34,7 @@ constexpr int64_t kSliceRows = 512;
 struct Layout {
   size_t total = 0;
   size_t meta = 0, threshold = 0, mask_off = 0, segs = 0, table = 0, err = 0, scal = 0;
+  size_t inv_dev = 0;
   std::vector<size_t> mscr, P, Xa, Xb, Phat, ostate, Qpart, Gpart, Rinv;
   size_t tc = 0;
   size_t table_bytes = 0, maps_bytes = 0;
@@ -87,6 +88,7 @@ Layout plan_layout(const psgd_config* c) {
   L.table = take(L.table_bytes + L.maps_bytes);
   L.err = take(16);
   L.scal = take(4 * kScalWords * (size_t)B * J);
+  L.inv_dev = take(4 * (size_t)B);
   for (int t = 0; t < B * J; ++t) {
     const psgd_shape s = c->shapes[t % J];
     const int64_t mpad = ceil_div(s.m, 128) * 128;
@@ -202,6 +204,7 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
   h.maps_bytes = h.tc ? L.maps_bytes : 0;
   h.d_err = reinterpret_cast<int*>(h.ws + L.err);
   h.d_scal_all = reinterpret_cast<float*>(h.ws + L.scal);
+  h.d_inv_dev = reinterpret_cast<float*>(h.ws + L.inv_dev);
 
   h.meta.resize(BJ);
   for (int t = 0; t < BJ; ++t) {
@@ -302,8 +305,12 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   if (!ph || !a) return fail(PSGD_EINVAL, "handle or args is NULL");
   Handle& h = ph->h;
   const size_t B = h.B, J = h.J, W = h.W;
-  if (!a->grads || !a->errs || !a->q_state || !a->scales || !a->ghat || !a->counts || !a->skip)
+  if (!a->grads || !a->errs || !a->q_state || !a->ghat || !a->counts || !a->skip)
     return fail(PSGD_EINVAL, "a required argument array is NULL");
+  const bool dev_scales = a->scales_device != nullptr;
+  if (!dev_scales && !a->scales) return fail(PSGD_EINVAL, "scales or scales_device is required");
+  if (dev_scales && (reinterpret_cast<uintptr_t>(a->scales_device) & 3u))
+    return fail(PSGD_EINVAL, "scales_device must be 4-byte aligned");
   if (h.cfg.unc_len > 0 && (!a->unc_in || !a->unc_out))
     return fail(PSGD_EINVAL, "unc_in/unc_out are required when unc_len > 0");
   if ((h.cfg.flags & PSGD_FLAG_MASK) && !a->mask_bits)
@@ -318,7 +325,7 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
     if (!aligned16(a->ghat[i])) return fail(PSGD_EINVAL, "G-hat pointers must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(a->q_state[i]) & 3u) return fail(PSGD_EINVAL, "Q must be 4-byte aligned");
   }
-  for (size_t b = 0; b < B; ++b) {
+  for (size_t b = 0; b < B && !dev_scales; ++b) {
     const float s = a->scales[b];
     if (!std::isfinite(s) || !(s >= 1.0f)) return fail(PSGD_EINVAL, "scales must be finite and >= 1");
   }
@@ -344,8 +351,8 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   o += 8 * B * W;
   if (h.cfg.unc_len > 0) std::memcpy(o, a->unc_out, 8 * B);
   o += 8 * B;
-  for (size_t b = 0; b < B; ++b) {
-    const float inv = (float)(1.0 / (double)a->scales[b]);
+  for (size_t b = 0; b < B; ++b) {  // unused (left 0) when the scales live on the device
+    const float inv = dev_scales ? 0.0f : (float)(1.0 / (double)a->scales[b]);
     std::memcpy(o + 4 * b, &inv, 4);
   }
   if (!h.have_table || tab != h.last_table) {
@@ -368,6 +375,7 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   p.meta = h.d_meta;
   p.threshold = h.d_threshold;
   p.tab = h.tab;
+  if (dev_scales) p.tab.inv_scale = h.d_inv_dev;  // formed below, before the ingest
   p.counts = a->counts;
   p.skip = a->skip;
   p.mask = (h.cfg.flags & PSGD_FLAG_MASK) ? a->mask_bits : nullptr;
@@ -379,6 +387,9 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   int phase = 0;
   auto mark = [&]() { if (ev) cudaEventRecord(ev[phase++], s); };
   mark();
+  if (dev_scales && (e = launch_inv_scale(h.B, a->scales_device, h.d_inv_dev, s)) != cudaSuccess)
+    return cuda_fail(e, "inv_scale");
+  if (dev_scales) ++h.launches;
   if ((e = cudaMemsetAsync(a->counts, 0, 8 * B * W, s)) != cudaSuccess) return cuda_fail(e, "counts");
   if ((e = cudaMemsetAsync(h.d_scal_all, 0, 4 * kScalWords * B * J, s)) != cudaSuccess) return cuda_fail(e, "scal");
   // The fused path ingests the gradients and forms the P partial sums in one sweep; the

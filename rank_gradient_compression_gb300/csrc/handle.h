@@ -52,6 +52,7 @@ struct Handle {
 
   int* d_err = nullptr;
   float* d_scal_all = nullptr;  // [B*J*kScalWords] scaling words, zeroed every step
+  float* d_inv_dev = nullptr;   // [B] 1/s_b formed on the device (psgd_step_args.scales_device)
   size_t maps_bytes = 0;        // TMA maps of the callers' G and E (tensor engine), after the table
   int max_mtiles = 0, max_S = 0, max_C = 0, max_ntiles64 = 0, max_mtiles64 = 0;
   int max_kchunks = 0, max_ntiles128 = 0;
@@ -84,5 +85,6 @@ psgd_status report_cuda_error(cudaError_t e, const char* where);
 // The orthonormalisation passes for one matrix whose plan, pass state and scratch were
 // not laid out by psgd_init (orth.cu). C: Gram row chunks; mtiles64: 64-row tiles.
 cudaError_t launch_orth_one(const Plan& p, int C, int mtiles64, cudaStream_t s);
+cudaError_t launch_inv_scale(int B, const float* scale, float* inv, cudaStream_t s);
 
 }  // namespace psgd

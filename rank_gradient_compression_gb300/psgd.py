@@ -24,7 +24,7 @@ EXPORTS = ("psgd_workspace_size", "psgd_mask_offset", "psgd_mask_words", "psgd_i
            "psgd_step", "psgd_check", "psgd_finalize", "psgd_strerror", "psgd_last_error",
            "psgd_debug_m", "psgd_debug_phat", "psgd_engine", "psgd_profile_begin",
            "psgd_profile_end", "psgd_launch_count", "psgd_debug_orth",
-           "psgd_orthonormalize_static")
+           "psgd_orthonormalize_static", "psgd_scale_update")
 PSGD_STATIC_MAX_ROWS, PSGD_STATIC_MAX_COLS = 16384, 128
 PSGD_MAX_ORTH_PASSES = 4
 PSGD_NUM_PHASES = 7
@@ -47,7 +47,7 @@ class psgd_step_args(ctypes.Structure):
                 ("q_state", POINTER(c_void_p)), ("scales", POINTER(ctypes.c_float)),
                 ("ghat", POINTER(c_void_p)), ("unc_in", POINTER(c_void_p)),
                 ("unc_out", POINTER(c_void_p)), ("counts", c_void_p), ("skip", c_void_p),
-                ("mask_bits", c_void_p)]
+                ("mask_bits", c_void_p), ("scales_device", c_void_p)]
 
 
 class PSGDError(RuntimeError):
@@ -95,6 +95,9 @@ def _load():
     lib.psgd_debug_orth.argtypes = [c_void_p, c_int32, c_int32, POINTER(c_int32), c_void_p]
     lib.psgd_orthonormalize_static.restype = c_int32
     lib.psgd_orthonormalize_static.argtypes = [c_void_p, c_void_p, c_int64, c_int32, c_void_p]
+    lib.psgd_scale_update.restype = c_int32
+    lib.psgd_scale_update.argtypes = [c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_double,
+                                      c_double, c_int32, c_void_p]
     return lib
 
 
@@ -177,6 +180,17 @@ def psgd_orthonormalize_static(p_ptr: int, phat_ptr: int, m: int, r: int, stream
                                           c_void_p(stream)))
 
 
+def psgd_scale_update(num_blocks: int, num_workers: int, counts_ptr: int, scale_ptr: int,
+                      streak_ptr: int, backoff: float, growth: float, interval: int,
+                      stream: int):
+    """Per-resblock dynamic scale update on the device, from a finished step's counts:
+    scale[b] *= backoff when block b had a nonfinite entry, else *= growth after
+    `interval` consecutive finite steps (streak[b] counts them)."""
+    _check(lib.psgd_scale_update(int(num_blocks), int(num_workers), c_void_p(counts_ptr),
+                                 c_void_p(scale_ptr), c_void_p(streak_ptr), float(backoff),
+                                 float(growth), int(interval), c_void_p(stream)))
+
+
 def _ptrs(tensors):
     return (c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
 
@@ -185,7 +199,8 @@ class PowerSGD:
     """Owns one psgd handle, its workspace and its count/skip outputs (torch tensors).
 
     ``step`` takes nested lists of CUDA tensors, grads[b][j][w], errs[b][j][w],
-    q[b][j], ghat[b][j], unc_in[b][w] and unc_out[b], plus host scales[b]. It
+    q[b][j], ghat[b][j], unc_in[b][w] and unc_out[b], plus host scales[b] or, with
+    ``scales_device`` (a CUDA fp32 tensor of B scales), scales read on the device. It
     enqueues one psgd_step on the current torch stream.
     """
 
@@ -214,18 +229,19 @@ class PowerSGD:
         self.handle = psgd_init(self.cfg, self._ws_ptr, ws, stream)
         self.engine = psgd_engine(self.handle)
 
-    def step(self, grads, errs, q, scales, ghat, unc_in=None, unc_out=None):
+    def step(self, grads, errs, q, scales, ghat, unc_in=None, unc_out=None, scales_device=None):
         B, J, W = self.B, self.J, self.W
         g = _ptrs([grads[b][j][w] for b in range(B) for j in range(J) for w in range(W)])
         e = _ptrs([errs[b][j][w] for b in range(B) for j in range(J) for w in range(W)])
         qq = _ptrs([q[b][j] for b in range(B) for j in range(J)])
         gh = _ptrs([ghat[b][j] for b in range(B) for j in range(J)])
-        sc = (ctypes.c_float * B)(*[float(s) for s in scales])
+        sc = (ctypes.c_float * B)(*[float(s) for s in scales]) if scales is not None else None
         ui = _ptrs([unc_in[b][w] for b in range(B) for w in range(W)]) if unc_in is not None else None
         uo = _ptrs([unc_out[b] for b in range(B)]) if unc_out is not None else None
         args = psgd_step_args(g, e, qq, sc, gh, ui, uo, c_void_p(self.counts.data_ptr()),
                               c_void_p(self.skip.data_ptr()),
-                              c_void_p(self.mask.data_ptr() if self.mask is not None else 0))
+                              c_void_p(self.mask.data_ptr() if self.mask is not None else 0),
+                              c_void_p(scales_device.data_ptr() if scales_device is not None else 0))
         psgd_step(self.handle, args, self.torch.cuda.current_stream(self.device).cuda_stream)
 
     def check(self):

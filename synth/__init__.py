@@ -125,6 +125,17 @@ def stress(steps=3, workers=8, rank=112, blocks=2, shapes=SHARD_SHAPES, bad_bloc
                     params={"bad_block": bad_block, "bad_step": bad_step, "frac": frac})
 
 
+def scaler_run(steps=5, workers=2, rank=8, shapes=((256, 192), (96, 64)),
+               spots=((1, 1, 5), (3, 0, 1))):
+    """Two blocks in fp16 for the dynamic-scale test: stress-style magnitudes with no
+    random nonfinite entries, except at the (step, block, count) spots, where matrix 0
+    of worker 0 gets `count` nonfinite entries (Inf, -Inf, NaN in thirds) at seeded
+    positions."""
+    return Workload(f"scaler_fp16_w{workers}_r{rank}", "stress", tuple(shapes), 2, workers,
+                    rank, "f16", "f16", steps,
+                    params={"frac": 0.0, "spots": {(st, b): c for st, b, c in spots}})
+
+
 def with_shapes(wl: Workload, shapes, **kw) -> Workload:
     return replace(wl, shapes=tuple(shapes), **kw)
 
@@ -196,6 +207,8 @@ def _stress_values(wl, step, block, j, w, m, n):
         kinds = rng.integers(0, 3, size=(m, n))
         return np.choose(kinds, [np.inf, -np.inf, np.nan]).astype(np.float64)
     cnt = int(round(p.get("frac", 1e-3) * m * n))
+    if j == 0 and w == 0:
+        cnt += p.get("spots", {}).get((step, block), 0)
     pos = rng.choice(m * n, size=cnt, replace=False)
     flat = x.reshape(-1)
     third = cnt // 3

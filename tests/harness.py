@@ -105,7 +105,9 @@ class OracleRun:
                 e=[[np.zeros(s) for _ in range(wl.workers)] for s in wl.shapes],
                 q=[synth.q0(wl, b, j).double().numpy() for j in range(len(wl.shapes))])
 
-    def step(self, step: int, pool=None):
+    def step(self, step: int, pool=None, scales=None):
+        """One oracle step of every sampled block, unscaled by wl.scale(b), or by
+        scales[b] when given (a scale that changes from step to step)."""
         wl = self.wl
 
         def one(b):
@@ -114,7 +116,8 @@ class OracleRun:
             unc = None
             if wl.unc_len:
                 unc = [synth.unc(wl, step, b, w).double().numpy() for w in range(wl.workers)]
-            return b, oracle.block_step(grads, self.state[b], wl.scale(b), wl.err_dtype,
+            s_b = wl.scale(b) if scales is None else float(scales[b])
+            return b, oracle.block_step(grads, self.state[b], s_b, wl.err_dtype,
                                         skip_fraction=wl.skip_fraction, unc=unc, orth=self.orth)
 
         if pool is None:

@@ -87,3 +87,31 @@ def test_no_cpu_fallback_when_library_missing(tmp_path):
             "try:\n import rank_gradient_compression_gb300.psgd\nexcept ImportError as e:\n print('raised')\n")
     r = subprocess.run(["python", "-c", code], capture_output=True, text=True, cwd=ROOT)
     assert "raised" in r.stdout
+
+
+_SCALER_OK = dict(num_blocks=2, num_workers=3, counts=0x10000, scale=0x20000, streak=0x30000,
+                  backoff=0.5, growth=2.0, interval=4)
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(num_blocks=0), "num_blocks"),
+    (dict(num_workers=0), "num_workers"),
+    (dict(counts=0), "device pointers"),
+    (dict(streak=0), "device pointers"),
+    (dict(counts=0x10004), "aligned"),
+    (dict(scale=0x20002), "aligned"),
+    (dict(backoff=1.0), "backoff"),
+    (dict(backoff=0.0), "backoff"),
+    (dict(growth=1.0), "growth"),
+    (dict(growth=float("inf")), "growth"),
+    (dict(interval=0), "interval"),
+])
+def test_scale_update_rejects_bad_arguments_before_any_launch(psgd, kw, msg):
+    """Every argument error of psgd_scale_update returns PSGD_EINVAL with a message before
+    anything is enqueued (no GPU is needed to see it)."""
+    a = dict(_SCALER_OK, **kw)
+    with pytest.raises(psgd.PSGDError) as ex:
+        psgd.psgd_scale_update(a["num_blocks"], a["num_workers"], a["counts"], a["scale"],
+                               a["streak"], a["backoff"], a["growth"], a["interval"], 0)
+    assert ex.value.status == psgd.PSGD_EINVAL
+    assert msg in str(ex.value), str(ex.value)

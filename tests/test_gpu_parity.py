@@ -267,6 +267,43 @@ def test_deterministic_and_resumable():
 
 
 # ------------------------------------------------------------------ argument errors
+def test_dynamic_scale_on_device_matches_oracle():
+    """Per-resblock dynamic scales kept on the device: psgd_step reads s_b through
+    scales_device, and psgd_scale_update (backoff 1/2, growth 2, interval 2) updates them
+    from the step's counts. Two blocks, five steps; block 1 has 5 nonfinite entries at
+    step 1 and block 0 one at step 3, so both blocks back off and grow. The scales used at
+    steps 0..4 are 2^10, 2^10, 2^11, 2^11, 2^10 for block 0 (grown after its second finite
+    step, backed off after step 3) and 2^10, 2^10, 2^9, 2^9, 2^10 for block 1 (backed off
+    after step 1, grown after steps 2 and 3). Each step matches the oracle run with the
+    same scales, and after each update the device scale and streak equal the oracle's
+    rule bit for bit."""
+    psgd = _psgd()
+    wl = synth.scaler_run()
+    B, W = wl.blocks, wl.workers
+    g = GpuRun(wl)
+    o = OracleRun(wl, range(B))
+    scale = torch.full((B,), 2.0 ** 10, dtype=torch.float32, device="cuda")
+    streak = torch.zeros(B, dtype=torch.int32, device="cuda")
+    s_ref, k_ref = [np.float32(2.0 ** 10)] * B, [0] * B
+    seen = []
+    for t in range(wl.steps):
+        g.load_inputs(t)
+        g.load_state(o)
+        g.ps.step(g.grads, g.errs, g.q, None, g.ghat, g.unc_in, g.unc_out, scales_device=scale)
+        res = o.step(t, scales=s_ref)
+        compare_step(g, res, o)
+        seen.append([float(x) for x in s_ref])
+        psgd.psgd_scale_update(B, W, g.ps.counts.data_ptr(), scale.data_ptr(), streak.data_ptr(),
+                               0.5, 2.0, 2, torch.cuda.current_stream().cuda_stream)
+        for b in range(B):
+            s_ref[b], k_ref[b] = oracle.scale_update(s_ref[b], k_ref[b], res[b].counts, 0.5, 2.0, 2)
+        torch.cuda.synchronize()
+        assert scale.cpu().numpy().tolist() == [float(x) for x in s_ref], t
+        assert streak.cpu().numpy().tolist() == k_ref, t
+    assert seen == [[2.0 ** 10, 2.0 ** 10], [2.0 ** 10, 2.0 ** 10], [2.0 ** 11, 2.0 ** 9],
+                    [2.0 ** 11, 2.0 ** 9], [2.0 ** 10, 2.0 ** 10]]
+
+
 def test_argument_errors_return_status():
     psgd = _psgd()
     ps = psgd.PowerSGD([(64, 32)], 1, 1, 2, "f16")
@@ -284,6 +321,13 @@ def test_argument_errors_return_status():
     mis = big[1:1 + 64 * 32].view(64, 32)  # 2-byte offset: not 16-byte aligned
     with pytest.raises(psgd.PSGDError) as ex:
         ps.step([[[mis]]], [[[e]]], [[q]], [1.0], [[gh]])
+    assert ex.value.status == psgd.PSGD_EINVAL
+    with pytest.raises(psgd.PSGDError) as ex:  # neither host nor device scales
+        ps.step([[[g]]], [[[e]]], [[q]], None, [[gh]])
+    assert ex.value.status == psgd.PSGD_EINVAL
+    sd = torch.ones(2, device="cuda")
+    with pytest.raises(psgd.PSGDError) as ex:  # device scales not 4-byte aligned
+        ps.step([[[g]]], [[[e]]], [[q]], None, [[gh]], scales_device=sd.view(torch.uint8)[1:5])
     assert ex.value.status == psgd.PSGD_EINVAL
     ps.step([[[g]]], [[[e]]], [[q]], [1.0], [[gh]])
     ps.check()
