@@ -14,6 +14,7 @@ import torch
 
 import oracle
 from oracle import numerics as nx
+from oracle import optim
 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "amp_fp16_bf16_values.txt")
@@ -444,3 +445,62 @@ def test_scale_update_rounds_each_product_to_fp32():
     assert s == np.float32(300.0) and s.dtype == np.float32
     s, _ = oracle.scale_update(s, 0, [1], 0.3, 2.0, 4)
     assert s == np.float32(90.0)
+
+
+# ------------------------------------------- consumer of G-hat: clipping + Adam ([amp] §6.2)
+
+
+def test_global_norm_is_the_norm_of_the_concatenated_shards():
+    """[amp] §6.2: the global norm is the root of the all-reduced local sums of squares.
+    It equals the 2-norm of all shards laid end to end (numpy's own norm)."""
+    rng = np.random.default_rng(5)
+    shards = [rng.standard_normal(s) for s in ((7, 3), (11,), (2, 5, 4))]
+    flat = np.concatenate([x.reshape(-1) for x in shards])
+    assert math.isclose(optim.global_norm(shards), float(np.linalg.norm(flat)), rel_tol=1e-14)
+    assert optim.global_norm([np.zeros(3)]) == 0.0
+    assert optim.global_norm([np.array([3.0]), np.array([4.0])]) == 5.0
+
+
+def test_clip_coefficient_hand_worked():
+    assert optim.clip_coefficient(5.0, 1.0) == 0.2
+    assert optim.clip_coefficient(0.5, 1.0) == 1.0
+    assert optim.clip_coefficient(1.0, 1.0) == 1.0
+    assert optim.clip_coefficient(0.0, 1.0) == 1.0
+    # clipping rescales the global norm to exactly C (up to rounding)
+    g = [np.array([3.0, 4.0]), np.array([12.0])]
+    c = optim.clip_coefficient(optim.global_norm(g), 2.0)
+    assert math.isclose(optim.global_norm([x * c for x in g]), 2.0, rel_tol=1e-15)
+
+
+def test_adam_first_step_closed_form():
+    """From zero moments, bias correction makes m_hat = g and v_hat = g^2, so the first
+    step moves theta by exactly -lr g / (|g| + eps)."""
+    g = np.array([0.5, -2.0, 1e-3, 0.0])
+    th, m, v = optim.adam_step(np.ones(4), np.zeros(4), np.zeros(4), g, 1, 1e-2, 0.9, 0.999, 1e-8)
+    assert np.allclose(th, 1.0 - 1e-2 * g / (np.abs(g) + 1e-8), rtol=0, atol=1e-15)
+    assert np.allclose(m, 0.1 * g) and np.allclose(v, 0.001 * g * g)
+
+
+def test_adam_constant_gradient_steps_tend_to_lr():
+    """For a constant gradient g, m_t = (1 - b1^t) g and v_t = (1 - b2^t) g^2 exactly, so
+    every bias-corrected step is lr * g / (|g| + eps): with eps = 0 it is lr sign(g)."""
+    g = np.array([2.0, -0.25])
+    th, m, v = np.zeros(2), np.zeros(2), np.zeros(2)
+    for t in range(1, 40):
+        before = th
+        th, m, v = optim.adam_step(th, m, v, g, t, 0.1, 0.9, 0.99, 0.0)
+        assert np.allclose(th - before, -0.1 * np.sign(g), rtol=0, atol=1e-12), t
+        assert np.allclose(m, (1 - 0.9 ** t) * g, rtol=1e-12)
+
+
+def test_adam_is_invariant_to_gradient_scale_without_eps_and_skip_keeps_state():
+    rng = np.random.default_rng(9)
+    gs = [rng.standard_normal(6) for _ in range(5)]
+    a = b = (np.zeros(6), np.zeros(6), np.zeros(6))
+    for t, g in enumerate(gs, 1):
+        a = optim.adam_step(*a, g, t, 1e-3, 0.9, 0.999, 0.0)
+        b = optim.adam_step(*b, 1024.0 * g, t, 1e-3, 0.9, 0.999, 0.0)
+    assert np.allclose(a[0], b[0], rtol=1e-12, atol=0)
+    st = (np.ones(3), np.full(3, 0.5), np.full(3, 0.25))
+    out = optim.adam_step(*st, np.full(3, np.nan), 3, 1e-3, 0.9, 0.999, 1e-8, skip=True)
+    assert all(np.array_equal(x, y) for x, y in zip(out, st))
