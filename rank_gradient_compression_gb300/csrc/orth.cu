@@ -9,7 +9,8 @@
 // taken at its typical sqrt(m) growth, not the worst case. The factor-of-m worst case
 // in fp32 would shift by more than the largest eigenvalue. A pass whose Cholesky is
 // unshifted and shows a nearly orthonormal X (pivot ratios >= 1/2, diag(R) within a
-// factor 2) is the last one. CholeskyQR2 (two passes) is the common case. Columns whose
+// factor 2) is the last one. After a warm start P is usually close to orthogonal and one
+// pass is final; otherwise CholeskyQR2 (two passes) is the common case. Columns whose
 // pivot vanishes are numerically dependent; their column of R^-1 is zeroed. That
 // leaves a zero column in P^ and the projector P^ P^T onto span(P) unchanged.
 //
