@@ -164,9 +164,11 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle (CPU) leg
-def oracle_sample(matrices, seconds_note=""):
-    """Time the fp64 oracle on one step of the given matrices of this workload (W = 8).
-    Returns (gradient bytes processed, seconds)."""
+def oracle_sample(matrices, min_seconds=0.0):
+    """Time the fp64 oracle on steps of the given matrices of this workload (W = 8): one
+    step, or as many consecutive steps (same gradients, evolving state) as it takes to
+    spend min_seconds in the oracle. Input generation is outside the timing.
+    Returns (gradient bytes processed, seconds, steps)."""
     import numpy as np
     import oracle
     import synth
@@ -174,10 +176,13 @@ def oracle_sample(matrices, seconds_note=""):
     grads = [[synth.grad(wl, 0, 0, j, w).double().numpy() for w in range(W)] for j in range(len(matrices))]
     st = oracle.BlockState(e=[[np.zeros(s) for _ in range(W)] for s in matrices],
                            q=[synth.q0(wl, 0, j).double().numpy() for j in range(len(matrices))])
-    t0 = time.perf_counter()
-    oracle.block_step(grads, st, wl.scale(0), "f16")
-    dt = time.perf_counter() - t0
-    return W * sum(m * n for m, n in matrices) * 2, dt
+    dt, n = 0.0, 0
+    while n == 0 or dt < min_seconds:
+        t0 = time.perf_counter()
+        oracle.block_step(grads, st, wl.scale(0), "f16")
+        dt += time.perf_counter() - t0
+        n += 1
+    return n * W * sum(m * n_ for m, n_ in matrices) * 2, dt, n
 
 
 def cpu_cores():
@@ -196,7 +201,7 @@ def run_reference(args):
         oracle_sample(sample)
     tot_b, tot_s = 0, 0.0
     for _ in range(args.steps):
-        b, s = oracle_sample(sample)
+        b, s, _ = oracle_sample(sample)
         tot_b += b
         tot_s += s
     val = tot_b / tot_s / 1e9
@@ -348,9 +353,10 @@ def run_ours(args):
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        b, s = oracle_sample(SHAPES)
+        b, s, nst = oracle_sample(SHAPES, min_seconds=10.0)
         line["cpu_baseline"] = {"value": b / s / 1e9, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                                "sample": "one full step of the workload (all 4 matrices, W=8) in fp64 numpy",
+                                "sample": f"{nst} consecutive full steps of the workload (all 4 matrices, "
+                                          f"W=8) in fp64 numpy, at least 10 s of oracle time",
                                 "seconds": s}
     if rank == 0:
         print(json.dumps(line), flush=True)
