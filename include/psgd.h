@@ -150,6 +150,45 @@ psgd_status psgd_scale_update(int32_t num_blocks, int32_t num_workers, const int
                               float* scale, int32_t* streak, double backoff, double growth,
                               int32_t interval, void* stream);
 
+/* Consumer of the decompressed gradient: global-norm clipping and one Adam step with
+ * fp32 moments ("Zero-Shot Text-to-Image Generation - 中文验证版" §方法适配: Adam with
+ * clipping and a skip rule; "AIGC 基本功|混合精度与数值稳定性" §6.2: the clipping norm is
+ * global and taken after unscaling; the update rule is the published bias-corrected
+ * Adam). Over every tensor t passed:
+ *   n = sqrt(sum_t ||grads[t]||^2); c = min(1, max_norm / n) (c = 1 if max_norm <= 0)
+ *   for tensors whose block is not skipped, element-wise with g' = c g:
+ *   m <- b1 m + (1 - b1) g'; v <- b2 v + (1 - b2) g'^2;
+ *   theta <- theta - lr (m / (1 - b1^step)) / (sqrt(v / (1 - b2^step)) + eps)
+ * The norm covers every tensor, skipped or not (psgd_step writes G-hat = 0 for a skipped
+ * block). */
+#define PSGD_ADAM_MAX_TENSORS 512
+typedef struct {
+  int32_t num_tensors;              /* T in [1, PSGD_ADAM_MAX_TENSORS] */
+  const float* const* grads;        /* [T] host array of device fp32 gradients */
+  float* const* params;             /* [T] device fp32 theta, updated */
+  float* const* exp_avg;            /* [T] device fp32 m, updated (start at 0) */
+  float* const* exp_avg_sq;         /* [T] device fp32 v, updated (start at 0) */
+  const int64_t* numel;             /* [T] host element counts (>= 0) */
+  const int32_t* block;             /* [T] host resblock index of each tensor (-1: never
+                                       skipped), or NULL */
+  const uint8_t* skip;              /* device [num_blocks] psgd_step skip flags, or NULL */
+  int32_t num_blocks;               /* entries of skip (required with skip) */
+  double max_norm;                  /* C; <= 0 disables clipping */
+  double lr, beta1, beta2, eps;     /* lr >= 0, 0 <= beta < 1, eps >= 0, all finite */
+  int32_t step;                     /* >= 1: the step number after this update */
+  float* norm_out;                  /* device fp32 [1]: n before clipping, or NULL */
+} psgd_adam_args;
+
+/* Bytes of device workspace psgd_clip_adam needs for these tensor sizes (0 on error). */
+size_t psgd_clip_adam_workspace_size(int32_t num_tensors, const int64_t* numel);
+
+/* Enqueue the clip + Adam update on `stream`. workspace: device, 256-byte aligned, at
+ * least psgd_clip_adam_workspace_size bytes, caller-owned (its contents are scratch).
+ * All device pointers 4-byte aligned. PSGD_EINVAL before any launch on a bad argument.
+ * Allocates nothing. */
+psgd_status psgd_clip_adam(const psgd_adam_args* args, void* workspace, size_t ws_bytes,
+                           void* stream);
+
 /* Wait for `stream`, then report a device-side error raised by an earlier step
  * (PSGD_ETIMEOUT for an expired bounded wait), and clear it. */
 psgd_status psgd_check(psgd_handle* h, void* stream);

@@ -24,9 +24,11 @@ EXPORTS = ("psgd_workspace_size", "psgd_mask_offset", "psgd_mask_words", "psgd_i
            "psgd_step", "psgd_check", "psgd_finalize", "psgd_strerror", "psgd_last_error",
            "psgd_debug_m", "psgd_debug_phat", "psgd_engine", "psgd_profile_begin",
            "psgd_profile_end", "psgd_launch_count", "psgd_debug_orth",
-           "psgd_orthonormalize_static", "psgd_scale_update")
+           "psgd_orthonormalize_static", "psgd_scale_update", "psgd_clip_adam_workspace_size",
+           "psgd_clip_adam")
 PSGD_STATIC_MAX_ROWS, PSGD_STATIC_MAX_COLS = 16384, 128
 PSGD_MAX_ORTH_PASSES = 4
+PSGD_ADAM_MAX_TENSORS = 512
 PSGD_NUM_PHASES = 7
 PHASES = ("ingest", "skip_unc", "pgemm", "orth", "qgemm", "qreduce", "decomp")
 
@@ -48,6 +50,16 @@ class psgd_step_args(ctypes.Structure):
                 ("ghat", POINTER(c_void_p)), ("unc_in", POINTER(c_void_p)),
                 ("unc_out", POINTER(c_void_p)), ("counts", c_void_p), ("skip", c_void_p),
                 ("mask_bits", c_void_p), ("scales_device", c_void_p)]
+
+
+class psgd_adam_args(ctypes.Structure):
+    _fields_ = [("num_tensors", c_int32), ("grads", POINTER(c_void_p)),
+                ("params", POINTER(c_void_p)), ("exp_avg", POINTER(c_void_p)),
+                ("exp_avg_sq", POINTER(c_void_p)), ("numel", POINTER(c_int64)),
+                ("block", POINTER(c_int32)), ("skip", c_void_p), ("num_blocks", c_int32),
+                ("max_norm", c_double), ("lr", c_double), ("beta1", c_double),
+                ("beta2", c_double), ("eps", c_double), ("step", c_int32),
+                ("norm_out", c_void_p)]
 
 
 class PSGDError(RuntimeError):
@@ -95,6 +107,10 @@ def _load():
     lib.psgd_debug_orth.argtypes = [c_void_p, c_int32, c_int32, POINTER(c_int32), c_void_p]
     lib.psgd_orthonormalize_static.restype = c_int32
     lib.psgd_orthonormalize_static.argtypes = [c_void_p, c_void_p, c_int64, c_int32, c_void_p]
+    lib.psgd_clip_adam_workspace_size.restype = c_size_t
+    lib.psgd_clip_adam_workspace_size.argtypes = [c_int32, POINTER(c_int64)]
+    lib.psgd_clip_adam.restype = c_int32
+    lib.psgd_clip_adam.argtypes = [POINTER(psgd_adam_args), c_void_p, c_size_t, c_void_p]
     lib.psgd_scale_update.restype = c_int32
     lib.psgd_scale_update.argtypes = [c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_double,
                                       c_double, c_int32, c_void_p]
@@ -189,6 +205,25 @@ def psgd_scale_update(num_blocks: int, num_workers: int, counts_ptr: int, scale_
     _check(lib.psgd_scale_update(int(num_blocks), int(num_workers), c_void_p(counts_ptr),
                                  c_void_p(scale_ptr), c_void_p(streak_ptr), float(backoff),
                                  float(growth), int(interval), c_void_p(stream)))
+
+
+def psgd_clip_adam_workspace_size(numel) -> int:
+    arr = (c_int64 * len(numel))(*[int(x) for x in numel])
+    return int(lib.psgd_clip_adam_workspace_size(len(numel), arr))
+
+
+def psgd_clip_adam(grads, params, exp_avg, exp_avg_sq, numel, workspace_ptr, ws_bytes, stream,
+                   lr, beta1=0.9, beta2=0.999, eps=1e-8, step=1, max_norm=0.0, block=None,
+                   skip_ptr=0, num_blocks=0, norm_out_ptr=0):
+    """Global-norm clip + one Adam step on lists of device pointers (fp32 tensors)."""
+    T = len(grads)
+    p = lambda xs: (c_void_p * T)(*[int(x) for x in xs])
+    args = psgd_adam_args(T, p(grads), p(params), p(exp_avg), p(exp_avg_sq),
+                          (c_int64 * T)(*[int(x) for x in numel]),
+                          (c_int32 * T)(*[int(x) for x in block]) if block is not None else None,
+                          c_void_p(skip_ptr), int(num_blocks), float(max_norm), float(lr),
+                          float(beta1), float(beta2), float(eps), int(step), c_void_p(norm_out_ptr))
+    _check(lib.psgd_clip_adam(byref(args), c_void_p(workspace_ptr), int(ws_bytes), c_void_p(stream)))
 
 
 def _ptrs(tensors):

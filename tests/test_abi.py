@@ -115,3 +115,23 @@ def test_scale_update_rejects_bad_arguments_before_any_launch(psgd, kw, msg):
                                a["streak"], a["backoff"], a["growth"], a["interval"], 0)
     assert ex.value.status == psgd.PSGD_EINVAL
     assert msg in str(ex.value), str(ex.value)
+
+
+def test_clip_adam_workspace_and_argument_checks(psgd):
+    """Sizes and argument errors of psgd_clip_adam, all answered before any launch."""
+    ws = psgd.psgd_clip_adam_workspace_size([8192, 1, 0, 20000])
+    assert ws > 0 and ws % 256 == 0
+    assert ws >= 256 + 8 * (1 + 1 + 0 + 3)
+    assert psgd.psgd_clip_adam_workspace_size([-1]) == 0
+    assert psgd.psgd_clip_adam_workspace_size([1] * (psgd.PSGD_ADAM_MAX_TENSORS + 1)) == 0
+    ok = dict(grads=[0x1000], params=[0x2000], exp_avg=[0x3000], exp_avg_sq=[0x4000],
+              numel=[16], workspace_ptr=0x10000, ws_bytes=1 << 20, stream=0, lr=1e-3)
+    for kw, msg in [(dict(lr=-1.0), "out of range"), (dict(beta1=1.0), "out of range"),
+                    (dict(step=0), "out of range"), (dict(workspace_ptr=0x10010), "256-byte"),
+                    (dict(ws_bytes=64), "workspace smaller"), (dict(params=[0x2002]), "aligned"),
+                    (dict(skip_ptr=0x5000), "skip needs"),
+                    (dict(skip_ptr=0x5000, block=[3], num_blocks=2), "block index")]:
+        with pytest.raises(psgd.PSGDError) as ex:
+            psgd.psgd_clip_adam(**dict(ok, **kw))
+        assert ex.value.status == psgd.PSGD_EINVAL
+        assert msg in str(ex.value), (kw, str(ex.value))

@@ -334,3 +334,51 @@ def test_argument_errors_return_status():
     with pytest.raises(psgd.PSGDError) as ex:
         psgd.PowerSGD([(64, 32)], 1, 1, 40, "f16")
     assert ex.value.status == psgd.PSGD_EINVAL
+
+
+def test_clip_adam_matches_oracle():
+    """Global-norm clipping + Adam (fp32 moments) against the oracle, three steps. Five
+    tensors span one to three 8192-element chunks (one has 3 elements); block 1 is
+    skipped, and the last tensor belongs to no block. max_norm is half the gradient norm,
+    so clipping is active. Each step starts both sides from the same fp32 state."""
+    psgd = _psgd()
+    from oracle import optim
+    rng = np.random.default_rng(21)
+    numel = [10000, 8192, 3, 20000, 257]
+    block = [0, 0, 1, 1, -1]
+    dev = "cuda"
+    th = [torch.from_numpy(rng.standard_normal(n).astype(np.float32)).to(dev) for n in numel]
+    m = [torch.zeros(n, device=dev) for n in numel]
+    v = [torch.zeros(n, device=dev) for n in numel]
+    skip = torch.tensor([0, 1], dtype=torch.uint8, device=dev)
+    ws_bytes = psgd.psgd_clip_adam_workspace_size(numel)
+    ws = torch.empty(ws_bytes + 256, dtype=torch.uint8, device=dev)
+    ws_ptr = (ws.data_ptr() + 255) // 256 * 256
+    norm_out = torch.zeros(1, device=dev)
+    for step in (1, 2, 3):
+        g = [torch.from_numpy((rng.standard_normal(n) * 10.0 ** -step).astype(np.float32)).to(dev)
+             for n in numel]
+        g64 = [x.double().cpu().numpy() for x in g]
+        nrm = optim.global_norm(g64)
+        c = optim.clip_coefficient(nrm, 0.5 * nrm)
+        ref = [optim.adam_step(th[t].cpu().numpy(), m[t].cpu().numpy(), v[t].cpu().numpy(), g64[t],
+                               step, 1e-2, 0.9, 0.99, 1e-8, clip=c,
+                               skip=block[t] >= 0 and bool(skip[block[t]]))
+               for t in range(len(numel))]
+        th_old = [x.double().cpu().numpy() for x in th]
+        psgd.psgd_clip_adam([x.data_ptr() for x in g], [x.data_ptr() for x in th],
+                            [x.data_ptr() for x in m], [x.data_ptr() for x in v], numel, ws_ptr,
+                            ws_bytes, torch.cuda.current_stream().cuda_stream, lr=1e-2, beta1=0.9,
+                            beta2=0.99, eps=1e-8, step=step, max_norm=0.5 * nrm, block=block,
+                            skip_ptr=skip.data_ptr(), num_blocks=2, norm_out_ptr=norm_out.data_ptr())
+        torch.cuda.synchronize()
+        assert abs(float(norm_out[0]) - nrm) <= 1e-6 * nrm
+        for t in range(len(numel)):
+            if block[t] >= 0 and skip[block[t]]:
+                assert np.array_equal(th[t].cpu().numpy(), ref[t][0].astype(np.float32))
+                continue
+            d_gpu = th[t].double().cpu().numpy() - th_old[t]
+            d_ref = ref[t][0] - th_old[t]
+            assert rel_err(d_gpu, d_ref) <= 1e-4, (step, t)
+            assert rel_err(m[t].double().cpu().numpy(), ref[t][1]) <= 1e-5, (step, t)
+            assert rel_err(v[t].double().cpu().numpy(), ref[t][2]) <= 1e-5, (step, t)
