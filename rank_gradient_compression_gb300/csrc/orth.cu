@@ -330,34 +330,65 @@ __device__ void cholesky_panels(float (&a)[kPanel][4], float (&z)[kPanel][4], in
     const int qg = pn >> 2;  // column group of this panel's pivots
     float* Zp = S.X[pn & 1];
     if (warp == pn) {  // the owner
+      // The panel's 8 x 8 diagonal block reaches every lane in one round of shuffles
+      // (upper triangle; columns k0.. sit in group qg at lanes l0..l0+7), and every lane
+      // factors it in registers: no shuffle lies on the chain of the 8 pivots.
+      const int nk = min(kPanel, r - k0);
+      const int l0 = k0 & 31;
+      float D[kPanel][kPanel];
+#pragma unroll
+      for (int s = 0; s < kPanel; ++s) {
+        const float v = sel4(a[s], qg);
+#pragma unroll
+        for (int t = s; t < kPanel; ++t) D[s][t] = __shfl_sync(0xffffffffu, v, l0 + t);
+      }
+      float inv[kPanel];
+      bool dead[kPanel];
 #pragma unroll
       for (int t = 0; t < kPanel; ++t) {
-        const int k = k0 + t;
-        if (k < r) {
-          const float d = __shfl_sync(0xffffffffu, sel4(a[t], qg), k & 31);
-          const float d0 = S.diag0[k];
+        inv[t] = 1.f;
+        dead[t] = true;
+        if (t < nk) {
+          const float d = D[t][t];
+          const float d0 = S.diag0[k0 + t];
           const bool bad = !(d > dead_tol * d0) || !isfinite(d) || !(d0 > 0.f);
-          const float rkk = bad ? 1.f : sqrtf(d);
-          const float inv = __frcp_rn(rkk);
+          const float iv = bad ? 1.f : rsqrtf(d);
+          inv[t] = iv;
+          dead[t] = bad;
+          D[t][t] = bad ? 1.f : d * iv;  // r_kk
+#pragma unroll
+          for (int u = t + 1; u < kPanel; ++u) D[t][u] = bad ? 0.f : D[t][u] * iv;  // R[t][u]
+#pragma unroll
+          for (int u = t + 1; u < kPanel; ++u)
+#pragma unroll
+            for (int v = u; v < kPanel; ++v) D[u][v] = fmaf(-D[t][u], D[t][v], D[u][v]);
+          if (lane == 0) {
+            S.dead[k0 + t] = bad;
+            S.ratio[k0 + t] = bad ? 0.f : __fdividef(d, d0);  // statistics only
+          }
+        }
+      }
+      // The panel's rows of R and Z by forward substitution with the block's R: row t
+      // loses R[s][t] times the finished row s (s < t), then is scaled by 1 / r_tt. These
+      // are the right-looking panel updates, in the same order.
+#pragma unroll
+      for (int t = 0; t < kPanel; ++t) {
+        if (t < nk) {
+          const int k = k0 + t;
+#pragma unroll
+          for (int s2 = 0; s2 < t; ++s2) {
+            const float c = D[s2][t];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              a[t][q] = fmaf(-c, a[s2][q], a[t][q]);
+              z[t][q] = fmaf(-c, z[s2][q], z[t][q]);
+            }
+          }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int j = lane + 32 * q;
-            a[t][q] = j < k ? 0.f : (j == k ? rkk : (bad ? 0.f : a[t][q] * inv));
-            z[t][q] *= inv;
-          }
-          if (lane == 0) {
-            S.dead[k] = bad;
-            S.ratio[k] = bad ? 0.f : __fdividef(d, d0);  // statistics only
-          }
-          // the rows below k in this panel
-#pragma unroll
-          for (int t2 = t + 1; t2 < kPanel; ++t2) {
-            const float c = __shfl_sync(0xffffffffu, sel4(a[t], qg), (k0 + t2) & 31);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              a[t2][q] = fmaf(-c, a[t][q], a[t2][q]);
-              z[t2][q] = fmaf(-c, z[t][q], z[t2][q]);
-            }
+            a[t][q] = j < k ? 0.f : (j == k ? D[t][t] : (dead[t] ? 0.f : a[t][q] * inv[t]));
+            z[t][q] *= inv[t];
           }
         }
       }
@@ -372,7 +403,7 @@ __device__ void cholesky_panels(float (&a)[kPanel][4], float (&z)[kPanel][4], in
         }
     }
     __syncthreads();
-    if (warp > pn) {
+    if (warp > pn && warp * kPanel < r) {  // warps whose rows all lie past r have nothing to update
       const int kend = min(kPanel, r - k0);
       const int i0 = warp * kPanel;
 #pragma unroll 1
