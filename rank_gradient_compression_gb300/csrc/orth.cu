@@ -372,7 +372,7 @@ __device__ void cholesky_panels(float (&a)[kPanel][4], float (&z)[kPanel][4], in
         }
     }
     __syncthreads();
-    if (warp > pn) {
+    if (warp > pn && warp * kPanel < r) {  // warps whose rows all lie past r have nothing to update
       const int kend = min(kPanel, r - k0);
       const int i0 = warp * kPanel;
 #pragma unroll 1
