@@ -28,8 +28,15 @@ size_t esize(int dt) { return dt == DT_F32 ? 4 : 2; }
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Rows of the Q-GEMM slices and Gram chunks of the FFMA engine.
-constexpr int64_t kSliceRows = 512;
+// Rows of a Q-GEMM slice (one Q partial sum each): 256 on the tensor engine, where
+// finer slices balance its units over the SMs; 512 on the FFMA engine, whose partials
+// at large r are large.
+constexpr int64_t kSliceRowsTc = 256, kSliceRowsSimt = 512;
+int64_t slice_rows(const psgd_config* c) {
+  std::string why;
+  const bool tc = c->err_dtype != DT_F32 && !(c->flags & PSGD_FLAG_SIMT) && tc_supported(c, &why);
+  return tc ? kSliceRowsTc : kSliceRowsSimt;
+}
 
 struct Layout {
   size_t total = 0;
@@ -92,7 +99,7 @@ Layout plan_layout(const psgd_config* c) {
   for (int t = 0; t < B * J; ++t) {
     const psgd_shape s = c->shapes[t % J];
     const int64_t mpad = ceil_div(s.m, 128) * 128;
-    const int64_t S = std::max<int64_t>(1, ceil_div(s.m, kSliceRows));
+    const int64_t S = std::max<int64_t>(1, ceil_div(s.m, slice_rows(c)));
     const int64_t C = std::max<int64_t>(1, ceil_div(s.m, kGramRows));
     L.mscr.push_back(take(es * (size_t)W * s.m * s.n));
     L.P.push_back(take(4 * (size_t)mpad * rp));
@@ -212,7 +219,7 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
     MatMeta& mt = h.meta[t];
     std::memset(&mt, 0, sizeof(mt));
     mt.m = sh.m; mt.n = sh.n; mt.b = t / h.J; mt.j = t % h.J;
-    mt.S = (int)std::max<int64_t>(1, ceil_div(sh.m, kSliceRows));
+    mt.S = (int)std::max<int64_t>(1, ceil_div(sh.m, h.tc ? kSliceRowsTc : kSliceRowsSimt));
     mt.C = (int)std::max<int64_t>(1, ceil_div(sh.m, kGramRows));
     mt.mtiles = (int)ceil_div(sh.m, 128);
     mt.mscr = h.ws + L.mscr[t];

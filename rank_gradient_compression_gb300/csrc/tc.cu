@@ -55,7 +55,7 @@ constexpr int PCHUNK_KB = 4;           // P GEMM: k-blocks of 64 columns per uni
 // Q reach G^ and E directly.
 constexpr int kGemmSegSteps = 16;
 constexpr int kIngSegSteps = 4;
-constexpr int QSLICE_ROWS = 512;       // Q GEMM: rows of m per unit (matches Qpart slices)
+constexpr int QSLICE_ROWS = 256;       // Q GEMM: rows of m per unit (matches Qpart slices)
 constexpr int DEC_NT = 128;            // G^ tile columns
 constexpr int NMAPS = 6;               // tensor maps per matrix
 enum { MAP_MP = 0, MAP_MQ = 1, MAP_QS = 2, MAP_PS = 3, MAP_PD = 4, MAP_QD = 5 };
