@@ -69,6 +69,12 @@ typedef struct {
 #define PSGD_FLAG_SIMT 0x1u          /* use the FFMA GEMM engine for 16-bit too (debug) */
 #define PSGD_FLAG_MASK 0x2u          /* write the nonfinite mask bitmap (debug output) */
 #define PSGD_FLAG_STOP_AFTER_INGEST 0x4u /* only unscale/mask/count/M and skip (debug) */
+#define PSGD_FLAG_DEBUG_EXPIRE_WAIT 0x8u /* test of the bounded waits (tensor engine only):
+                                            every CTA of the decompression kernel waits a
+                                            few hundred microseconds on a barrier that
+                                            nothing completes, then winds down. The step's
+                                            G^, E and Q are invalid, and psgd_check returns
+                                            PSGD_ETIMEOUT. */
 
 typedef struct {
   int32_t num_blocks;       /* B >= 1 resblocks */
@@ -93,9 +99,11 @@ typedef struct {
   void* const* errs;            /* [B*J*W] E_{b,j,w}, err_dtype m x n, read and updated */
   float* const* q_state;        /* [B*J] Q_{b,j}, fp32 n x r row-major; the caller
                                    writes Q0 before the first step; updated in place */
-  const float* scales;          /* [B] host: s_b, finite and >= 1 (powers of two give
-                                   a bit-exact M). May be NULL when scales_device is
-                                   given; ignored then. */
+  const float* scales;          /* [B] host: s_b, finite and > 0 (powers of two give
+                                   a bit-exact M). Below 1, 1/s_b > 1 and a product
+                                   that overflows counts as nonfinite, as for device
+                                   scales. May be NULL when scales_device is given;
+                                   ignored then. */
   float* const* ghat;           /* [B*J] G^_{b,j}, fp32 m x n (written; 0 when skipped) */
   const float* const* unc_in;   /* [B*W] raw gains/biases, fp32 unc_len (NULL if none) */
   float* const* unc_out;        /* [B] mean gains/biases, fp32 unc_len (NULL if none) */
@@ -110,7 +118,8 @@ typedef struct {
                                    psgd_scale_update keeps), so no host round trip sits
                                    between steps. Each s_b must be > 0; it may be below 1
                                    (then 1/s_b > 1, and a product that overflows counts
-                                   as nonfinite). Nothing checks the values on the host. */
+                                   as nonfinite). Nothing checks the values on the host;
+                                   psgd_scale_update keeps them finite normal floats. */
 } psgd_step_args;
 
 /* Bytes of device workspace psgd_init needs for this configuration (0 on error). */
@@ -189,6 +198,30 @@ size_t psgd_clip_adam_workspace_size(int32_t num_tensors, const int64_t* numel);
 psgd_status psgd_clip_adam(const psgd_adam_args* args, void* workspace, size_t ws_bytes,
                            void* stream);
 
+/* Uncompressed 32-bit reduction of a gradient that PowerSGD leaves out: the embedding and
+ * unembedding (vocabulary x d_model), or any other fp32 tensor outside the compressed
+ * matrices ("Zero-Shot Text-to-Image Generation - 中文验证版" §方法适配: embedding,
+ * unembedding, gains and biases are reduced in 32-bit, uncompressed; "[논문 정리] Zero-Shot
+ * Text-to-Image Generation" §Mixed-Precision Training: Inf/NaN become 0 on unscaling).
+ * The arithmetic equals that of psgd_step's gains/biases:
+ *   out[i]    = (sum_{w=0..W-1} zero_nonfinite(in[w][i] * (1/scale))) / W   (fp32, in order)
+ *   counts[w] = entries of in[w] whose unscaled value is not finite (overwritten)
+ * If skip is given and *skip != 0 (e.g. psgd_step's skip flag of a resblock, or a
+ * caller's global decision), out is written as 0; the counts are still reported.
+ *   num_workers  W in [1, PSGD_UNC_MAX_WORKERS]
+ *   in           host array [W] of device fp32 pointers, len entries each, 16-byte aligned
+ *   len          entries per worker (>= 0; any value, the tail past a multiple of 4 included)
+ *   scale        the tensor's gradient scale s, finite and > 0 (1 when it is not scaled)
+ *   out          device fp32 [len], 16-byte aligned; may not overlap an input
+ *   counts       device int64 [W], 8-byte aligned
+ *   skip         device uint8 [1] or NULL
+ * One HBM sweep: W * len * 4 bytes read, len * 4 written. Asynchronous on `stream`;
+ * allocates nothing. PSGD_EINVAL before any launch on a bad argument. */
+#define PSGD_UNC_MAX_WORKERS 16
+psgd_status psgd_reduce_uncompressed(int32_t num_workers, const float* const* in, int64_t len,
+                                     float scale, float* out, int64_t* counts,
+                                     const uint8_t* skip, void* stream);
+
 /* Wait for `stream`, then report a device-side error raised by an earlier step
  * (PSGD_ETIMEOUT for an expired bounded wait), and clear it. */
 psgd_status psgd_check(psgd_handle* h, void* stream);
@@ -230,10 +263,9 @@ const char* psgd_engine(psgd_handle* h);
 
 /* Orthonormalise one fp32 matrix with scratch that is part of the library image.
  *
- * The pages have no counterpart of this call. It runs the adaptive shifted CholeskyQR
- * passes that psgd_step applies to each P ("Cholesky-QR or Gram-Schmidt in fp32" on the
- * reading card's PowerSGD list) for a single matrix, without a handle or a workspace,
- * and it allocates no memory of any kind. It serves callers that hold one P but no
+ * The pages have no counterpart of this call. It runs the orthonormalisation passes
+ * (adaptive shifted CholeskyQR in fp32) that psgd_step applies to each P, for a single
+ * matrix, without a handle or a workspace, and it allocates no memory of any kind. It serves callers that hold one P but no
  * handle and cannot allocate at that point: cudaMalloc/cudaFree synchronise the device
  * and would stall the work queued around the call, and a process whose device memory is
  * all handed out to a caching allocator or a fixed budget has none to give.
@@ -250,7 +282,10 @@ const char* psgd_engine(psgd_handle* h);
  * Scratch: a fixed __device__ array of 16.1 MiB in each device's copy of the library
  * module (Gram partial sums, R^-1, plan and pass state). The first call on a device
  * looks up that array's device address (cudaGetSymbolAddress, with the device current)
- * and keeps it; make that first call on each device before any stream capture begins.
+ * and keeps it, with the ID of the context it belongs to; make that first call on each
+ * device before any stream capture begins. After a device reset, or when the device's
+ * primary context is created anew, the next call is again a first call: it looks the
+ * address up again (so it, too, belongs outside a capture).
  * Every call clears the scratch words that must start at zero before it uses them.
  * All calls share the one array: calls that overlap on the GPU (different streams of a
  * device) race on it, so the caller must serialise them, e.g. on one stream.

@@ -33,9 +33,6 @@ Parity status per function:
   scale_update: pinned by the closed form 2^(e0 + growths - backoffs) for power-of-two
     factors over a long random finite/nonfinite sequence, by hand-worked sequences that
     include a drop below 1, and by the fp32 product of a non-power-of-two factor.
-  orthonormalize(method="cholqr_f32") is used only to derive a tolerance (an fp32
-    orthonormalisation's own distance from fp64). It is pinned by orthonormality and span
-    of well- and ill-conditioned inputs to fp32 accuracy.
   The values of P-hat and Q themselves depend on the basis and are not compared.
   Only G-hat, E, masks, counts and skips are compared.
 """
@@ -111,53 +108,29 @@ def scale_update(scale: float, streak: int, counts_per_worker, backoff: float, g
       after a backoff.
     - S is fp32 state. Each update is one IEEE single multiply by the factor rounded to
       fp32.
+    - The page leaves open what happens when S leaves fp32's range. Here an update whose
+      fp32 product is not a finite normal number (it overflows, or falls below 2^-126)
+      keeps S, and the streak restarts as if the update had happened. A scale of 0 or
+      Inf would turn every unscaled entry into a nonfinite value or into 0.
 
     Returns (S', streak').
     """
     s = np.float32(scale)
+
+    def scaled(f):
+        with np.errstate(over="ignore", under="ignore"):
+            t = np.float32(s * np.float32(f))
+        return t if (np.isfinite(t) and abs(float(t)) >= 2.0 ** -126) else s
+
     if int(np.sum(np.asarray(counts_per_worker, dtype=np.int64))) > 0:
-        return np.float32(s * np.float32(backoff)), 0
+        return scaled(backoff), 0
     streak = int(streak) + 1
     if streak >= int(interval):
-        return np.float32(s * np.float32(growth)), 0
+        return scaled(growth), 0
     return s, streak
 
 
 # ----------------------------------------------------------------------- power step
-def _cholqr_f32(p: np.ndarray, passes: int = 4) -> np.ndarray:
-    """Shifted CholeskyQR carried out in fp32 (numpy float32), four passes.
-
-    Not a parity reference. The method fixes the orthonormalisation as Cholesky-QR or
-    Gram-Schmidt in fp32. This function measures how far such an fp32 orthonormalisation
-    of the same P lands from the fp64 basis, so that a tolerance can be derived from that
-    arithmetic. Per pass: G = X^T X. If its Cholesky fails, or a pivot keeps less than
-    2^-16 of its diagonal, the pass uses G + s I with s = 2^-20 sqrt(m) tr(G) instead (the
-    shifted CholeskyQR of Fukaya et al., 2020). Then X <- X R^-1. X starts as P scaled
-    by a power of two that puts max|P| in [1, 2).
-    """
-    m = p.shape[0]
-    amax = float(np.max(np.abs(p))) if p.size else 0.0
-    if amax == 0.0:
-        return np.zeros_like(p, dtype=np.float64)
-    x = (p * 2.0 ** (-math.floor(math.log2(amax)))).astype(np.float32)
-    for _ in range(passes):
-        g = x.T @ x
-        lower = None
-        try:
-            lower = np.linalg.cholesky(g)
-            piv = np.diag(lower).astype(np.float64) ** 2
-            if np.any(piv < 2.0 ** -16 * np.diag(g).astype(np.float64)):
-                lower = None
-        except np.linalg.LinAlgError:
-            lower = None
-        if lower is None:
-            shift = np.float32(2.0 ** -20 * math.sqrt(m) * float(np.trace(g)))
-            lower = np.linalg.cholesky(g + shift * np.eye(g.shape[0], dtype=np.float32))
-        rinv = np.linalg.inv(lower.T).astype(np.float32)
-        x = (x @ rinv).astype(np.float32)
-    return x.astype(np.float64)
-
-
 def orthonormalize(p: np.ndarray, method: str = "householder") -> np.ndarray:
     """Orthonormal basis of span(P), as many columns as P.
 
@@ -168,8 +141,6 @@ def orthonormalize(p: np.ndarray, method: str = "householder") -> np.ndarray:
     if method == "householder":
         qm, _ = np.linalg.qr(p, mode="reduced")
         return qm
-    if method == "cholqr_f32":
-        return _cholqr_f32(p)
     if method == "mgs2":
         v = np.array(p, dtype=np.float64, copy=True)
         m, r = v.shape
@@ -192,8 +163,7 @@ class PowerStepResult:
     g_hat: np.ndarray  # decompressed gradient P_hat Q^T, m x n
 
 
-def power_step(ms, q: np.ndarray, orth: str = "householder", accum_noise: float = 0.0,
-               noise_seed: int = 0) -> PowerStepResult:
+def power_step(ms, q: np.ndarray, orth: str = "householder") -> PowerStepResult:
     """One warm-started subspace-iteration step over W workers that share Q.
 
     [card] 方法适配: the low-rank factors are all-reduced between machines instead of
@@ -208,27 +178,11 @@ def power_step(ms, q: np.ndarray, orth: str = "householder", accum_noise: float 
     not factor the mean through M-bar, so the linearity of the mean stays a pin and
     is not an assumption.
 
-    accum_noise = c > 0 models fp32 accumulation: it adds to each entry of P and of the new
-    Q the error c * u32 * z * sqrt(sum of its squared product terms), with z ~ N(0, 1)
-    seeded. That is the probabilistic rounding-error size of a blocked fp32 sum. The
-    default, 0, follows the algorithm. The option measures how much the step's outputs
-    move under the rounding an fp32 implementation's long accumulations leave. That is
-    large where the sums cancel: in the small singular directions of a decaying
-    spectrum the terms are kappa times the result. It sets the tolerance such inputs
-    are tested at.
     """
     w = len(ms)
-    rng = np.random.default_rng(noise_seed)
-    u32 = 2.0 ** -24
     p = sum(np.asarray(mw, dtype=np.float64) @ q for mw in ms) / w
-    if accum_noise > 0:
-        mag = np.sqrt(sum((np.asarray(mw, dtype=np.float64) ** 2) @ (q ** 2) for mw in ms)) / w
-        p = p + accum_noise * u32 * mag * rng.standard_normal(p.shape)
     p_hat = orthonormalize(p, orth)
     q_new = sum(np.asarray(mw, dtype=np.float64).T @ p_hat for mw in ms) / w
-    if accum_noise > 0:
-        mag = np.sqrt(sum((np.asarray(mw, dtype=np.float64) ** 2).T @ (p_hat ** 2) for mw in ms)) / w
-        q_new = q_new + accum_noise * u32 * mag * rng.standard_normal(q_new.shape)
     q_new = round_to_format(q_new, "f32")
     g_hat = p_hat @ q_new.T
     return PowerStepResult(p=p, p_hat=p_hat, q=q_new, g_hat=g_hat)
@@ -287,8 +241,7 @@ class BlockResult:
 
 
 def block_step(grads, state: BlockState, scale: float, err_fmt: str,
-               skip_fraction: float = 1.0, unc=None, orth: str = "householder",
-               accum_noise: float = 0.0):
+               skip_fraction: float = 1.0, unc=None, orth: str = "householder"):
     """One PowerSGD step for one resblock: every matrix j, every worker w.
 
     ``grads[j][w]`` holds the raw (scaled) gradient values as fp64, and ``unc[w]`` the raw
@@ -324,7 +277,7 @@ def block_step(grads, state: BlockState, scale: float, err_fmt: str,
             unc_out=None if unc is None else np.zeros_like(unc_mean))
     g_hats, e_pres, p_hats = [], [], []
     for j in range(J):
-        res = power_step(ms[j], state.q[j], orth, accum_noise, noise_seed=j)
+        res = power_step(ms[j], state.q[j], orth)
         state.q[j] = res.q
         pre_j = []
         for w in range(W):

@@ -200,6 +200,10 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
   h.ws_bytes = ws_bytes;
   std::string why;
   h.tc = h.edt != DT_F32 && !(cfg->flags & PSGD_FLAG_SIMT) && tc_supported(cfg, &why);
+  if ((cfg->flags & PSGD_FLAG_DEBUG_EXPIRE_WAIT) && !h.tc) {
+    delete ph;
+    return fail(PSGD_EUNSUPPORTED, "PSGD_FLAG_DEBUG_EXPIRE_WAIT needs the tensor engine");
+  }
 
   const int BJ = h.B * h.J;
   h.d_meta = reinterpret_cast<MatMeta*>(h.ws + L.meta);
@@ -334,7 +338,7 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   }
   for (size_t b = 0; b < B && !dev_scales; ++b) {
     const float s = a->scales[b];
-    if (!std::isfinite(s) || !(s >= 1.0f)) return fail(PSGD_EINVAL, "scales must be finite and >= 1");
+    if (!std::isfinite(s) || !(s > 0.0f)) return fail(PSGD_EINVAL, "scales must be finite and > 0");
   }
   if (h.cfg.unc_len > 0) {
     for (size_t i = 0; i < B * W; ++i)
@@ -388,6 +392,7 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   p.mask = (h.cfg.flags & PSGD_FLAG_MASK) ? a->mask_bits : nullptr;
   p.mask_off = h.d_mask_off;
   p.err_word = h.d_err;
+  p.debug_expire = (h.cfg.flags & PSGD_FLAG_DEBUG_EXPIRE_WAIT) ? 1 : 0;
 
   cudaEvent_t* ev = nullptr;
   if (h.prof_used < h.prof_max) ev = &h.prof_events[(size_t)h.prof_used++ * (PSGD_NUM_PHASES + 1)];

@@ -539,6 +539,18 @@ __global__ void __launch_bounds__(kCholThreads, 1) k_chol(Plan p, int pass) {
 }
 
 // X <- X R^-1 on 64-row tiles (R^-1 upper triangular, r <= 128). grid = (ceil(m/64), B*J).
+//
+// kAcc: every entry of X R^-1 is accumulated as a compensated dot product (dot2_acc) and
+// rounded once. The span of the result is what the step keeps: any invertible R leaves
+// span(X R^-1) = span(X) in exact arithmetic, so only the rounding of this product can move
+// the subspace. Plain fp32 sums lose up to u * |X| |R^-1| per entry, which is cond(X)
+// times the entry itself when the columns of X are nearly dependent (a warm-started P at
+// high rank, column-scaled condition number up to ~4e5 at r = 896 on a 1/k spectrum).
+// Compensated, each output column is within about u of its exact value relative to its
+// own size, the same as rounding P to fp32 once. The blocked orthonormalisation of ranks
+// above 128 uses it; at r <= 128 (warm-started P nearly orthogonal, one pass) the plain sum
+// is within the tolerance and half the instructions.
+template <bool kAcc>
 __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
@@ -561,11 +573,11 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
   // chunks of R^-1 below its strip (rows k > its last column: zero) are skipped whole.
   const int tid = threadIdx.x, tx = tid >> 4, ty = tid & 15;
   const int warp_last_col = (tid >> 5) * 16 + 15;
-  float acc[4][8];
+  float acc[4][8], lo[4][8];  // lo: compensation terms (kAcc only)
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 8; ++j) acc[i][j] = lo[i][j] = 0.f;
   // 16-byte loads and stores when the row pitch and the buffers allow them (always in
   // the step: pitch rp a multiple of 16, workspace buffers 256-byte aligned); scalar ones
   // otherwise (a caller's 4-byte-aligned matrix in the one-matrix entry point).
@@ -628,9 +640,18 @@ __global__ void __launch_bounds__(kT) k_apply(Plan p, int pass) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) {
+          if (kAcc) dot2_acc(acc[i][j], lo[i][j], a[i], b[j]);
+          else acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
     }
     __syncthreads();
+  }
+  if (kAcc) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = __fadd_rn(acc[i][j], lo[i][j]);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -762,6 +783,11 @@ __global__ void __launch_bounds__(kT) k_proj_sum(Plan p, int c0, int rb) {
 // Xa_blk = S_blk - P^[:, <c0] C on 64-row tiles (16 x 16 threads: 4 rows x 8 columns
 // each; K = c0 in chunks of 32). S may be Xa itself: a CTA reads the rows of S it writes
 // only at its end, and no other CTA touches them. grid = (ceil(m / 64), B*J).
+// Adding multiples of the finished columns to S_blk leaves span(P^[:, <c0], S_blk)
+// unchanged whatever C is, so the subspace moves only by the rounding of this update. It
+// is a compensated dot product (dot2_acc) and one exactly rounded subtraction (TwoSum),
+// so each entry is within about u of S - P^ C relative to itself, also where the block
+// is nearly inside the span of the finished columns and the subtraction cancels.
 __global__ void __launch_bounds__(kT) k_proj_apply(Plan p, int c0, int rb, int src_xa) {
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
@@ -775,11 +801,11 @@ __global__ void __launch_bounds__(kT) k_proj_apply(Plan p, int c0, int rb, int s
   __shared__ __align__(16) float As[32][64 + 4];
   __shared__ __align__(16) float Bs[32][128];
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  float acc[4][8];
+  float acc[4][8], lo[4][8];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 8; ++j) acc[i][j] = lo[i][j] = 0.f;
   for (int k0 = 0; k0 < c0; k0 += 32) {
     {
       const int rr = tid >> 2, kk = (tid & 3) * 8;
@@ -803,7 +829,7 @@ __global__ void __launch_bounds__(kT) k_proj_apply(Plan p, int c0, int rb, int s
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) dot2_acc(acc[i][j], lo[i][j], a[i], b[j]);
     }
     __syncthreads();
   }
@@ -814,7 +840,13 @@ __global__ void __launch_bounds__(kT) k_proj_apply(Plan p, int c0, int rb, int s
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int c = tx * 8 + j;
-      if (c < rb) Y[row * xl + c] = S[row * xl + c] - acc[i][j];
+      if (c < rb) {
+        // (S - hi) exactly as a sum of two floats, then the small terms, one rounding each
+        const float sv = S[row * xl + c], nh = -acc[i][j];
+        const float d = __fadd_rn(sv, nh), z = __fsub_rn(d, sv);
+        const float de = __fadd_rn(__fsub_rn(sv, __fsub_rn(d, z)), __fsub_rn(nh, z));
+        Y[row * xl + c] = __fadd_rn(d, __fsub_rn(de, lo[i][j]));
+      }
     }
   }
 }
@@ -852,7 +884,8 @@ cudaError_t launch_orth(const Handle& h, const Plan& p, cudaStream_t s) {
       }
       launch_pdl(k_gsum, dim3(gsum_blocks(pb.ob_rp), BJ), dim3(kT), 0, s, pb, pass);
       launch_pdl(k_chol, dim3(BJ), dim3(kCholThreads), kCholSmem, s, pb, pass);
-      launch_pdl(k_apply, dim3(h.max_mtiles64, BJ), dim3(kT), 0, s, pb, pass);
+      if (p.r > kRankBlock) launch_pdl(k_apply<true>, dim3(h.max_mtiles64, BJ), dim3(kT), 0, s, pb, pass);
+      else launch_pdl(k_apply<false>, dim3(h.max_mtiles64, BJ), dim3(kT), 0, s, pb, pass);
       h.launches += 3;
     }
   }
@@ -867,7 +900,7 @@ cudaError_t launch_orth_one(const Plan& p, int C, int mtiles64, cudaStream_t s) 
     if (pass == 0) launch_pdl(k_gram, dim3(C, 1), dim3(kGramThreads), 0, s, p, pass);
     launch_pdl(k_gsum, dim3(gsum_blocks(p.ob_rp), 1), dim3(kT), 0, s, p, pass);
     launch_pdl(k_chol, dim3(1), dim3(kCholThreads), kCholSmem, s, p, pass);
-    launch_pdl(k_apply, dim3(mtiles64, 1), dim3(kT), 0, s, p, pass);
+    launch_pdl(k_apply<false>, dim3(mtiles64, 1), dim3(kT), 0, s, p, pass);
   }
   return cudaGetLastError();
 }

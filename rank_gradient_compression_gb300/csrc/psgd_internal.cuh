@@ -79,6 +79,8 @@ struct Plan {
   // buffer pass 0 reads (0 = P, 1 = Xa, the block projected off the earlier blocks).
   // One block (ob_r = r, ob_rp = rp, ob_c0 = 0, ob_src0 = 0) when r <= kRankBlock.
   int32_t ob_r, ob_rp, ob_c0, ob_src0;
+  int32_t debug_expire;          // PSGD_FLAG_DEBUG_EXPIRE_WAIT: the decompression kernel's
+                                 // MMA thread waits on a barrier nothing completes
 };
 
 // Programmatic dependent launch. A kernel launched by launch_pdl may be scheduled while
@@ -170,6 +172,22 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 __device__ __forceinline__ float add_round_odd(float a, float b) {
   const float up = __fadd_ru(a, b), dn = __fadd_rd(a, b);
   return (up == dn || (__float_as_uint(up) & 1u)) ? up : dn;
+}
+
+// hi + lo += a * b, with hi + lo an unevaluated sum of two floats. The product's rounding
+// error comes out of one FMA (exact), the sum's from Knuth's branch-free TwoSum (exact), and
+// both go into lo. A dot product accumulated this way is as accurate as one carried in
+// twice the working precision and rounded once at the end (Ogita, Rump and Oishi,
+// "Accurate sum and dot product", 2005, Dot2). The _rn intrinsics keep the compiler from
+// contracting the error terms into FMAs.
+__device__ __forceinline__ void dot2_acc(float& hi, float& lo, float a, float b) {
+  const float p = __fmul_rn(a, b);
+  const float pe = fmaf(a, b, -p);
+  const float s = __fadd_rn(hi, p);
+  const float z = __fsub_rn(s, hi);
+  const float se = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, z)), __fsub_rn(p, z));
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(pe, se));
 }
 
 // round_E(a + b) with E = T; exact single rounding for 16-bit T, plain RN for fp32.

@@ -29,11 +29,15 @@ __global__ void k_scale_update(int B, int W, const int64_t* __restrict__ counts,
   for (int w = 0; w < W; ++w) c += counts[(int64_t)b * W + w];
   float s = scale[b];
   int k = streak[b];
+  // A product that is not a finite normal float (overflow, or below 2^-126) keeps S: a
+  // scale of Inf or 0 would make 1/S zero or Inf in the next step.
   if (c > 0) {
-    s = __fmul_rn(s, backoff);
+    const float t = __fmul_rn(s, backoff);
+    if (isfinite(t) && fabsf(t) >= 0x1p-126f) s = t;
     k = 0;
   } else if (++k >= interval) {
-    s = __fmul_rn(s, growth);
+    const float t = __fmul_rn(s, growth);
+    if (isfinite(t) && fabsf(t) >= 0x1p-126f) s = t;
     k = 0;
   }
   scale[b] = s;
@@ -69,17 +73,18 @@ extern "C" psgd_status psgd_scale_update(int32_t num_blocks, int32_t num_workers
     return report_error(PSGD_EINVAL, "counts, scale and streak must be device pointers");
   if (!aligned(counts, 8) || !aligned(scale, 4) || !aligned(streak, 4))
     return report_error(PSGD_EINVAL, "counts, scale and streak must be aligned to their element size");
-  if (!(backoff > 0.0 && backoff < 1.0))
-    return report_error(PSGD_EINVAL, "backoff must be in (0, 1)");
-  if (!(growth > 1.0) || !std::isfinite(growth))
-    return report_error(PSGD_EINVAL, "growth must be finite and > 1");
+  // The checks apply to the factors as the kernel uses them, rounded to fp32.
+  const float bf = (float)backoff, gf = (float)growth;
+  if (!(backoff > 0.0 && backoff < 1.0) || !(bf > 0.0f && bf < 1.0f))
+    return report_error(PSGD_EINVAL, "backoff must be in (0, 1) as an fp32 value");
+  if (!(growth > 1.0) || !std::isfinite(growth) || !(gf > 1.0f) || !std::isfinite(gf))
+    return report_error(PSGD_EINVAL, "growth must be finite and > 1 as an fp32 value");
   if (interval < 1) return report_error(PSGD_EINVAL, "interval must be >= 1");
   if ((int64_t)num_blocks * num_workers > ((int64_t)1 << 40))
     return report_error(PSGD_EINVAL, "num_blocks * num_workers is too large");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   k_scale_update<<<(num_blocks + 127) / 128, 128, 0, s>>>(
-      num_blocks, num_workers, counts, scale, reinterpret_cast<int*>(streak), (float)backoff,
-      (float)growth, interval);
+      num_blocks, num_workers, counts, scale, reinterpret_cast<int*>(streak), bf, gf, interval);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return report_cuda_error(e, "psgd_scale_update");
   return PSGD_OK;

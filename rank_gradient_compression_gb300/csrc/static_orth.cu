@@ -26,6 +26,8 @@
 // Order of calls: every call uses the one array, so calls that overlap on the GPU
 // (different streams of one device, or host threads that enqueue concurrently on
 // different streams) race on it. The caller serialises them, e.g. on one stream.
+#include <cuda.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -55,10 +57,39 @@ static_assert(kOffGpart % 256 == 0 && kStaticBytes % 256 == 0, "alignment");
 
 __device__ __align__(256) static unsigned char g_scratch[kStaticBytes];
 
-// Device address of g_scratch, looked up once per device (with that device current).
+// Device address of g_scratch, looked up with the device current and kept per device,
+// together with the ID of the CUDA context it belongs to. A later call in another context
+// of that device (after cudaDeviceReset, or when the primary context was released and
+// created again, which loads the module anew) looks the address up again instead of
+// using one that belonged to the old context.
 constexpr int kMaxDevices = 64;
 std::mutex g_addr_mu;
 unsigned char* g_addr[kMaxDevices] = {};
+unsigned long long g_ctx_id[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename F>
+F driver_fn(const char* name) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(f);
+}
+
+// ID of the calling thread's current context (0 if there is none or it cannot be read).
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_cur = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 psgd_status scratch_address(unsigned char** out) {
   int dev = -1;
@@ -67,12 +98,14 @@ psgd_status scratch_address(unsigned char** out) {
   if (dev < 0 || dev >= kMaxDevices)
     return report_error(PSGD_EUNSUPPORTED, "device index beyond the static scratch table");
   std::lock_guard<std::mutex> lock(g_addr_mu);
-  if (!g_addr[dev]) {
+  const unsigned long long id = current_ctx_id();
+  if (!g_addr[dev] || id == 0 || id != g_ctx_id[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_scratch);
+    e = cudaGetSymbolAddress(&p, g_scratch);  // makes the device's context current if needed
     if (e != cudaSuccess) return report_cuda_error(e, "cudaGetSymbolAddress(static scratch)");
     if (!p) return report_error(PSGD_ECUDA, "cudaGetSymbolAddress returned a null address");
     g_addr[dev] = static_cast<unsigned char*>(p);
+    g_ctx_id[dev] = current_ctx_id();
   }
   *out = g_addr[dev];
   return PSGD_OK;

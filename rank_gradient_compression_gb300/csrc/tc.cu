@@ -340,6 +340,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
     for (int i = 0; i < B_STAGES; ++i) { mbar_init(&sm.full_b[i], 1); mbar_init(&sm.empty_b[i], 1); }
     for (int i = 0; i < kGemmAccs; ++i) { mbar_init(&sm.acc_full[i], 1); mbar_init(&sm.acc_empty[i], kGemmEpiWarps); }
     mbar_init(&sm.done, 1);
+    abort_reset();
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -388,9 +389,9 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
       }
       // wait (bounded) for every load this thread issued before the CTA may exit
       for (uint32_t k = (ia > A_STAGES ? ia - A_STAGES : 0); k < ia; ++k)
-        mbar_wait(&sm.full_a[k % A_STAGES], (k / A_STAGES) & 1, err, 1u << 20);
+        mbar_drain(&sm.full_a[k % A_STAGES], (k / A_STAGES) & 1, err, 1u << 20);
       for (uint32_t k = (ib > B_STAGES ? ib - B_STAGES : 0); k < ib; ++k)
-        mbar_wait(&sm.full_b[k % B_STAGES], (k / B_STAGES) & 1, err, 1u << 20);
+        mbar_drain(&sm.full_b[k % B_STAGES], (k / B_STAGES) & 1, err, 1u << 20);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -447,7 +448,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
         }
       }
       umma_commit(&sm.done);
-      mbar_wait(&sm.done, 0, err, 1u << 22);
+      mbar_drain(&sm.done, 0, err, 1u << 22);
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..9)
@@ -604,6 +605,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
     for (int i = 0; i < ge_stages; ++i) { mbar_init(&sm.full_ge[i], 1); mbar_init(&sm.empty_ge[i], kIngWarps); }
     for (int i = 0; i < 2; ++i) { mbar_init(&sm.acc_full[i], 1); mbar_init(&sm.acc_empty[i], 4); }
     mbar_init(&sm.done, 1);
+    abort_reset();
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -636,7 +638,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
           }
       }
       for (uint32_t k = (ib > B_STAGES ? ib - B_STAGES : 0); k < ib; ++k)
-        mbar_wait(&sm.full_b[k % B_STAGES], (k / B_STAGES) & 1, err, 1u << 20);
+        mbar_drain(&sm.full_b[k % B_STAGES], (k / B_STAGES) & 1, err, 1u << 20);
     }
   } else if (warp == kIngGeWarp) {
     // ------------------------------------------------------------ TMA: G/E tiles
@@ -659,7 +661,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
         ti.next(units, nunits, p.W);
       }
       for (uint32_t k = (ig > (uint32_t)ge_stages ? ig - ge_stages : 0); k < ig; ++k)
-        mbar_wait(&sm.full_ge[k % ge_stages], (k / ge_stages) & 1, err, 1u << 20);
+        mbar_drain(&sm.full_ge[k % ge_stages], (k / ge_stages) & 1, err, 1u << 20);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -714,7 +716,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
         }
       }
       umma_commit(&sm.done);
-      mbar_wait(&sm.done, 0, err, 1u << 22);
+      mbar_drain(&sm.done, 0, err, 1u << 22);
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue (warps 2..5)
@@ -870,6 +872,7 @@ struct DecSmem {
   uint64_t full[DEC_STAGES], empty[DEC_STAGES];
   uint64_t acc_full[2], acc_empty[2], done;
   uint64_t mfull[DEC_MSTAGES], mdone[DEC_MSTAGES];
+  uint64_t never;  // no thread arrives on it (the PSGD_FLAG_DEBUG_EXPIRE_WAIT test wait)
   uint32_t tmem;
 };
 
@@ -894,7 +897,9 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
     for (int i = 0; i < DEC_STAGES; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&sm.acc_full[i], 1); mbar_init(&sm.acc_empty[i], 8); }
     for (int i = 0; i < DEC_MSTAGES; ++i) { mbar_init(&sm.mfull[i], 1); mbar_init(&sm.mdone[i], 8); }
+    mbar_init(&sm.never, 1);
     mbar_init(&sm.done, 1);
+    abort_reset();
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -928,7 +933,7 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
         }
       }
       for (uint32_t k = (it > DEC_STAGES ? it - DEC_STAGES : 0); k < it; ++k)
-        mbar_wait(&sm.full[k % DEC_STAGES], (k / DEC_STAGES) & 1, err, 1u << 20);
+        mbar_drain(&sm.full[k % DEC_STAGES], (k / DEC_STAGES) & 1, err, 1u << 20);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -936,6 +941,9 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
       const uint32_t idesc = idesc_f16(BM, DEC_NT, false, false, false);
       uint32_t it = 0, ju = 0;
       bool ok = true;
+      // Test of the expiry path: a short wait on a barrier that nothing completes. It
+      // expires, records DEVERR_TIMEOUT and raises the CTA's abort flag; the CTA winds down.
+      if (p.debug_expire) ok = mbar_wait(&sm.never, 0, err, 4096);
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const Unit un = units[u];
         if (p.skip[p.meta[un.t].b]) continue;
@@ -964,7 +972,7 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
         ++ju;
       }
       umma_commit(&sm.done);
-      mbar_wait(&sm.done, 0, err, 1u << 22);
+      mbar_drain(&sm.done, 0, err, 1u << 22);
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ TMA: M_w in, E_w out
@@ -1009,7 +1017,7 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
       for (uint32_t j = (i > DEC_MSTAGES ? i - DEC_MSTAGES : 0); j < i && ok; ++j) ok = store_tile(j);
       if (!ok)  // wait (bounded) for the loads this thread issued before the CTA may exit
         for (uint32_t j = (i > DEC_MSTAGES ? i - DEC_MSTAGES : 0); j < i; ++j)
-          mbar_wait(&sm.mfull[j % DEC_MSTAGES], (j / DEC_MSTAGES) & 1, err, 1u << 20);
+          mbar_drain(&sm.mfull[j % DEC_MSTAGES], (j / DEC_MSTAGES) & 1, err, 1u << 20);
       bulk_wait_all();
     }
   } else {

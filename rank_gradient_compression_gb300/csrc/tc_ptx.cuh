@@ -39,15 +39,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, polling at most `limit` times.
-// On expiry, record DEVERR_TIMEOUT in *err (if not already set) and return false; the
-// caller then stops issuing work and winds down.
+// Abort flag of the CTA. The first pipeline wait of a CTA that runs out of polls sets it,
+// and every other pipeline wait of that CTA then gives up within 64 polls instead of
+// running out its own limit, so a CTA with one expired wait winds down in microseconds.
+// Thread 0 clears it before the kernel's first block barrier (abort_reset).
+static __shared__ int s_abort;
+__device__ __forceinline__ void abort_reset() { s_abort = 0; }
+
+// Pipeline wait: wait for the phase with the given parity to complete, polling at most
+// `limit` times. On expiry, record DEVERR_TIMEOUT in *err (if not already set), raise the
+// CTA's abort flag and return false; it also returns false once another wait of the CTA
+// has raised the flag. The caller then stops issuing work and winds down.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err,
                                           uint32_t limit = PSGD_SPIN_LIMIT) {
   for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (i > 64) {
+      if (*reinterpret_cast<volatile int*>(&s_abort)) return false;
+      __nanosleep(32);
+    }
+  }
+  *reinterpret_cast<volatile int*>(&s_abort) = 1;
+  if (err) atomicCAS(err, DEVERR_NONE, DEVERR_TIMEOUT);
+  return false;
+}
+
+// Drain wait: the same, but it ignores the abort flag. A thread uses it for the loads it
+// issued itself (or the MMAs it committed) before the CTA may release shared memory or
+// TMEM: those complete whatever the rest of the pipeline does.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, int* err, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
     if (i > 64) __nanosleep(32);
   }
+  *reinterpret_cast<volatile int*>(&s_abort) = 1;
   if (err) atomicCAS(err, DEVERR_NONE, DEVERR_TIMEOUT);
   return false;
 }

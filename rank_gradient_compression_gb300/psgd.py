@@ -16,6 +16,7 @@ LIB_PATH = os.environ.get("PSGD_LIB", os.path.join(HERE, "libpsgd.so"))
 PSGD_F32, PSGD_F16, PSGD_BF16 = 0, 1, 2
 PSGD_OK, PSGD_EINVAL, PSGD_ECUDA, PSGD_EUNSUPPORTED, PSGD_ETIMEOUT = range(5)
 PSGD_FLAG_SIMT, PSGD_FLAG_MASK, PSGD_FLAG_STOP_AFTER_INGEST = 0x1, 0x2, 0x4
+PSGD_FLAG_DEBUG_EXPIRE_WAIT = 0x8
 
 DTYPE_CODE = {"f32": PSGD_F32, "f16": PSGD_F16, "bf16": PSGD_BF16}
 
@@ -25,10 +26,11 @@ EXPORTS = ("psgd_workspace_size", "psgd_mask_offset", "psgd_mask_words", "psgd_i
            "psgd_debug_m", "psgd_debug_phat", "psgd_engine", "psgd_profile_begin",
            "psgd_profile_end", "psgd_launch_count", "psgd_debug_orth",
            "psgd_orthonormalize_static", "psgd_scale_update", "psgd_clip_adam_workspace_size",
-           "psgd_clip_adam")
+           "psgd_clip_adam", "psgd_reduce_uncompressed")
 PSGD_STATIC_MAX_ROWS, PSGD_STATIC_MAX_COLS = 16384, 128
 PSGD_MAX_ORTH_PASSES = 4
 PSGD_ADAM_MAX_TENSORS = 512
+PSGD_UNC_MAX_WORKERS = 16
 PSGD_NUM_PHASES = 7
 PHASES = ("ingest", "skip_unc", "pgemm", "orth", "qgemm", "qreduce", "decomp")
 
@@ -111,6 +113,9 @@ def _load():
     lib.psgd_clip_adam_workspace_size.argtypes = [c_int32, POINTER(c_int64)]
     lib.psgd_clip_adam.restype = c_int32
     lib.psgd_clip_adam.argtypes = [POINTER(psgd_adam_args), c_void_p, c_size_t, c_void_p]
+    lib.psgd_reduce_uncompressed.restype = c_int32
+    lib.psgd_reduce_uncompressed.argtypes = [c_int32, POINTER(c_void_p), c_int64, ctypes.c_float,
+                                             c_void_p, c_void_p, c_void_p, c_void_p]
     lib.psgd_scale_update.restype = c_int32
     lib.psgd_scale_update.argtypes = [c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_double,
                                       c_double, c_int32, c_void_p]
@@ -224,6 +229,15 @@ def psgd_clip_adam(grads, params, exp_avg, exp_avg_sq, numel, workspace_ptr, ws_
                           c_void_p(skip_ptr), int(num_blocks), float(max_norm), float(lr),
                           float(beta1), float(beta2), float(eps), int(step), c_void_p(norm_out_ptr))
     _check(lib.psgd_clip_adam(byref(args), c_void_p(workspace_ptr), int(ws_bytes), c_void_p(stream)))
+
+
+def psgd_reduce_uncompressed(in_ptrs, length: int, scale: float, out_ptr: int, counts_ptr: int,
+                             skip_ptr: int = 0, stream: int = 0):
+    """out = mean over workers of the unscaled, nonfinite-zeroed fp32 inputs (device pointers)."""
+    W = len(in_ptrs)
+    arr = (c_void_p * max(W, 1))(*[int(x) for x in in_ptrs])
+    _check(lib.psgd_reduce_uncompressed(W, arr, int(length), float(scale), c_void_p(out_ptr),
+                                        c_void_p(counts_ptr), c_void_p(skip_ptr), c_void_p(stream)))
 
 
 def _ptrs(tensors):

@@ -237,3 +237,28 @@ def q0(wl: Workload, block: int, j: int) -> torch.Tensor:
 def zeros_err(wl: Workload, j: int) -> torch.Tensor:
     m, n = wl.shapes[j]
     return torch.zeros((m, n), dtype=TORCH_DTYPE[wl.err_dtype])
+
+
+# ------------------------------------------------------------- uncompressed tensors
+# The image vocabulary is 8192 and the transformer sees 256 text + 1024 image positions
+# with d_model = 3968 ("Zero-Shot Text-to-Image Generation - 中文验证版", §计算设置). The
+# pages do not give the text vocabulary, so the vocabulary-scale tensor here is the image
+# embedding (8192 x 3968); the unembedding has the same shape.
+IMAGE_VOCAB = 8192
+
+
+def embedding_grad(step: int, w: int, rows: int = IMAGE_VOCAB, cols: int = D_MODEL,
+                   log2_sig: int = -2, frac: float = 1e-3, scale_log2: int = 10) -> torch.Tensor:
+    """Raw (scaled) fp32 gradient of a vocabulary x d_model embedding on worker w, flattened:
+    N(0, 2^log2_sig) values (the true gradient times 2^scale_log2), and a fraction `frac`
+    of the entries at seeded positions set to +Inf, -Inf and NaN in thirds."""
+    rng = np.random.default_rng([BASE_SEED, _tag("embed"), step, rows, cols, w, scale_log2])
+    n = rows * cols
+    x = rng.standard_normal(n, dtype=np.float32) * np.float32(2.0 ** log2_sig)
+    cnt = int(round(frac * n))
+    pos = rng.choice(n, size=cnt, replace=False)
+    third = cnt // 3
+    x[pos[:third]] = np.inf
+    x[pos[third:2 * third]] = -np.inf
+    x[pos[2 * third:]] = np.nan
+    return torch.from_numpy(x)

@@ -102,6 +102,8 @@ _SCALER_OK = dict(num_blocks=2, num_workers=3, counts=0x10000, scale=0x20000, st
     (dict(scale=0x20002), "aligned"),
     (dict(backoff=1.0), "backoff"),
     (dict(backoff=0.0), "backoff"),
+    (dict(backoff=1e-50), "backoff"),
+    (dict(growth=1e300), "growth"),
     (dict(growth=1.0), "growth"),
     (dict(growth=float("inf")), "growth"),
     (dict(interval=0), "interval"),
@@ -133,5 +135,20 @@ def test_clip_adam_workspace_and_argument_checks(psgd):
                     (dict(skip_ptr=0x5000, block=[3], num_blocks=2), "block index")]:
         with pytest.raises(psgd.PSGDError) as ex:
             psgd.psgd_clip_adam(**dict(ok, **kw))
+        assert ex.value.status == psgd.PSGD_EINVAL
+        assert msg in str(ex.value), (kw, str(ex.value))
+
+
+def test_reduce_uncompressed_argument_checks(psgd):
+    """Argument errors of psgd_reduce_uncompressed, all answered before any launch."""
+    ok = dict(in_ptrs=[0x1000, 0x2000], length=16, scale=1.0, out_ptr=0x3000, counts_ptr=0x4000)
+    for kw, msg in [(dict(in_ptrs=[]), "num_workers"),
+                    (dict(in_ptrs=[0x1000] * (psgd.PSGD_UNC_MAX_WORKERS + 1)), "num_workers"),
+                    (dict(length=-1), "len"), (dict(scale=0.0), "scale"),
+                    (dict(scale=float("inf")), "scale"), (dict(out_ptr=0x3004), "aligned"),
+                    (dict(counts_ptr=0x4004), "aligned"), (dict(in_ptrs=[0x1000, 0x2008]), "aligned"),
+                    (dict(in_ptrs=[0x1000, 0]), "NULL"), (dict(out_ptr=0), "required")]:
+        with pytest.raises(psgd.PSGDError) as ex:
+            psgd.psgd_reduce_uncompressed(**dict(ok, **kw))
         assert ex.value.status == psgd.PSGD_EINVAL
         assert msg in str(ex.value), (kw, str(ex.value))

@@ -175,36 +175,22 @@ def test_spectrum_rank_sweep(rank):
     Ranks above 128 run on the FFMA engine with the orthonormalisation in 128-column
     blocks (block Gram-Schmidt with re-orthogonalisation, CholeskyQR within a block).
 
-    After a warm start, P has condition number about r^2 (up to 2e6 at r = 896), and
-    rounding in P is amplified into the span of P^. G-hat is held to the plain 1e-4. E is
-    held to max(1e-4, 4 s). Here s is the distance from the fp64 oracle of the same step
-    done with fp32 arithmetic where the method prescribes fp32: the orthonormalisation in
-    fp32 (shifted CholeskyQR), and the two GEMMs with modelled fp32 accumulation error.
-    At high rank E is only 2-4% of M, and s alone exceeds 1e-4 there (1.7e-4 for the
-    orthonormalisation at r = 896). s is computed only for the steps where E misses 1e-4."""
-    import copy
+    After the first warm start, P has condition number about 1.5e6 at r = 896 and its
+    columns, scaled to unit length, about 4e5. G-hat and E (before storage) are held to
+    the plain 1e-4 at every rank and step. Holding P in fp32 already costs about 4e-5 of
+    E at r = 896 there; the products that change the span of P (X R^-1 and the block
+    projections) are compensated so that the orthonormalisation adds little to it."""
     wl = synth.spectrum(rank=rank, steps=5)
     g = GpuRun(wl)
     o = OracleRun(wl, [0])
     for t in range(wl.steps):
         g.load_inputs(t)
         g.load_state(o)
-        before = copy.deepcopy(o.state[0])
         g.step()
         torch.cuda.synchronize()
         res = o.step(t)
-        # G-hat, masks, counts and M are held here; E (before storage) is checked below
-        errs = compare_step(g, res, o, tol=lambda kind, b, j: TOL if kind == "g" else np.inf)
-        e_bar, note = TOL, ""
-        if errs[1] > TOL:  # s is needed only where E misses the plain bar
-            grads = [[synth.grad(wl, t, 0, 0, w).double().numpy() for w in range(wl.workers)]]
-            pert = oracle.block_step(grads, copy.deepcopy(before), wl.scale(0), wl.err_dtype,
-                                     orth="cholqr_f32", accum_noise=14.0)
-            sens_e = rel_err(pert.e_pre[0][0], res[0].e_pre[0][0])
-            e_bar = max(TOL, 4 * sens_e)
-            note = f"; fp32-method sensitivity of E {sens_e:.2e}"
-        print(f"rank {rank} step {t}: GPU (G-hat, E, stored E) {errs}{note}; E bar {e_bar:.2e}")
-        assert errs[1] <= e_bar, f"rank {rank} step {t}: E rel err {errs[1]:.3e} > {e_bar:.3e}"
+        errs = compare_step(g, res, o)
+        print(f"rank {rank} step {t}: GPU (G-hat, E, stored E) {errs}")
 
 
 # ------------------------------------------------------------------ properties
@@ -304,6 +290,31 @@ def test_dynamic_scale_on_device_matches_oracle():
                     [2.0 ** 11, 2.0 ** 9], [2.0 ** 10, 2.0 ** 10]]
 
 
+def test_host_scale_below_one_matches_oracle():
+    """Host scales below 1 are accepted, as device scales are: s_b = 2^-1 multiplies the
+    raw gradient by 2 on unscaling (small ragged shapes, fp16, two steps)."""
+    from dataclasses import replace
+    wl = replace(synth.with_shapes(synth.resblock_shard(steps=2, workers=2, rank=8),
+                                   ((200, 136), (72, 64))), scale_log2=-1, sigma_raw=2.0 ** -6)
+    run_parity(wl)
+
+
+def test_scale_update_keeps_scales_in_the_normal_range():
+    """psgd_scale_update on the device at the ends of fp32's range: a growth from 2^127 and
+    a backoff from 2^-126 keep S (the oracle's reading), one step inside moves it."""
+    psgd = _psgd()
+    scale = torch.tensor([2.0 ** 127, 2.0 ** -126, 2.0 ** 126, 2.0 ** -125], device="cuda")
+    streak = torch.tensor([3, 0, 3, 0], dtype=torch.int32, device="cuda")
+    counts = torch.tensor([0, 4, 0, 1], dtype=torch.int64, device="cuda")
+    psgd.psgd_scale_update(4, 1, counts.data_ptr(), scale.data_ptr(), streak.data_ptr(), 0.5, 2.0,
+                           4, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    want = [oracle.scale_update(s0, k0, [c], 0.5, 2.0, 4)
+            for s0, k0, c in zip([2.0 ** 127, 2.0 ** -126, 2.0 ** 126, 2.0 ** -125], [3, 0, 3, 0], [0, 4, 0, 1])]
+    assert scale.cpu().tolist() == [float(w[0]) for w in want]
+    assert streak.cpu().tolist() == [w[1] for w in want]
+
+
 def test_argument_errors_return_status():
     psgd = _psgd()
     ps = psgd.PowerSGD([(64, 32)], 1, 1, 2, "f16")
@@ -311,9 +322,10 @@ def test_argument_errors_return_status():
     e = torch.zeros_like(g)
     q = torch.zeros((32, 2), device="cuda")
     gh = torch.zeros((64, 32), device="cuda")
-    with pytest.raises(psgd.PSGDError) as ex:
-        ps.step([[[g]]], [[[e]]], [[q]], [0.5], [[gh]])
-    assert ex.value.status == psgd.PSGD_EINVAL
+    for bad in (0.0, -1.0, float("nan")):
+        with pytest.raises(psgd.PSGDError) as ex:
+            ps.step([[[g]]], [[[e]]], [[q]], [bad], [[gh]])
+        assert ex.value.status == psgd.PSGD_EINVAL
     with pytest.raises(psgd.PSGDError) as ex:
         ps.step([[[g]]], [[[e]]], [[q]], [float("inf")], [[gh]])
     assert ex.value.status == psgd.PSGD_EINVAL
@@ -382,3 +394,63 @@ def test_clip_adam_matches_oracle():
             assert rel_err(d_gpu, d_ref) <= 1e-4, (step, t)
             assert rel_err(m[t].double().cpu().numpy(), ref[t][1]) <= 1e-5, (step, t)
             assert rel_err(v[t].double().cpu().numpy(), ref[t][2]) <= 1e-5, (step, t)
+
+
+# ------------------------------------------------------- vocabulary-scale uncompressed reduce
+@pytest.mark.parametrize("scale_log2,length", [(10, synth.IMAGE_VOCAB * synth.D_MODEL), (0, 4099)])
+def test_reduce_uncompressed_vocabulary_scale(scale_log2, length):
+    """The image-token embedding gradient (8192 x 3968 fp32, 130 MB per worker) over W = 8
+    workers, reduced in fp32 without compression, and a short ragged length. 0.1% of the
+    entries are +-Inf/NaN. Counts are bit-exact; the mean is within 1e-4 of the oracle's
+    (its fp64 mean rounded to fp32). With the skip flag set, the output is 0 and the
+    counts are still reported."""
+    psgd = _psgd()
+    W = 8
+    rows = synth.IMAGE_VOCAB if length == synth.IMAGE_VOCAB * synth.D_MODEL else 1
+    cols = length // rows
+    host = [synth.embedding_grad(0, w, rows=rows, cols=cols, scale_log2=scale_log2) for w in range(W)]
+    dev = [h.cuda() for h in host]
+    out = torch.empty(length, device="cuda")
+    counts = torch.zeros(W, dtype=torch.int64, device="cuda")
+    s = 2.0 ** scale_log2
+    stream = torch.cuda.current_stream().cuda_stream
+    psgd.psgd_reduce_uncompressed([t.data_ptr() for t in dev], length, s, out.data_ptr(),
+                                  counts.data_ptr(), 0, stream)
+    torch.cuda.synchronize()
+    mean, _, cnt = oracle.uncompressed_mean([h.double().numpy() for h in host], s)
+    assert counts.cpu().tolist() == cnt
+    ref = oracle.round_to_format(mean, "f32")
+    assert rel_err(f64(out), ref) <= TOL
+    skip = torch.ones(1, dtype=torch.uint8, device="cuda")
+    psgd.psgd_reduce_uncompressed([t.data_ptr() for t in dev], length, s, out.data_ptr(),
+                                  counts.data_ptr(), skip.data_ptr(), stream)
+    torch.cuda.synchronize()
+    assert counts.cpu().tolist() == cnt
+    assert not bool(out.any())
+
+
+def test_expired_wait_reports_timeout_and_next_step_is_correct():
+    """The bounded-wait path on the GPU, without a fault: with PSGD_FLAG_DEBUG_EXPIRE_WAIT
+    every CTA of the decompression kernel waits on a barrier that nothing completes. The
+    wait expires after its short limit, the CTA winds down (its own loads and MMAs drained,
+    TMEM released), and psgd_check reports PSGD_ETIMEOUT once. A normal handle in the same
+    context then runs a step that matches the oracle."""
+    psgd = _psgd()
+    wl = synth.with_shapes(synth.resblock_shard(steps=1, workers=2, rank=16), ((384, 256), (256, 136)))
+    o = OracleRun(wl, range(wl.blocks))
+    bad = GpuRun(wl, flags=psgd.PSGD_FLAG_DEBUG_EXPIRE_WAIT)
+    assert bad.ps.engine == "tcgen05"
+    bad.load_inputs(0)
+    bad.load_state(o)
+    bad.step()
+    with pytest.raises(psgd.PSGDError) as ex:
+        bad.ps.check()
+    assert ex.value.status == psgd.PSGD_ETIMEOUT
+    bad.ps.check()  # the error word was cleared
+    g = GpuRun(wl)
+    g.load_inputs(0)
+    g.load_state(o)
+    g.step()
+    torch.cuda.synchronize()
+    compare_step(g, o.step(0), o)
+    g.ps.check()

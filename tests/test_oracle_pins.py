@@ -369,24 +369,6 @@ def test_parameter_count_is_12B():
     assert 64 * sum(m * n for m, n in synth.SHARD_SHAPES) * 8 == 64 * 12 * 3968 ** 2
 
 
-def test_fp32_cholesky_qr_orthonormal_basis_of_span():
-    """The fp32 shifted CholeskyQR (used only to derive a tolerance) returns an
-    orthonormal basis of span(P) to fp32 accuracy: on a well-conditioned P, and on a P
-    with condition number 1e6 (the shift path), where the columns stay orthonormal and
-    the span of P's dominant part is kept."""
-    rng = np.random.default_rng(3)
-    p = rng.standard_normal((300, 24))
-    x = oracle.orthonormalize(p, "cholqr_f32")
-    assert np.abs(x.T @ x - np.eye(24)).max() < 1e-5
-    assert np.linalg.norm(x @ (x.T @ p) - p) / np.linalg.norm(p) < 1e-5
-    u = np.linalg.qr(rng.standard_normal((400, 32)))[0]
-    v = np.linalg.qr(rng.standard_normal((32, 32)))[0]
-    p = (u * np.logspace(0, -6, 32)) @ v.T
-    x = oracle.orthonormalize(p, "cholqr_f32")
-    assert np.abs(x.T @ x - np.eye(32)).max() < 1e-5
-    assert np.linalg.norm(x @ (x.T @ p) - p) / np.linalg.norm(p) < 1e-5
-
-
 # ------------------------------------------------------------- dynamic scale ([amp] §3.2)
 def _run_scaler(s0, events, backoff, growth, interval):
     s, k, trace = s0, 0, []
@@ -445,6 +427,20 @@ def test_scale_update_rounds_each_product_to_fp32():
     assert s == np.float32(300.0) and s.dtype == np.float32
     s, _ = oracle.scale_update(s, 0, [1], 0.3, 2.0, 4)
     assert s == np.float32(90.0)
+
+
+def test_scale_update_stays_a_finite_normal_float():
+    """At the ends of fp32's range the update keeps S: 2^127 * 2 overflows and 2^-126 / 2
+    is subnormal, so both stay; the streak still restarts. One step inside the range
+    moves as usual (2^126 * 2 = 2^127, 2^-125 / 2 = 2^-126)."""
+    big, tiny = np.float32(2.0 ** 127), np.float32(2.0 ** -126)
+    assert oracle.scale_update(big, 3, [0], 0.5, 2.0, 4) == (big, 0)
+    assert oracle.scale_update(tiny, 2, [5], 0.5, 2.0, 4) == (tiny, 0)
+    assert oracle.scale_update(np.float32(2.0 ** 126), 3, [0], 0.5, 2.0, 4)[0] == big
+    assert oracle.scale_update(np.float32(2.0 ** -125), 0, [1], 0.5, 2.0, 4)[0] == tiny
+    # a backoff that would go below the normal range from a non-power-of-two scale
+    s = np.float32(1.5 * 2.0 ** -126)
+    assert oracle.scale_update(s, 0, [1], 0.5, 2.0, 4)[0] == s
 
 
 # ------------------------------------------- consumer of G-hat: clipping + Adam ([amp] §6.2)
