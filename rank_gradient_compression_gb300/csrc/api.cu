@@ -41,7 +41,7 @@ int64_t slice_rows(const psgd_config* c) {
 struct Layout {
   size_t total = 0;
   size_t meta = 0, threshold = 0, mask_off = 0, segs = 0, table = 0, err = 0, scal = 0;
-  size_t inv_dev = 0;
+  size_t inv_dev = 0, gbar = 0;
   std::vector<size_t> mscr, P, Xa, Xb, Phat, ostate, Qpart, Gpart, Rinv;
   size_t tc = 0;
   size_t table_bytes = 0, maps_bytes = 0;
@@ -96,6 +96,7 @@ Layout plan_layout(const psgd_config* c) {
   L.err = take(16);
   L.scal = take(4 * kScalWords * (size_t)B * J);
   L.inv_dev = take(4 * (size_t)B);
+  L.gbar = take(sizeof(GridBarrier));
   for (int t = 0; t < B * J; ++t) {
     const psgd_shape s = c->shapes[t % J];
     const int64_t mpad = ceil_div(s.m, 128) * 128;
@@ -216,6 +217,7 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
   h.d_err = reinterpret_cast<int*>(h.ws + L.err);
   h.d_scal_all = reinterpret_cast<float*>(h.ws + L.scal);
   h.d_inv_dev = reinterpret_cast<float*>(h.ws + L.inv_dev);
+  h.d_gbar = reinterpret_cast<GridBarrier*>(h.ws + L.gbar);
 
   h.meta.resize(BJ);
   for (int t = 0; t < BJ; ++t) {
@@ -369,7 +371,7 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   if (!h.have_table || tab != h.last_table) {
     if (h.have_table && (e = cudaEventSynchronize(h.upload_ev)) != cudaSuccess) return cuda_fail(e, "table event");
     std::memcpy(h.h_stage, tab.data(), h.table_bytes);
-    if (h.maps_bytes && !tc_encode_ge_maps(h, a->grads, a->errs, h.h_stage + h.table_bytes))
+    if (h.maps_bytes && !tc_encode_ge_maps(h, a->grads, a->errs, a->ghat, h.h_stage + h.table_bytes))
       return fail(PSGD_ECUDA, "cuTensorMapEncodeTiled failed for a gradient or error buffer");
     if ((e = cudaMemcpyAsync(h.d_table, h.h_stage, h.table_bytes + h.maps_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
       return cuda_fail(e, "table upload");
@@ -433,10 +435,22 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
     if ((e = launch_pgemm_simt(h, p, s)) != cudaSuccess) return cuda_fail(e, "pgemm");
   }
   mark();
-  if ((e = launch_orth(h, p, s)) != cudaSuccess) return cuda_fail(e, "orth");
+  if (h.r <= kRankBlock) {
+    // Pass 0 as separate kernels; the later passes, which a warm-started P rarely needs,
+    // in one cooperative launch that leaves at once when none is needed.
+    if ((e = launch_orth_passes(h, p, 0, 0, s)) != cudaSuccess) return cuda_fail(e, "orth");
+    e = launch_orth_coop(h, p, false, false, 0, tc_pchunk_kb(), 1, s);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+      cudaGetLastError();  // nothing was enqueued: separate kernels for the later passes
+      e = launch_orth_passes(h, p, 1, kMaxPasses - 1, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "orth");
+  } else if ((e = launch_orth(h, p, s)) != cudaSuccess) {
+    return cuda_fail(e, "orth");
+  }
   mark();
   if (h.tc) {
-    if ((e = launch_qgemm_tc(h, p, s)) != cudaSuccess) return cuda_fail(e, "qgemm_tc");
+    if ((e = launch_qgemm_tc(h, p, s, false)) != cudaSuccess) return cuda_fail(e, "qgemm_tc");
   } else if ((e = launch_qgemm_simt(h, p, s)) != cudaSuccess) {
     return cuda_fail(e, "qgemm");
   }

@@ -53,6 +53,7 @@ struct Handle {
   int* d_err = nullptr;
   float* d_scal_all = nullptr;  // [B*J*kScalWords] scaling words, zeroed every step
   float* d_inv_dev = nullptr;   // [B] 1/s_b formed on the device (psgd_step_args.scales_device)
+  GridBarrier* d_gbar = nullptr;  // the cooperative orthonormalisation kernel's barrier
   size_t maps_bytes = 0;        // TMA maps of the callers' G and E (tensor engine), after the table
   int max_mtiles = 0, max_S = 0, max_C = 0, max_ntiles64 = 0, max_mtiles64 = 0;
   int max_kchunks = 0, max_ntiles128 = 0;
@@ -72,9 +73,12 @@ cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_ingest_p(const Handle& h, const Plan& p, cudaStream_t s);
 cudaError_t launch_preduce(const Handle& h, const Plan& p, cudaStream_t s);
 size_t tc_ge_maps_bytes(const psgd_config* cfg);
-bool tc_encode_ge_maps(const Handle& h, const void* const* grads, void* const* errs, void* out);
+bool tc_encode_ge_maps(const Handle& h, const void* const* grads, void* const* errs, float* const* ghat,
+                       void* out);
 cudaError_t launch_rescale_tiny(const Handle& h, const Plan& p, cudaStream_t s);
-cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s, bool psplit_done);
+int tc_kpad(const Handle& h);
+int tc_pchunk_kb();
 cudaError_t launch_decomp_tc(const Handle& h, const Plan& p, cudaStream_t s);
 void tc_free(Handle& h);
 
@@ -85,6 +89,18 @@ psgd_status report_cuda_error(cudaError_t e, const char* where);
 // The orthonormalisation passes for one matrix whose plan, pass state and scratch were
 // not laid out by psgd_init (orth.cu). C: Gram row chunks; mtiles64: 64-row tiles.
 cudaError_t launch_orth_one(const Plan& p, int C, int mtiles64, cudaStream_t s);
+
+// The orthonormalisation of every matrix (r <= kRankBlock) in one cooperative launch
+// (orth_coop.cu): optionally forms P from the tensor engine's partial sums first and
+// writes the split P^ operands last. Returns cudaErrorCooperativeLaunchTooLarge, with
+// nothing enqueued, when the device cannot hold the grid; the caller then uses the
+// separate kernels.
+cudaError_t launch_orth_coop(const Handle& h, const Plan& p, bool fused_preduce, bool do_psplit, int kp,
+                             int pchunk_kb, int start_pass, cudaStream_t s);
+// The orthonormalisation of the step: separate kernels for pass 0, then (r <= kRankBlock)
+// the cooperative kernel for the passes after it, or separate kernels for all passes.
+cudaError_t launch_orth_passes(const Handle& h, const Plan& p, int first_pass, int last_pass, cudaStream_t s);
+int orth_coop_grid();
 cudaError_t launch_inv_scale(int B, const float* scale, float* inv, cudaStream_t s);
 
 }  // namespace psgd

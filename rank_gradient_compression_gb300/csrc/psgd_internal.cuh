@@ -59,6 +59,12 @@ struct StepTable {
   const void* ge_maps;           // [B*J*W][2] TMA maps of G and E (tensor engine) or null
 };
 
+// State of the cooperative orthonormalisation kernel's grid barrier (workspace; zeroed
+// before every launch): arrivals, generation, and a flag that an expired wait raises.
+struct GridBarrier {
+  unsigned count, gen, abort, pad;
+};
+
 constexpr int kScalWords = 8;
 enum { SC_MAXM = 0, SC_MAXP = 1, SC_MAXQ = 2, SC_MAXQN = 3, SC_MSHIFT = 4 };
 
@@ -106,6 +112,16 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+// Barrier policies of device code that a group of threads runs: the whole CTA
+// (__syncthreads), or one 256-thread half of a 512-thread CTA (named barrier 1 or 2).
+struct CtaBar {
+  __device__ __forceinline__ void sync() const { __syncthreads(); }
+};
+struct HalfBar {
+  uint32_t id;
+  __device__ __forceinline__ void sync() const { asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory"); }
+};
 
 // Max of v over the block, returned in thread 0 (every thread of the block must call it;
 // blockDim.x a multiple of 32). One atomic per block instead of one per warp: atomics on

@@ -195,41 +195,61 @@ __global__ void __launch_bounds__(kT) k_qgemm(Plan p) {
   }
 }
 
-// Q = (sum_s Qpart[s]) * qscale / W in slice order -> the caller's fp32 Q state (n x r),
-// and max|Q| -> scal[3]. qscale undoes the power-of-two scale of a split P^ (exact).
+// Q = (sum over slices of Qpart) * qscale / W -> the caller's fp32 Q state (n x r), and
+// max|Q| -> scal[3]. qscale undoes the power-of-two scale of a split P^ (exact).
+// Four warps share a row of Q: warp g sums the slices s = g, g + 4, ... in order (all of
+// its loads in flight together), and the four sums are added in the order g = 0, 1, 2, 3,
+// a fixed order whatever the run. Lane l takes 4 consecutive columns per 128-column
+// chunk of the row (one 16-byte load per slice; rp is a multiple of 16).
+// grid = (ceil(max n / 2), B*J), 256 threads: rows 2 blockIdx.x and 2 blockIdx.x + 1.
+constexpr int kQredSplit = 4;
 __global__ void __launch_bounds__(256) k_qreduce(Plan p, float qscale) {
   pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
-  // one warp per row of Q; lane covers columns lane, lane + 32, ...
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = warp & (kQredSplit - 1);
+  const int64_t row = (int64_t)blockIdx.x * 2 + (warp >> 2);
+  if ((int64_t)blockIdx.x * 2 >= mt.n) return;  // whole block past the end (block-uniform)
   const float fw = (float)p.W;
   float* q = p.tab.q[blockIdx.y];
   const int msh = reinterpret_cast<const int*>(mt.scal)[SC_MSHIFT];  // rescaled M: Q * 2^msh
   const size_t stride = (size_t)mt.n * p.rp;  // one slice of Qpart
+  __shared__ float4 part[2][kQredSplit][32];
   unsigned vmax = 0u;
-  if (row < mt.n) {
-    // lane takes 4 consecutive columns (one 16-byte load per slice; rp is a multiple of 16)
-    for (int c0 = lane * 4; c0 < p.r; c0 += 128) {
-      const float* src = mt.Qpart + (size_t)row * p.rp + c0;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-      for (int s = 0; s < mt.S; ++s) {
-        const float4 v = *reinterpret_cast<const float4*>(src + (size_t)s * stride);
+  for (int c0 = 0; c0 < p.r; c0 += 128) {
+    const int c = c0 + lane * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < mt.n && c < p.r) {
+      const float* src = mt.Qpart + (size_t)row * p.rp + c;
+#pragma unroll 16
+      for (int s = g; s < mt.S; s += kQredSplit) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(src + (size_t)s * stride));
         acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
         acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
       }
-      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+    }
+    part[warp >> 2][g][lane] = acc;
+    __syncthreads();
+    if (g == 0 && row < mt.n && c < p.r) {
+      float4 t = part[warp >> 2][0][lane];
+#pragma unroll
+      for (int k = 1; k < kQredSplit; ++k) {
+        const float4 v = part[warp >> 2][k][lane];
+        t.x = __fadd_rn(t.x, v.x); t.y = __fadd_rn(t.y, v.y);
+        t.z = __fadd_rn(t.z, v.z); t.w = __fadd_rn(t.w, v.w);
+      }
+      const float a4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        if (c0 + i < p.r) {
+        if (c + i < p.r) {
           const float v = ldexpf(__fdiv_rn(a4[i] * qscale, fw), -msh);
-          q[row * p.r + c0 + i] = v;
+          q[row * p.r + c + i] = v;
           vmax = max(vmax, __float_as_uint(fabsf(v)));
         }
       }
     }
+    __syncthreads();
   }
   vmax = block_max_u32(vmax);
   if (threadIdx.x == 0 && vmax) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 3, vmax);
@@ -343,7 +363,7 @@ cudaError_t launch_qgemm_simt(const Handle& h, const Plan& p, cudaStream_t s) {
 cudaError_t launch_qreduce(const Handle& h, const Plan& p, cudaStream_t s) {
   int64_t max_n = 0;
   for (const MatMeta& mt : h.meta) max_n = std::max<int64_t>(max_n, mt.n);
-  dim3 grid((unsigned)((max_n + 7) / 8), p.B * p.J);
+  dim3 grid((unsigned)((max_n + 1) / 2), p.B * p.J);
   launch_pdl(k_qreduce, dim3(grid), dim3(256), 0, s, p, h.tc ? 0x1p-14f : 1.0f);
   h.launches += 1;
   return cudaGetLastError();

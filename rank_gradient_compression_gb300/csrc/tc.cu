@@ -29,13 +29,16 @@
 #include <vector>
 
 #include "handle.h"
+#include "split_dev.cuh"
 #include "tc_ptx.cuh"
 
 namespace psgd {
 namespace {
 
 using namespace tc;
+using namespace splitdev;
 
+constexpr int kDynSmemCap = 227 * 1024 - 256;  // dynamic shared memory of the persistent kernels
 constexpr int BM = 128;                // MMA M and A-tile rows (MN extent)
 constexpr int BK = 64;                 // K per stage (one 128-byte swizzle span)
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
@@ -71,46 +74,13 @@ struct TcPlan {
   Unit* d_dunits = nullptr;
   int np = 0, nq = 0, nd = 0;
   int kp = 0;                      // K pad of each decompression term (multiple of 64)
+  int qkps = 1;                    // Q GEMM k-blocks per stage
   int grid = 0;
 };
 
 __host__ __device__ inline int kpad_of(int rp) { return (rp + 63) / 64 * 64; }
 
 // ---------------------------------------------------------------- small kernels
-__device__ __forceinline__ int exp_of_max(unsigned bits) {  // floor(log2 max|x|)
-  if (bits == 0u) return 0;
-  const int ex = (int)((bits >> 23) & 0xff);
-  return (ex == 0 ? -126 : ex - 127);
-}
-
-template <typename T> __device__ __forceinline__ uint16_t bits16(T x) {
-  return *reinterpret_cast<uint16_t*>(&x);
-}
-
-// Split x*2^e into hi + lo in type T (RNE each).
-template <typename T>
-__device__ __forceinline__ void split2(float xs, uint16_t& hi, uint16_t& lo) {
-  const T h = from_f<T>(xs);
-  const T l = from_f<T>(__fsub_rn(xs, to_f(h)));
-  hi = bits16(h);
-  lo = bits16(l);
-}
-
-// Split x*2^e into hi + mid + lo in type T (RNE each). Each remainder is exact in fp32.
-template <typename T>
-__device__ __forceinline__ void split3(float xs, uint16_t& hi, uint16_t& mid, uint16_t& lo) {
-  const T h = from_f<T>(xs);
-  const float r1 = __fsub_rn(xs, to_f(h));
-  const T m = from_f<T>(r1);
-  const T l = from_f<T>(__fsub_rn(r1, to_f(m)));
-  hi = bits16(h);
-  mid = bits16(m);
-  lo = bits16(l);
-}
-
-// Number of 16-bit terms the fp32 operand of the P and Q GEMMs is split into.
-template <typename T> __host__ __device__ constexpr int nterms() { return sizeof(T) == 2 && !std::is_same<T, __half>::value ? 3 : 2; }
-
 // max|Q| of the caller's Q state -> scal[2] (bits). grid = (qmax_blocks, B*J). This and k_qsplit
 // run for every matrix: they can precede the skip decision of the step.
 __global__ void k_qmax(Plan p) {
@@ -198,55 +168,15 @@ __global__ void k_preduce(Plan p, int pchunk_kb) {
   if (threadIdx.x == 0 && mx) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 1, mx);
 }
 
-// From P^ (m x rp fp32, |entries| <= 1): psplit[terms*rp][mpad] = the terms of
-// (P^ * 2^14)^T in type T (the type of M), and pdec[mpad][3 kp] = [hi | lo | hi] in fp16
-// for the decompression. A block stages 32 rows of P^ (one contiguous run) in shared
-// memory; pdec rows are written 8 columns per 16-byte store, psplit rows 8 rows of P^
-// per 16-byte store. grid = (mpad / 32, B*J).
+// From P^ (m x rp fp32): the Q GEMM's split operand and the decompression's A operand,
+// 32 rows of P^ per CTA (psplit_rows). grid = (mpad / 32, B*J).
 template <typename T>
 __global__ void __launch_bounds__(256) k_psplit(Plan p, int kp) {
   pdl_wait();
   const MatMeta& mt = p.meta[blockIdx.y];
   if (p.skip[mt.b]) return;
-  const int64_t mpad = (mt.m + 127) / 128 * 128;
-  const int64_t row0 = (int64_t)blockIdx.x * 32;
-  if (row0 >= mpad) return;
-  const int r = p.r, rp = p.rp;
   __shared__ float xs[32][kRankBlock + 1];
-  const int64_t left = mt.m - row0;
-  const int nrows = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
-  const float* src = mt.Phat + row0 * rp;
-  stage_rows<256>(xs, src, nrows * rp, rp,  // * 2^14, exact
-                  [r](float v, int c) { return c < r ? v * 16384.0f : 0.f; });
-  __syncthreads();
-  // pdec rows: [hi | lo | hi], kp / 8 groups of 8 columns per segment
-  const int gpr = kp / 8;
-  for (int it = threadIdx.x; it < 32 * gpr; it += blockDim.x) {
-    const int rr = it / gpr, c0 = (it - rr * gpr) * 8;
-    __align__(16) uint16_t hh[8], hl[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) split2<__half>(c0 + i < rp ? xs[rr][c0 + i] : 0.f, hh[i], hl[i]);
-    uint16_t* pd = mt.pdec + (size_t)(row0 + rr) * 3 * kp;
-    *reinterpret_cast<uint4*>(pd + c0) = *reinterpret_cast<const uint4*>(hh);
-    *reinterpret_cast<uint4*>(pd + kp + c0) = *reinterpret_cast<const uint4*>(hl);
-    *reinterpret_cast<uint4*>(pd + 2 * kp + c0) = *reinterpret_cast<const uint4*>(hh);
-  }
-  // psplit rows: term k of column c, rows row0 + 8g .. row0 + 8g + 7
-  for (int it = threadIdx.x; it < rp * 4; it += blockDim.x) {
-    const int c = it >> 2, g = it & 3;
-    __align__(16) uint16_t t0[8], t1[8], t2[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      t2[i] = 0;
-      if (nterms<T>() == 3) split3<T>(xs[8 * g + i][c], t0[i], t1[i], t2[i]);
-      else split2<T>(xs[8 * g + i][c], t0[i], t1[i]);
-    }
-    const size_t col = (size_t)row0 + 8 * g;
-    *reinterpret_cast<uint4*>(mt.psplit + (size_t)c * mpad + col) = *reinterpret_cast<const uint4*>(t0);
-    *reinterpret_cast<uint4*>(mt.psplit + (size_t)(rp + c) * mpad + col) = *reinterpret_cast<const uint4*>(t1);
-    if (nterms<T>() == 3)
-      *reinterpret_cast<uint4*>(mt.psplit + (size_t)(2 * rp + c) * mpad + col) = *reinterpret_cast<const uint4*>(t2);
-  }
+  psplit_rows<T>(p, mt, kp, blockIdx.x, xs, threadIdx.x, CtaBar{});
 }
 
 // qdec[npad][3 kp] = [hi | hi | lo] of the new Q * 2^e in fp16 (e from max|Q|, scal[3]).
@@ -296,7 +226,8 @@ struct GemmSmem {
   uint8_t* a0;
   uint8_t* b0;
   GemmBars* bar;
-  __device__ uint8_t* a(int s) const { return a0 + (size_t)s * A_BYTES; }
+  uint32_t a_bytes;
+  __device__ uint8_t* a(int s) const { return a0 + (size_t)s * a_bytes; }
   __device__ uint8_t* b(int s, uint32_t b_stage) const { return b0 + (size_t)s * b_stage; }
 };
 
@@ -309,17 +240,22 @@ __device__ __forceinline__ bool unit_off(const Plan& p, const MatMeta& mt, int o
 
 // MN_A = false: P GEMM (A = M tile K-major, unit = row tile x k-chunk).
 // MN_A = true:  Q GEMM (A = M^T tile MN-major, unit = column tile x m-slice).
+// kps (Q GEMM): k-blocks per stage. With 2, an A stage is 128 rows of M (two 64 x 128-row
+// boxes, 32 KB) and a B stage holds the two k-blocks' split P^ tiles. 128-row boxes read
+// HBM at 5.7 TB/s where 64-row boxes of the same columns reach 3.6 (a pure TMA read of
+// the M scratch on GB300). The MMA steps through the stage's k-blocks in order.
 constexpr int kGemmThreads = 320;  // warps: 0 TMA, 1 MMA, 2..9 epilogue
 constexpr int kGemmEpiWarps = 8;   // two per TMEM lane quarter, each with half the columns
 template <bool MN_A, bool BF16>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
-       int a_stages, uint32_t b_stage, int only_shifted, int seg) {
+       int a_stages, uint32_t b_stage, int only_shifted, int seg, int kps) {
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  GemmSmem S{base, base + (size_t)a_stages * A_BYTES,
-             reinterpret_cast<GemmBars*>(base + (size_t)a_stages * A_BYTES + (size_t)B_STAGES * b_stage)};
+  const uint32_t a_bytes = (uint32_t)kps * A_BYTES;  // one A stage
+  GemmSmem S{base, base + (size_t)a_stages * a_bytes,
+             reinterpret_cast<GemmBars*>(base + (size_t)a_stages * a_bytes + (size_t)B_STAGES * b_stage), a_bytes};
   GemmBars& sm = *S.bar;
   const int A_STAGES = a_stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -332,7 +268,8 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
   constexpr uint32_t kAccCols = 128;
   static_assert(NACC * kAccCols <= 512 && kAccCols >= kRankBlock, "accumulators fit in TMEM");
   const int NBOX = N <= 256 ? 1 : 2;            // TMA boxes per B tile (<= 256 rows each)
-  const uint32_t b_bytes = (uint32_t)N * BK * 2;
+  const uint32_t b_bytes = (uint32_t)N * BK * 2;  // one k-block's B tile
+  const uint32_t b_tile = b_stage / (uint32_t)kps;  // its slot in a B stage (1 KB multiple)
   int* err = p.err_word;
 
   if (threadIdx.x == 0) {
@@ -364,24 +301,29 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
         if (unit_off(p, mt, only_shifted)) continue;
         const CUtensorMap* mm = maps + (size_t)un.t * NMAPS + (MN_A ? MAP_MQ : MAP_MP);
         const CUtensorMap* mb = maps + (size_t)un.t * NMAPS + (MN_A ? MAP_PS : MAP_QS);
-        for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
+        for (int kb = un.kb0; kb < un.kb1 && ok; kb += kps) {
+          const int nk = min(kps, un.kb1 - kb);  // k-blocks of this stage
           const int sb = ib % B_STAGES;
           ok = mbar_wait(&sm.empty_b[sb], ((ib / B_STAGES) & 1) ^ 1, err);
           if (!ok) break;
-          mbar_arrive_expect_tx(&sm.full_b[sb], b_bytes);
-          for (int x = 0; x < NBOX; ++x)
-            tma_load_2d(S.b(sb, b_stage) + x * (N / NBOX) * BK * 2, mb, kb * BK, x * (N / NBOX), &sm.full_b[sb]);
+          mbar_arrive_expect_tx(&sm.full_b[sb], (uint32_t)nk * b_bytes);
+          for (int h = 0; h < nk; ++h)
+            for (int x = 0; x < NBOX; ++x)
+              tma_load_2d(S.b(sb, b_stage) + h * b_tile + x * (N / NBOX) * BK * 2, mb, (kb + h) * BK,
+                          x * (N / NBOX), &sm.full_b[sb]);
           ++ib;
           for (int w = 0; w < p.W; ++w) {
             const int sa = ia % A_STAGES;
             ok = mbar_wait(&sm.empty_a[sa], ((ia / A_STAGES) & 1) ^ 1, err);
             if (!ok) break;
-            mbar_arrive_expect_tx(&sm.full_a[sa], A_BYTES);
+            // the boxes span kps k-blocks whatever nk is (rows past the matrix read as 0),
+            // so the stage always receives a_bytes
+            mbar_arrive_expect_tx(&sm.full_a[sa], a_bytes);
             if (!MN_A) {
               tma_load_3d(S.a(sa), mm, kb * BK, un.tile * BM, w, &sm.full_a[sa]);
             } else {
               tma_load_3d(S.a(sa), mm, un.tile * BM, kb * BK, w, &sm.full_a[sa]);
-              tma_load_3d(S.a(sa) + A_BYTES / 2, mm, un.tile * BM + 64, kb * BK, w, &sm.full_a[sa]);
+              tma_load_3d(S.a(sa) + a_bytes / 2, mm, un.tile * BM + 64, kb * BK, w, &sm.full_a[sa]);
             }
             ++ia;
           }
@@ -405,43 +347,47 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
         const int nsteps = (un.kb1 - un.kb0) * p.W;
         int step = 0, acc = 0;
         uint32_t d_tmem = tmem_base, accum = 0;
-        for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
+        for (int kb = un.kb0; kb < un.kb1 && ok; kb += kps) {
+          const int nk = min(kps, un.kb1 - kb);
           const int sb = ib % B_STAGES;
           ok = mbar_wait(&sm.full_b[sb], (ib / B_STAGES) & 1, err);
           if (!ok) break;
           tc_fence_after();
           const uint32_t b_addr = smem_u32(S.b(sb, b_stage));
-          for (int w = 0; w < p.W; ++w) {
-            if (step % seg == 0) {  // open an accumulator segment
-              acc = (int)(ju % NACC);
-              ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
-              if (!ok) break;
-              tc_fence_after();
-              d_tmem = tmem_base + (uint32_t)acc * kAccCols;
-              accum = 0;
-            }
+          for (int w = 0; w < p.W && ok; ++w) {
             const int sa = ia % A_STAGES;
             ok = mbar_wait(&sm.full_a[sa], (ia / A_STAGES) & 1, err);
             if (!ok) break;
             tc_fence_after();
             const uint32_t a_addr = smem_u32(S.a(sa));
+            for (int h = 0; h < nk; ++h) {  // one step per k-block of the stage
+              if (step % seg == 0) {  // open an accumulator segment
+                acc = (int)(ju % NACC);
+                ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
+                if (!ok) break;
+                tc_fence_after();
+                d_tmem = tmem_base + (uint32_t)acc * kAccCols;
+                accum = 0;
+              }
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              const uint64_t adesc = MN_A ? smem_desc(a_addr + k * 2048, A_BYTES / 2, 1024)
-                                          : smem_desc(a_addr + k * 32, 16, 1024);
+              for (int k = 0; k < BK / 16; ++k) {
+                // MN-major A: 64 x (64 kps)-row boxes, k-block h at h * 64 rows of 128 bytes
+                const uint64_t adesc = MN_A ? smem_desc(a_addr + h * 8192 + k * 2048, a_bytes / 2, 1024)
+                                            : smem_desc(a_addr + k * 32, 16, 1024);
 #pragma unroll
-              for (int tm = 0; tm < TERMS; ++tm) {  // B rows [tm rp, (tm + 1) rp): term tm
-                umma_f16(d_tmem, adesc, smem_desc(b_addr + tm * rp * 128 + k * 32, 16, 1024), idesc,
-                         accum);
-                accum = 1;
+                for (int tm = 0; tm < TERMS; ++tm) {  // B rows [tm rp, (tm + 1) rp): term tm
+                  umma_f16(d_tmem, adesc, smem_desc(b_addr + h * b_tile + tm * rp * 128 + k * 32, 16, 1024),
+                           idesc, accum);
+                  accum = 1;
+                }
+              }
+              if (++step % seg == 0 || step == nsteps) {  // close the segment
+                umma_commit(&sm.acc_full[acc]);
+                ++ju;
               }
             }
             umma_commit(&sm.empty_a[sa]);
             ++ia;
-            if (++step % seg == 0 || step == nsteps) {  // close the segment
-              umma_commit(&sm.acc_full[acc]);
-              ++ju;
-            }
           }
           umma_commit(&sm.empty_b[sb]);
           ++ib;
@@ -543,7 +489,13 @@ constexpr int kIngGeWarp = 6 + kIngWarps;           // the G/E TMA warp, after t
 constexpr int kIngThreads = 32 * (kIngGeWarp + 1);
 constexpr int kIngRowsPerPass = 4 * kIngWarps;      // tile rows the ingest warps cover at once
 static_assert(128 % kIngRowsPerPass == 0, "ingest rows");
-constexpr int GE_BYTES = 2 * A_BYTES;  // one staged G tile + one E tile
+// A G/E stage holds `kps` (1 or 2) consecutive k-blocks of one worker's G and E: G boxes
+// first, then E boxes, each a 128 x 64 tile in the 128-byte swizzle. Two k-blocks put 256
+// contiguous bytes of every row in flight at once; a stream of 128-byte row pieces reads
+// HBM markedly slower (measured on GB300: 4.4 against 6.1 TB/s for a pure TMA read of the
+// same bytes).
+constexpr int kMaxKps = 2;
+__host__ __device__ constexpr int ge_bytes(int kps) { return 2 * kps * A_BYTES; }
 constexpr int kMaxGeStages = 4;
 struct IngBars {
   uint64_t full_a[kMaxAStages], empty_a[kMaxAStages];
@@ -553,39 +505,42 @@ struct IngBars {
   uint32_t tmem;
 };
 
-// Walk the (unit, worker, k-block) tile sequence of this CTA. The k-blocks of one worker
-// come back to back: a 128-byte tile row of G or E that starts off a 128-byte line (any
-// n * 2 not a multiple of 128) shares its second line with the next k-block's row, which
-// then still finds it in L2.
-struct TileIter {
-  int u, kb, w;
+// Walk the (unit, worker, stage) sequence of this CTA, a stage being kps consecutive
+// k-blocks of the unit (fewer at the unit's end). The stages of one worker come back to
+// back: a row piece that starts off a 128-byte line (any n * 2 not a multiple of 128)
+// shares its last line with the next stage's piece, which then still finds it in L2.
+struct StageIter {
+  int u, kb, nk, w;
   bool valid;
   Unit un;
-  __device__ void start(const Unit* units, int nunits) {
+  __device__ void set_nk(int kps) { nk = min(kps, un.kb1 - kb); }
+  __device__ void start(const Unit* units, int nunits, int kps) {
     u = blockIdx.x; w = 0;
     valid = u < nunits;
-    if (valid) { un = units[u]; kb = un.kb0; }
+    if (valid) { un = units[u]; kb = un.kb0; set_nk(kps); }
   }
-  __device__ void next(const Unit* units, int nunits, int W) {
-    if (++kb < un.kb1) return;
+  __device__ void next(const Unit* units, int nunits, int W, int kps) {
+    kb += nk;
+    if (kb < un.kb1) { set_nk(kps); return; }
     kb = un.kb0;
-    if (++w < W) return;
+    if (++w < W) { set_nk(kps); return; }
     w = 0;
     u += gridDim.x;
     valid = u < nunits;
-    if (valid) { un = units[u]; kb = un.kb0; }
+    if (valid) { un = units[u]; kb = un.kb0; set_nk(kps); }
   }
 };
 
 template <typename TE>
 __global__ void __launch_bounds__(kIngThreads, 1)
 k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
-           int a_stages, int ge_stages, uint32_t b_stage, int seg) {
+           int a_stages, int ge_stages, int kps, uint32_t b_stage, int seg) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* a0 = base;
   uint8_t* b0 = a0 + (size_t)a_stages * A_BYTES;
   uint8_t* ge0 = b0 + (size_t)B_STAGES * b_stage;
+  const int GE_BYTES = ge_bytes(kps);
   IngBars& sm = *reinterpret_cast<IngBars*>(ge0 + (size_t)ge_stages * GE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr bool BF16 = std::is_same<TE, __nv_bfloat16>::value;
@@ -644,8 +599,8 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
     // ------------------------------------------------------------ TMA: G/E tiles
     if (lane == 0) {
       const CUtensorMap* gem = static_cast<const CUtensorMap*>(p.tab.ge_maps);
-      TileIter ti;
-      ti.start(units, nunits);
+      StageIter ti;
+      ti.start(units, nunits, kps);
       uint32_t ig = 0;
       bool ok = true;
       while (ti.valid && ok) {
@@ -653,12 +608,14 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
         const int s = ig % ge_stages;
         ok = mbar_wait(&sm.empty_ge[s], ((ig / ge_stages) & 1) ^ 1, err);
         if (!ok) break;
-        mbar_arrive_expect_tx(&sm.full_ge[s], GE_BYTES);
+        mbar_arrive_expect_tx(&sm.full_ge[s], (uint32_t)(2 * ti.nk * A_BYTES));
         uint8_t* st = ge0 + (size_t)s * GE_BYTES;
-        tma_load_2d(st, gem + 2 * slot, ti.kb * BK, ti.un.tile * BM, &sm.full_ge[s]);
-        tma_load_2d(st + A_BYTES, gem + 2 * slot + 1, ti.kb * BK, ti.un.tile * BM, &sm.full_ge[s]);
+        for (int h = 0; h < ti.nk; ++h)  // the G boxes of the stage's k-blocks, side by side
+          tma_load_2d(st + h * A_BYTES, gem + 2 * slot, (ti.kb + h) * BK, ti.un.tile * BM, &sm.full_ge[s]);
+        for (int h = 0; h < ti.nk; ++h)  // then the E boxes
+          tma_load_2d(st + (kps + h) * A_BYTES, gem + 2 * slot + 1, (ti.kb + h) * BK, ti.un.tile * BM, &sm.full_ge[s]);
         ++ig;
-        ti.next(units, nunits, p.W);
+        ti.next(units, nunits, p.W, kps);
       }
       for (uint32_t k = (ig > (uint32_t)ge_stages ? ig - ge_stages : 0); k < ig; ++k)
         mbar_drain(&sm.full_ge[k % ge_stages], (k / ge_stages) & 1, err, 1u << 20);
@@ -771,64 +728,87 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
     const int it = threadIdx.x - 6 * 32;          // 0 .. 32 kIngWarps - 1
     const int cq = it & 7;                        // 16-byte chunk within the 128-byte row
     const int rq = it >> 3;                       // first row; rows rq + kIngRowsPerPass k
-    TileIter ti;
-    ti.start(units, nunits);
+    StageIter ti;
+    ti.start(units, nunits, kps);
     uint32_t ia = 0, ig = 0;
     bool ok = true;
     while (ti.valid && ok) {
       const MatMeta& mt = p.meta[ti.un.t];
-      const int sa = ia % a_stages, sg = ig % ge_stages;
-      ok = mbar_wait(&sm.empty_a[sa], ((ia / a_stages) & 1) ^ 1, err);
-      if (ok) ok = mbar_wait(&sm.full_ge[sg], (ig / ge_stages) & 1, err);
+      const int sg = ig % ge_stages;
+      ok = mbar_wait(&sm.full_ge[sg], (ig / ge_stages) & 1, err);
       if (!ok) break;
-      uint8_t* tile = a0 + (size_t)sa * A_BYTES;
-      const uint8_t* gs = ge0 + (size_t)sg * GE_BYTES;
+      const uint8_t* gstage = ge0 + (size_t)sg * GE_BYTES;
       const float inv_s = p.tab.inv_scale[mt.b];
-      // fp16 with a power-of-two scale: x = g / s keeps g's 11-bit significand, so one
-      // round-to-nearest fp32 add followed by the rounding to fp16 already gives
-      // round_E(x + E) (the fp32 sum is exact unless one term is below 2^-12 of the other,
-      // and then it is below half an ulp of the result; checked by brute force over
-      // every fp16 pattern, including ties). Other cases take the round-to-odd sum.
-      const bool rn_sum = !BF16 && (__float_as_uint(inv_s) & 0x7fffffu) == 0u;
+      // fp16 with a power-of-two 1/s in [2^-24, 1]: 1/s is exact in fp16 (a subnormal at
+      // the low end) and g / s cannot overflow. One fp16 FMA then gives M = round_E(g / s + E)
+      // with a single rounding of the exact value (IEEE fused multiply-add, subnormals
+      // kept), two entries per instruction. An entry is nonfinite exactly when g's
+      // exponent bits are all ones, and a zeroed entry gives M = E. Other scales and bf16
+      // take the fp32 path with the round-to-odd sum.
+      const bool h2_path = !BF16 && (__float_as_uint(inv_s) & 0x7fffffu) == 0u && inv_s <= 1.0f &&
+                           inv_s >= 0x1p-24f;
+      const __half2 inv2 = __float2half2_rn(inv_s);
       TE* mo = static_cast<TE*>(mt.mscr) + (size_t)ti.w * mt.m * mt.n;
-      const int64_t col = (int64_t)ti.kb * BK + cq * 8;
       int cnt = 0;
       unsigned mmax = 0u;
+      for (int h = 0; h < ti.nk && ok; ++h) {  // the stage's k-blocks, one A tile each
+        const int sa = ia % a_stages;
+        ok = mbar_wait(&sm.empty_a[sa], ((ia / a_stages) & 1) ^ 1, err);
+        if (!ok) break;
+        uint8_t* tile = a0 + (size_t)sa * A_BYTES;
+        const uint8_t* gs = gstage + h * A_BYTES;           // G box of k-block kb + h
+        const uint8_t* es = gstage + (kps + h) * A_BYTES;   // E box of k-block kb + h
+        const int64_t col = (int64_t)(ti.kb + h) * BK + cq * 8;
 #pragma unroll
-      for (int k = 0; k < 128 / kIngRowsPerPass; ++k) {
-        const int rl = rq + kIngRowsPerPass * k;
-        const int64_t row = (int64_t)ti.un.tile * BM + rl;
-        uint4 mv = make_uint4(0u, 0u, 0u, 0u);
-        if (row < mt.m && col < mt.n) {
-          const int so = rl * 128 + ((cq ^ (rl & 7)) << 4);  // 128-byte swizzle of the staged tiles
-          const uint4 gv = *reinterpret_cast<const uint4*>(gs + so);
-          const uint4 ev = *reinterpret_cast<const uint4*>(gs + A_BYTES + so);
-          const TE* gx = reinterpret_cast<const TE*>(&gv);
-          const TE* ex = reinterpret_cast<const TE*>(&ev);
-          TE* mx = reinterpret_cast<TE*>(&mv);
-          if (rn_sum) {
+        for (int k = 0; k < 128 / kIngRowsPerPass; ++k) {
+          const int rl = rq + kIngRowsPerPass * k;
+          const int64_t row = (int64_t)ti.un.tile * BM + rl;
+          uint4 mv = make_uint4(0u, 0u, 0u, 0u);
+          if (row < mt.m && col < mt.n) {
+            const int so = rl * 128 + ((cq ^ (rl & 7)) << 4);  // 128-byte swizzle of the staged tiles
+            const uint4 gv = *reinterpret_cast<const uint4*>(gs + so);
+            const uint4 ev = *reinterpret_cast<const uint4*>(es + so);
+            const TE* gx = reinterpret_cast<const TE*>(&gv);
+            const TE* ex = reinterpret_cast<const TE*>(&ev);
+            TE* mx = reinterpret_cast<TE*>(&mv);
+            if (h2_path) {
+              const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, ew[4] = {ev.x, ev.y, ev.z, ev.w};
+              uint32_t mw[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float x = to_f(gx[i]) * inv_s;
-              const bool bad = !isfinite(x);
-              cnt += bad;
-              mx[i] = from_f<TE>(__fadd_rn(bad ? 0.0f : x, to_f(ex[i])));
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t xe = gw[i] & 0x7C007C00u;  // exponent fields of the two entries
+                const uint32_t bad = ((xe & 0xFFFFu) == 0x7C00u ? 0x0000FFFFu : 0u) |
+                                     ((xe >> 16) == 0x7C00u ? 0xFFFF0000u : 0u);
+                cnt += __popc(bad) >> 4;
+                __half2 gh, eh;
+                memcpy(&gh, &gw[i], 4);
+                memcpy(&eh, &ew[i], 4);
+                const __half2 r = __hfma2(gh, inv2, eh);
+                uint32_t rw;
+                memcpy(&rw, &r, 4);
+                mw[i] = (rw & ~bad) | (ew[i] & bad);
+              }
+              mv = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float x = to_f(gx[i]) * inv_s;
+                const bool bad = !isfinite(x);
+                cnt += bad;
+                mx[i] = add_to<TE>(bad ? 0.0f : x, to_f(ex[i]));
+                if (BF16) mmax = max(mmax, __float_as_uint(fabsf(to_f(mx[i]))));
+              }
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float x = to_f(gx[i]) * inv_s;
-              const bool bad = !isfinite(x);
-              cnt += bad;
-              mx[i] = add_to<TE>(bad ? 0.0f : x, to_f(ex[i]));
-              if (BF16) mmax = max(mmax, __float_as_uint(fabsf(to_f(mx[i]))));
-            }
+            __stcg(reinterpret_cast<uint4*>(mo + row * mt.n + col), mv);
           }
-          __stcg(reinterpret_cast<uint4*>(mo + row * mt.n + col), mv);
+          *reinterpret_cast<uint4*>(tile + rl * 128 + ((cq ^ (rl & 7)) << 4)) = mv;
         }
-        *reinterpret_cast<uint4*>(tile + rl * 128 + ((cq ^ (rl & 7)) << 4)) = mv;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.full_a[sa]);
+        ++ia;
       }
-      fence_proxy_async_smem();
+      if (!ok) break;
       cnt = __reduce_add_sync(0xffffffffu, cnt);
       if (BF16) mmax = __reduce_max_sync(0xffffffffu, mmax);
       if (lane == 0 && cnt)
@@ -837,12 +817,9 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
       if (BF16 && lane == 0 && mmax)  // only the bf16 subnormal rescale reads max|M|
         atomicMax(reinterpret_cast<unsigned*>(mt.scal) + SC_MAXM, mmax);
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sm.full_a[sa]);
-        mbar_arrive(&sm.empty_ge[sg]);
-      }
-      ++ia; ++ig;
-      ti.next(units, nunits, p.W);
+      if (lane == 0) mbar_arrive(&sm.empty_ge[sg]);
+      ++ig;
+      ti.next(units, nunits, p.W, kps);
     }
   }
   tc_fence_before();
@@ -852,18 +829,28 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
 }
 
 // Stage counts of the fused kernel: A stages for the MMA, G/E staging stages.
-void ingest_stages(int edt, uint32_t b_stage, int* a_st, int* ge_st, size_t* smem) {
-  const size_t budget = 227 * 1024 - 1024 - sizeof(IngBars) - (size_t)B_STAGES * b_stage;
-  int a = edt == DT_BF16 ? 2 : 3;
-  int ge = (int)std::min<size_t>(kMaxGeStages, (budget - (size_t)a * A_BYTES) / GE_BYTES);
+// Two k-blocks per G/E stage when two such stages fit next to two A stages; otherwise
+// (the bf16 case, whose three split terms make the B stages larger) one k-block per stage.
+void ingest_stages(int edt, uint32_t b_stage, int* a_st, int* ge_st, int* kps, size_t* smem) {
+  const size_t budget = kDynSmemCap - 1024 - sizeof(IngBars) - (size_t)B_STAGES * b_stage;
+  int a = 2, k = kMaxKps;
+  int ge = (int)std::min<size_t>(kMaxGeStages, (budget - (size_t)a * A_BYTES) / ge_bytes(k));
+  if (ge < 2) {
+    k = 1;
+    a = edt == DT_BF16 ? 2 : 3;
+    ge = (int)std::min<size_t>(kMaxGeStages, (budget - (size_t)a * A_BYTES) / ge_bytes(k));
+  }
   *a_st = a;
   *ge_st = ge;
-  *smem = 1024 + (size_t)a * A_BYTES + (size_t)B_STAGES * b_stage + (size_t)ge * GE_BYTES + sizeof(IngBars);
+  *kps = k;
+  *smem = 1024 + (size_t)a * A_BYTES + (size_t)B_STAGES * b_stage + (size_t)ge * ge_bytes(k) + sizeof(IngBars);
 }
 
 // ---------------------------------------------------------------- decompression kernel
 constexpr int DEC_STAGES = 2;   // P^ / Q operand stages of the G^ MMA
-constexpr int DEC_MSTAGES = 4;  // M_w tile ring (E is formed in place and stored from it)
+constexpr int DEC_MSTAGES = 4;  // M_w tile ring (E is formed in place and stored from it;
+                                // G^ goes out through the same ring, 64 fp32 columns a stage)
+constexpr int DEC_MSTAGE_BYTES = 2 * A_BYTES;
 constexpr int DEC_THREADS = 352;
 struct DecSmem {
   alignas(1024) uint8_t a[DEC_STAGES][A_BYTES];          // P^ split tiles, 128 x 64
@@ -978,38 +965,60 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
     // ------------------------------------------------------------ TMA: M_w in, E_w out
     if (lane == 0) {
       const CUtensorMap* gem = static_cast<const CUtensorMap*>(p.tab.ge_maps);
-      // tiles held by the stages: (matrix, worker, row0, col0)
+      const CUtensorMap* ghm = gem + 2 * (size_t)p.B * p.J * p.W;  // G^ maps, one per matrix
+      // What each stage holds: (matrix, worker, row0, col0, second 64-column box) for an
+      // E tile; worker -1 - g for half g (64 columns, fp32) of the unit's G^ tile.
       int st_t[DEC_MSTAGES] = {}, st_w[DEC_MSTAGES] = {}, st_r[DEC_MSTAGES] = {}, st_c[DEC_MSTAGES] = {},
           st_two[DEC_MSTAGES] = {};
+      int64_t st_n[DEC_MSTAGES] = {};
       uint32_t i = 0;
       bool ok = true;
       auto store_tile = [&](uint32_t j) -> bool {
         const int s = (int)(j % DEC_MSTAGES);
         if (!mbar_wait(&sm.mdone[s], (j / DEC_MSTAGES) & 1, err)) return false;
-        const CUtensorMap* em = gem + 2 * ((size_t)st_t[s] * p.W + st_w[s]) + 1;
-        tma_store_2d(em, sm.mt[s], st_c[s], st_r[s]);
-        if (st_two[s]) tma_store_2d(em, sm.mt[s] + A_BYTES, st_c[s] + 64, st_r[s]);
+        if (st_w[s] >= 0) {
+          const CUtensorMap* em = gem + 2 * ((size_t)st_t[s] * p.W + st_w[s]) + 1;
+          tma_store_2d(em, sm.mt[s], st_c[s], st_r[s]);
+          if (st_two[s]) tma_store_2d(em, sm.mt[s] + A_BYTES, st_c[s] + 64, st_r[s]);
+        } else {  // G^: two boxes of 32 fp32 columns; none starts past the matrix edge
+          const CUtensorMap* gm = ghm + st_t[s];
+          for (int b = 0; b < 2; ++b)
+            if (st_c[s] + 32 * b < st_n[s]) tma_store_2d(gm, sm.mt[s] + b * (DEC_MSTAGE_BYTES / 2), st_c[s] + 32 * b, st_r[s]);
+        }
         bulk_commit();
+        return true;
+      };
+      // claim stage i % DEC_MSTAGES: store what it held and wait until the store has read it
+      auto claim = [&]() -> bool {
+        if (i < DEC_MSTAGES) return true;
+        if (!store_tile(i - DEC_MSTAGES)) return false;
+        bulk_wait_read_all();
         return true;
       };
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const Unit un = units[u];
         const MatMeta& mt = p.meta[un.t];
-        if (p.skip[mt.b]) continue;
-        const CUtensorMap* mm = maps + (size_t)un.t * NMAPS + MAP_MP;
         const int row0 = un.tile * BM, col0 = un.kb0 * DEC_NT;
-        const int two = (int64_t)col0 + 64 < mt.n ? 1 : 0;
-        for (int w = 0; w < p.W && ok; ++w) {
-          const int s = (int)(i % DEC_MSTAGES);
-          if (i >= DEC_MSTAGES) {  // the stage's previous tile: store its E, then reuse
-            ok = store_tile(i - DEC_MSTAGES);
+        if (!p.skip[mt.b]) {
+          const CUtensorMap* mm = maps + (size_t)un.t * NMAPS + MAP_MP;
+          const int two = (int64_t)col0 + 64 < mt.n ? 1 : 0;
+          for (int w = 0; w < p.W && ok; ++w) {
+            const int s = (int)(i % DEC_MSTAGES);
+            ok = claim();
             if (!ok) break;
-            bulk_wait_read_all();
+            st_t[s] = un.t; st_w[s] = w; st_r[s] = row0; st_c[s] = col0; st_two[s] = two;
+            mbar_arrive_expect_tx(&sm.mfull[s], (uint32_t)(1 + two) * A_BYTES);
+            tma_load_3d(sm.mt[s], mm, col0, row0, w, &sm.mfull[s]);
+            if (two) tma_load_3d(sm.mt[s] + A_BYTES, mm, col0 + 64, row0, w, &sm.mfull[s]);
+            ++i;
           }
-          st_t[s] = un.t; st_w[s] = w; st_r[s] = row0; st_c[s] = col0; st_two[s] = two;
-          mbar_arrive_expect_tx(&sm.mfull[s], (uint32_t)(1 + two) * A_BYTES);
-          tma_load_3d(sm.mt[s], mm, col0, row0, w, &sm.mfull[s]);
-          if (two) tma_load_3d(sm.mt[s] + A_BYTES, mm, col0 + 64, row0, w, &sm.mfull[s]);
+        }
+        for (int g = 0; g < 2 && ok; ++g) {  // the G^ tile, 64 columns per stage (0 if skipped)
+          const int s = (int)(i % DEC_MSTAGES);
+          ok = claim();
+          if (!ok) break;
+          st_t[s] = un.t; st_w[s] = -1 - g; st_r[s] = row0; st_c[s] = col0 + 64 * g; st_n[s] = mt.n;
+          mbar_arrive(&sm.mfull[s]);  // the stage is free for the epilogue to fill
           ++i;
         }
       }
@@ -1066,19 +1075,11 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
 #pragma unroll
         for (int c = 0; c < 64; ++c) gv[c] = 0.f;
       }
-      // G^ (this row's 64 columns; n is a multiple of 8)
-      if (row < m) {
-        float* gp = p.tab.ghat[un.t] + row * n + colh;
-#pragma unroll
-        for (int c = 0; c < 64; c += 4)
-          if (colh + c < n) *reinterpret_cast<float4*>(gp + c) = make_float4(gv[c], gv[c + 1], gv[c + 2], gv[c + 3]);
-      }
-      if (skipped) continue;
       TE* mbase = static_cast<TE*>(mt.mscr);
       // a rescaled bf16 M scratch holds M * 2^sh: undo it exactly, and restore M
       const int msh = reinterpret_cast<const int*>(mt.scal)[SC_MSHIFT];
       const float munscale = __uint_as_float((uint32_t)(127 - msh) << 23);
-      for (int w = 0; w < p.W; ++w) {
+      for (int w = 0; w < p.W && !skipped; ++w) {
         const int s = (int)(i % DEC_MSTAGES);
         ok = mbar_wait(&sm.mfull[s], (i / DEC_MSTAGES) & 1, err);
         if (!ok) break;
@@ -1105,6 +1106,28 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
         if (lane == 0) mbar_arrive(&sm.mdone[s]);
         ++i;
       }
+      if (!ok) break;
+      // G^: half g of the tile (this warp's 64 columns when half == g) goes into a stage in
+      // the 128-byte-swizzled layout of two 32-column fp32 boxes, which the TMA warp stores.
+      // The other half's warps only arrive.
+      for (int g = 0; g < 2; ++g) {
+        const int s = (int)(i % DEC_MSTAGES);
+        if (half == g) {
+          ok = mbar_wait(&sm.mfull[s], (i / DEC_MSTAGES) & 1, err);
+          if (!ok) break;
+          uint8_t* st = sm.mt[s] + row_in_tile * 128;
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<float4*>(st + b * (DEC_MSTAGE_BYTES / 2) + ((j ^ sw) << 4)) =
+                  make_float4(gv[32 * b + 4 * j], gv[32 * b + 4 * j + 1], gv[32 * b + 4 * j + 2], gv[32 * b + 4 * j + 3]);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.mdone[s]);
+        ++i;
+      }
     }
   }
   tc_fence_before();
@@ -1127,14 +1150,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_map(CUtensorMap* out, void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-              const uint32_t* box, bool swizzle = true) {
+              const uint32_t* box, bool swizzle = true,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_UINT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[3], s[2];
   cuuint32_t b[3], es[3] = {1, 1, 1};
   for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
   for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
-  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, (cuuint32_t)rank, base, d, s, b, es,
+  CUresult r = fn(out, dtype, (cuuint32_t)rank, base, d, s, b, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1149,17 +1173,22 @@ int num_sms() {
 }
 
 // B stage bytes and the number of A stages that fit next to two B stages.
-uint32_t gemm_b_stage(int edt, int rp) {
+// B stage bytes (kps k-blocks' split tiles, each rounded up to 1 KB), the number of A stages
+// (kps k-blocks each) that fit next to two B stages, and the kernel's shared memory.
+uint32_t gemm_b_stage(int edt, int rp, int kps = 1) {
   const int rows = (edt == DT_BF16 ? 3 : 2) * rp;
-  return (uint32_t)((rows * BK * 2 + 1023) / 1024 * 1024);
+  return (uint32_t)kps * (uint32_t)((rows * BK * 2 + 1023) / 1024 * 1024);
 }
-int gemm_a_stages(uint32_t b_stage) {
-  const size_t budget = 227 * 1024 - 1024 - sizeof(GemmBars) - (size_t)B_STAGES * b_stage;
-  return (int)std::min<size_t>(kMaxAStages, budget / A_BYTES);
+int gemm_a_stages(uint32_t b_stage, int kps = 1) {
+  const size_t budget = kDynSmemCap - 1024 - sizeof(GemmBars) - (size_t)B_STAGES * b_stage;
+  return (int)std::min<size_t>(kMaxAStages, budget / ((size_t)kps * A_BYTES));
 }
-size_t gemm_smem(uint32_t b_stage, int a_stages) {
-  return 1024 + (size_t)a_stages * A_BYTES + (size_t)B_STAGES * b_stage + sizeof(GemmBars);
+size_t gemm_smem(uint32_t b_stage, int a_stages, int kps = 1) {
+  return 1024 + (size_t)a_stages * kps * A_BYTES + (size_t)B_STAGES * b_stage + sizeof(GemmBars);
 }
+// The Q GEMM stages two k-blocks when three such A stages still fit (fp16 up to r = 128);
+// bf16's three split terms make the paired B stages too large, and it stages one.
+int qgemm_kps(int edt, int rp) { return gemm_a_stages(gemm_b_stage(edt, rp, 2), 2) >= 3 ? 2 : 1; }
 size_t dec_smem() { return sizeof(DecSmem) + 1024; }
 
 struct TcLayout {
@@ -1229,13 +1258,24 @@ __global__ void k_rescale_tiny(Plan p) {
 
 size_t tc_ge_maps_bytes(const psgd_config* cfg) {
   if (cfg->err_dtype == PSGD_F32 || (cfg->flags & PSGD_FLAG_SIMT) || cfg->rank > kRankBlock) return 0;
-  return 2 * sizeof(CUtensorMap) * (size_t)cfg->num_blocks * cfg->mats_per_block * cfg->num_workers;
+  const size_t BJ = (size_t)cfg->num_blocks * cfg->mats_per_block;
+  return sizeof(CUtensorMap) * (2 * BJ * cfg->num_workers + BJ);
 }
 
 // TMA maps of each (matrix, worker) G and E: 2D {n, m}, 128 x 64 boxes, 128-byte swizzle
-// (the fused ingest reads G/E tiles through them; the decompression stores E tiles).
-bool tc_encode_ge_maps(const Handle& h, const void* const* grads, void* const* errs, void* out) {
+// (the fused ingest reads G/E tiles through them; the decompression stores E tiles), then
+// one per matrix for G^: fp32 {n, m}, 128 x 32 boxes, 128-byte swizzle (decompression).
+bool tc_encode_ge_maps(const Handle& h, const void* const* grads, void* const* errs, float* const* ghat,
+                       void* out) {
   CUtensorMap* maps = static_cast<CUtensorMap*>(out);
+  for (int t = 0; t < h.B * h.J; ++t) {
+    const MatMeta& mt = h.meta[t];
+    uint64_t d[2] = {(uint64_t)mt.n, (uint64_t)mt.m}, st[1] = {(uint64_t)mt.n * 4};
+    uint32_t box[2] = {32, 128};
+    if (!make_map(&maps[(size_t)2 * h.B * h.J * h.W + t], ghat[t], 2, d, st, box, true,
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return false;
+  }
   for (int t = 0; t < h.B * h.J; ++t) {
     const MatMeta& mt = h.meta[t];
     uint64_t d[2] = {(uint64_t)mt.n, (uint64_t)mt.m}, st[1] = {(uint64_t)mt.n * 2};
@@ -1257,7 +1297,7 @@ cudaError_t launch_rescale_tiny(const Handle& h, const Plan& p, cudaStream_t s) 
   const uint32_t bst = gemm_b_stage(h.edt, p.rp);
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
-  launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 1, kGemmSegSteps);
+  launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 1, kGemmSegSteps, 1);
   h.launches += 1;
   return cudaGetLastError();
 }
@@ -1285,6 +1325,7 @@ cudaError_t tc_plan(Handle& h, char* ws_tc, cudaStream_t s) {
   h.tc_plan = tp;
   const int B = h.B, J = h.J, W = h.W, rp = h.rp, kp = kpad_of(rp);
   tp->kp = kp;
+  tp->qkps = qgemm_kps(h.edt, rp);
   tp->d_maps = reinterpret_cast<CUtensorMap*>(ws_tc + L.maps);
   tp->d_punits = reinterpret_cast<Unit*>(ws_tc + L.punits);
   tp->d_qunits = reinterpret_cast<Unit*>(ws_tc + L.qunits);
@@ -1307,7 +1348,7 @@ cudaError_t tc_plan(Handle& h, char* ws_tc, cudaStream_t s) {
     {  // M_w as a 3D tensor {n, m, W}
       uint64_t d[3] = {(uint64_t)n, (uint64_t)m, (uint64_t)W};
       uint64_t st[2] = {(uint64_t)n * 2, (uint64_t)m * n * 2};
-      uint32_t bp[3] = {64, 128, 1}, bq[3] = {64, 64, 1};
+      uint32_t bp[3] = {64, 128, 1}, bq[3] = {64, (uint32_t)(64 * tp->qkps), 1};
       ok &= make_map(&tm[MAP_MP], mt.mscr, 3, d, st, bp);
       ok &= make_map(&tm[MAP_MQ], mt.mscr, 3, d, st, bq);
     }
@@ -1356,7 +1397,9 @@ cudaError_t tc_plan(Handle& h, char* ws_tc, cudaStream_t s) {
   if (e == cudaSuccess) e = cudaMemcpyAsync(tp->d_dunits, du.data(), sizeof(Unit) * du.size(), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return e;
-  const int gs = 227 * 1024, ds = (int)dec_smem();
+  // The dynamic-size cap leaves room for the kernels' few bytes of static shared memory
+  // (the abort flag): static + dynamic must stay within the 227 KB a CTA may use.
+  const int gs = kDynSmemCap, ds = (int)dec_smem();
   e = cudaFuncSetAttribute(k_gemm<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
@@ -1400,8 +1443,8 @@ cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
   const int seg = kGemmSegSteps;
-  if (h.edt == DT_BF16) launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg);
-  else launch_pdl(k_gemm<false, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg);
+  if (h.edt == DT_BF16) launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg, 1);
+  else launch_pdl(k_gemm<false, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg, 1);
   int64_t maxe = 0;
   for (const MatMeta& mt : h.meta) maxe = std::max<int64_t>(maxe, mt.m * p.rp);
   launch_pdl(k_preduce, dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), dim3(256), 0, s, p, PCHUNK_KB);
@@ -1413,12 +1456,12 @@ cudaError_t launch_ingest_p(const Handle& h, const Plan& p, cudaStream_t s) {
   const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
   const int grid = std::min(tp->grid, tp->np);
   const uint32_t bst = gemm_b_stage(h.edt, p.rp);
-  int ast, gst;
+  int ast, gst, kps;
   size_t sm;
-  ingest_stages(h.edt, bst, &ast, &gst, &sm);
+  ingest_stages(h.edt, bst, &ast, &gst, &kps, &sm);
   const int seg = kIngSegSteps;
-  if (h.edt == DT_BF16) k_ingest_p<__nv_bfloat16><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst, seg);
-  else k_ingest_p<__half><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, bst, seg);
+  if (h.edt == DT_BF16) k_ingest_p<__nv_bfloat16><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, kps, bst, seg);
+  else k_ingest_p<__half><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, kps, bst, seg);
   h.launches += 1;
   return cudaGetLastError();
 }
@@ -1431,19 +1474,26 @@ cudaError_t launch_preduce(const Handle& h, const Plan& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
+int tc_kpad(const Handle& h) { return static_cast<const TcPlan*>(h.tc_plan)->kp; }
+int tc_pchunk_kb() { return PCHUNK_KB; }
+
+cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s, bool psplit_done) {
   const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
-  dim3 g((unsigned)h.max_mtiles * 4, p.B * p.J);
-  if (h.edt == DT_BF16) launch_pdl(k_psplit<__nv_bfloat16>, dim3(g), dim3(256), 0, s, p, tp->kp);
-  else launch_pdl(k_psplit<__half>, dim3(g), dim3(256), 0, s, p, tp->kp);
+  if (!psplit_done) {
+    dim3 g((unsigned)h.max_mtiles * 4, p.B * p.J);
+    if (h.edt == DT_BF16) launch_pdl(k_psplit<__nv_bfloat16>, dim3(g), dim3(256), 0, s, p, tp->kp);
+    else launch_pdl(k_psplit<__half>, dim3(g), dim3(256), 0, s, p, tp->kp);
+    h.launches += 1;
+  }
   const int grid = std::min(tp->grid, tp->nq);
-  const uint32_t bst = gemm_b_stage(h.edt, p.rp);
-  const int ast = gemm_a_stages(bst);
-  const size_t sm = gemm_smem(bst, ast);
+  const int kps = tp->qkps;
+  const uint32_t bst = gemm_b_stage(h.edt, p.rp, kps);
+  const int ast = gemm_a_stages(bst, kps);
+  const size_t sm = gemm_smem(bst, ast, kps);
   const int seg = kGemmSegSteps;
-  if (h.edt == DT_BF16) launch_pdl(k_gemm<true, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg);
-  else launch_pdl(k_gemm<true, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg);
-  h.launches += 2;
+  if (h.edt == DT_BF16) launch_pdl(k_gemm<true, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg, kps);
+  else launch_pdl(k_gemm<true, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg, kps);
+  h.launches += 1;
   return cudaGetLastError();
 }
 

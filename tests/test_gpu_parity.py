@@ -59,6 +59,42 @@ def test_ingest_every_bit_pattern(dtype, scale):
     assert counts.sum() == 2 * (2048 if dtype == "f16" else 256)  # all-ones exponent patterns
 
 
+@pytest.mark.parametrize("dtype,scale", [("f16", 2.0 ** 10), ("f16", 1.0), ("f16", 2.0 ** 20),
+                                         ("bf16", 2.0 ** 20)])
+def test_fused_ingest_every_bit_pattern(dtype, scale):
+    """The production path (the fused ingest + P GEMM kernel, a full step): every 16-bit
+    pattern once per worker as a gradient entry, under random finite error-buffer values
+    below 2^10. M and the nonfinite counts must equal the oracle's bit for bit."""
+    psgd = _psgd()
+    tdt = synth.TORCH_DTYPE[dtype]
+    rng = np.random.default_rng(13)
+    W, m, n, r = 2, 256, 256, 16
+    ps = psgd.PowerSGD([(m, n)], 1, W, r, dtype)
+    assert ps.engine == "tcgen05"
+    grads, errs, gin, ein = [], [], [], []
+    top = 0x6400 if dtype == "f16" else 0x4480  # |E| < 2^10
+    for w in range(W):
+        bits = rng.permutation(1 << 16).astype(np.uint16)
+        gt = torch.from_numpy(bits.view(np.int16).reshape(m, n)).view(tdt)
+        eb = rng.integers(0, top, size=m * n).astype(np.uint16)
+        eb |= (rng.random(m * n) < 0.5).astype(np.uint16) << 15
+        et = torch.from_numpy(eb.view(np.int16).reshape(m, n)).view(tdt)
+        grads.append(gt.cuda()); errs.append(et.cuda())
+        gin.append(gt.to(torch.float64).numpy()); ein.append(et.to(torch.float64).numpy())
+    q = [[torch.from_numpy(rng.standard_normal((n, r)).astype(np.float32)).cuda()]]
+    gh = [[torch.zeros((m, n), device="cuda")]]
+    ps.step([[grads]], [[errs]], q, [scale], gh)
+    torch.cuda.synchronize()
+    counts = ps.counts.cpu().numpy()
+    for w in range(W):
+        g, mask = oracle.unscale_and_mask(gin[w], scale)
+        want_m = oracle.accumulate_error(g, ein[w], dtype)
+        got_m = f64(ps.debug_m(0, 0, w, tdt))
+        same = (got_m == want_m) | (np.isnan(got_m) & np.isnan(want_m))
+        assert same.all(), f"worker {w}: {int((~same).sum())} M entries differ"
+        assert counts[w] == int(mask.sum())
+
+
 def test_ingest_fp32_specials():
     psgd = _psgd()
     rng = np.random.default_rng(12)
