@@ -75,6 +75,10 @@ typedef struct {
                                             nothing completes, then winds down. The step's
                                             G^, E and Q are invalid, and psgd_check returns
                                             PSGD_ETIMEOUT. */
+#define PSGD_FLAG_EXCHANGE 0x10u     /* plan the data-parallel exchange points: workspace
+                                        for the P and Q exchange buffers, and the calls
+                                        psgd_step_p / psgd_step_q / psgd_step_e. Needs
+                                        unc_len == 0 and not STOP_AFTER_INGEST. */
 
 typedef struct {
   int32_t num_blocks;       /* B >= 1 resblocks */
@@ -137,6 +141,53 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes,
 
 /* Enqueue one PowerSGD step on `stream` (see the top of this file). */
 psgd_status psgd_step(psgd_handle* h, const psgd_step_args* args, void* stream);
+
+/* Data-parallel exchange points (a handle made with PSGD_FLAG_EXCHANGE).
+ *
+ * The method all-reduces the two low-rank factors between machines instead of the
+ * gradient ("Zero-Shot Text-to-Image Generation - 中文验证版", §方法适配), and every rank
+ * takes the same skip decision ("AIGC 基本功|混合精度与数值稳定性", §6.2). With R ranks
+ * (one handle each, W workers per rank; W may differ between ranks, total_workers =
+ * the sum), one step is three calls with two caller all-reduces (sum) between them:
+ *
+ *   psgd_step_p(h, args, s)      ingest, nonfinite counts, and this rank's sum
+ *                                P_r = sum_w M_w Q into psgd_exchange_p(h, b, j)
+ *                                (fp32 m x r, row-major), and the rank's per-block
+ *                                nonfinite counts into psgd_exchange_counts(h) (int64 [B]).
+ *   caller: all-reduce (sum) every exchange P buffer and the counts over the ranks.
+ *   psgd_step_q(h, args, counts, total_workers, s)
+ *                                skip_b from the summed counts, P = sum / total_workers,
+ *                                orthonormalisation, and this rank's sum Q_r = sum_w
+ *                                M_w^T P^ into psgd_exchange_q(h, b, j) (fp32 n x r).
+ *   caller: all-reduce (sum) every exchange Q buffer.
+ *   psgd_step_e(h, args, total_workers, s)
+ *                                Q state = sum / total_workers, G^ and the error update.
+ *
+ * All three calls take the same psgd_step_args as psgd_step (the same tables; the skip
+ * flags are written by psgd_step_q). Every rank must hold the same Q state at the start
+ * of a step (the previous step's all-reduced Q). Skipped blocks leave their buffers
+ * untouched in the later calls; the caller may still all-reduce them. The sums are
+ * fp32 round-to-nearest; an all-reduce that adds in another order changes the low bits
+ * of P and Q, not the method. With one rank (the buffers passed through unchanged) the
+ * three calls give bit for bit the result of psgd_step.
+ * block_counts: device int64 [B], 8-byte aligned: the per-block nonfinite counts summed
+ * over every rank (it may be the psgd_exchange_counts buffer itself, all-reduced in place).
+ * total_workers >= this handle's num_workers. Errors: PSGD_EUNSUPPORTED without the flag,
+ * PSGD_EINVAL for a bad pointer or total_workers, as for psgd_step otherwise. */
+psgd_status psgd_step_p(psgd_handle* h, const psgd_step_args* args, void* stream);
+psgd_status psgd_step_q(psgd_handle* h, const psgd_step_args* args, const int64_t* block_counts,
+                        int32_t total_workers, void* stream);
+psgd_status psgd_step_e(psgd_handle* h, const psgd_step_args* args, int32_t total_workers,
+                        void* stream);
+/* Device addresses of the exchange buffers (inside the workspace; valid while the handle
+ * lives), or NULL for a handle without PSGD_FLAG_EXCHANGE or an index out of range.
+ * The P buffers of all matrices lie back to back in (b, j) order, fp32 m_j x r each, so
+ * one all-reduce of B * sum_j m_j * r floats from psgd_exchange_p(h, 0, 0) covers them;
+ * likewise the Q buffers (B * sum_j n_j * r floats from psgd_exchange_q(h, 0, 0)).
+ * psgd_exchange_counts: int64 [B], written by psgd_step_p. */
+float* psgd_exchange_p(psgd_handle* h, int32_t b, int32_t j);
+float* psgd_exchange_q(psgd_handle* h, int32_t b, int32_t j);
+int64_t* psgd_exchange_counts(psgd_handle* h);
 
 /* Dynamic per-resblock gradient scale ("AIGC 基本功|混合精度与数值稳定性", §3.2, the
  * dynamic scaler rule, applied per resblock as "Zero-Shot Text-to-Image Generation -

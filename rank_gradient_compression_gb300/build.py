@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libpsgd.so")
-SOURCES = ["api.cu", "ingest.cu", "simt.cu", "orth.cu", "tc.cu", "static_orth.cu", "scaler.cu", "consumer.cu", "unc.cu", "orth_coop.cu"]
+SOURCES = ["api.cu", "ingest.cu", "simt.cu", "orth.cu", "tc.cu", "static_orth.cu", "scaler.cu", "consumer.cu", "unc.cu", "orth_coop.cu", "exchange.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

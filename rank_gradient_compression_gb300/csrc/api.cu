@@ -41,8 +41,8 @@ int64_t slice_rows(const psgd_config* c) {
 struct Layout {
   size_t total = 0;
   size_t meta = 0, threshold = 0, mask_off = 0, segs = 0, table = 0, err = 0, scal = 0;
-  size_t inv_dev = 0, gbar = 0;
-  std::vector<size_t> mscr, P, Xa, Xb, Phat, ostate, Qpart, Gpart, Rinv;
+  size_t inv_dev = 0, gbar = 0, noskip = 0, xcnt = 0;
+  std::vector<size_t> mscr, P, Xa, Xb, Phat, ostate, Qpart, Gpart, Rinv, xp, xq;
   size_t tc = 0;
   size_t table_bytes = 0, maps_bytes = 0;
   int64_t nseg = 0;
@@ -63,6 +63,10 @@ psgd_status validate_config(const psgd_config* c) {
   if (c->rank > kMaxRank)
     return fail(PSGD_EUNSUPPORTED, "rank above 1024 is not supported by this build");
   if (c->unc_len < 0) return fail(PSGD_EINVAL, "unc_len must be >= 0");
+  if ((c->flags & PSGD_FLAG_EXCHANGE) && c->unc_len != 0)
+    return fail(PSGD_EUNSUPPORTED, "PSGD_FLAG_EXCHANGE needs unc_len == 0 (reduce gains/biases separately)");
+  if ((c->flags & PSGD_FLAG_EXCHANGE) && (c->flags & PSGD_FLAG_STOP_AFTER_INGEST))
+    return fail(PSGD_EUNSUPPORTED, "PSGD_FLAG_EXCHANGE and PSGD_FLAG_STOP_AFTER_INGEST do not mix");
   if (!(c->skip_fraction > 0.0 && c->skip_fraction <= 1.0))
     return fail(PSGD_EINVAL, "skip_fraction must be in (0, 1]");
   const size_t es = esize(c->grad_dtype);
@@ -97,6 +101,8 @@ Layout plan_layout(const psgd_config* c) {
   L.scal = take(4 * kScalWords * (size_t)B * J);
   L.inv_dev = take(4 * (size_t)B);
   L.gbar = take(sizeof(GridBarrier));
+  L.noskip = take((size_t)B);
+  if (c->flags & PSGD_FLAG_EXCHANGE) L.xcnt = take(8 * (size_t)B);
   for (int t = 0; t < B * J; ++t) {
     const psgd_shape s = c->shapes[t % J];
     const int64_t mpad = ceil_div(s.m, 128) * 128;
@@ -111,6 +117,22 @@ Layout plan_layout(const psgd_config* c) {
     L.Qpart.push_back(take(4 * (size_t)S * s.n * rp));
     L.Gpart.push_back(take(4 * (size_t)(C + 1) * rp * rp));  // C partials + their sum
     L.Rinv.push_back(take(4 * (size_t)rp * rp));
+  }
+  if (c->flags & PSGD_FLAG_EXCHANGE) {
+    // The exchange buffers of the data-parallel calls: every matrix's P sum back to back
+    // in (b, j) order, then every Q sum, so that one all-reduce covers each.
+    size_t np = 0, nq = 0;
+    for (int t = 0; t < B * J; ++t) {
+      np += (size_t)c->shapes[t % J].m * c->rank;
+      nq += (size_t)c->shapes[t % J].n * c->rank;
+    }
+    size_t op = take(4 * np), oq = take(4 * nq);
+    for (int t = 0; t < B * J; ++t) {
+      L.xp.push_back(op);
+      L.xq.push_back(oq);
+      op += 4 * (size_t)c->shapes[t % J].m * c->rank;
+      oq += 4 * (size_t)c->shapes[t % J].n * c->rank;
+    }
   }
   L.tc = take(tc_workspace_bytes(c));
   L.total = off;
@@ -218,6 +240,8 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
   h.d_scal_all = reinterpret_cast<float*>(h.ws + L.scal);
   h.d_inv_dev = reinterpret_cast<float*>(h.ws + L.inv_dev);
   h.d_gbar = reinterpret_cast<GridBarrier*>(h.ws + L.gbar);
+  h.d_noskip = reinterpret_cast<uint8_t*>(h.ws + L.noskip);
+  if (cfg->flags & PSGD_FLAG_EXCHANGE) h.d_xcnt = reinterpret_cast<int64_t*>(h.ws + L.xcnt);
 
   h.meta.resize(BJ);
   for (int t = 0; t < BJ; ++t) {
@@ -238,6 +262,10 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
     mt.Gpart = reinterpret_cast<float*>(h.ws + L.Gpart[t]);
     mt.Rinv = reinterpret_cast<float*>(h.ws + L.Rinv[t]);
     mt.scal = h.d_scal_all + kScalWords * t;
+    if (cfg->flags & PSGD_FLAG_EXCHANGE) {
+      mt.xp = reinterpret_cast<float*>(h.ws + L.xp[t]);
+      mt.xq = reinterpret_cast<float*>(h.ws + L.xq[t]);
+    }
     h.max_mtiles = std::max(h.max_mtiles, mt.mtiles);
     h.max_S = std::max(h.max_S, mt.S);
     h.max_C = std::max(h.max_C, mt.C);
@@ -289,6 +317,7 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
   if (e == cudaSuccess) e = cudaMemcpyAsync(h.d_mask_off, moff.data(), 8 * moff.size(), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(h.d_segs, h.segs.data(), sizeof(IngestSeg) * h.segs.size(), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(h.d_err, 0, 16, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h.d_noskip, 0, (size_t)h.B, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&h.h_stage), h.table_bytes + h.maps_bytes, cudaHostAllocDefault);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.upload_ev, cudaEventDisableTiming);
@@ -314,7 +343,9 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
+// Validation of a step's arguments, the pointer table (uploaded when it changes) and the
+// plan of the launches. Every step entry point starts here.
+static psgd_status prepare_step(psgd_handle* ph, const psgd_step_args* a, void* stream, Plan& p) {
   if (!ph || !a) return fail(PSGD_EINVAL, "handle or args is NULL");
   Handle& h = ph->h;
   const size_t B = h.B, J = h.J, W = h.W;
@@ -380,7 +411,7 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
     h.have_table = true;
   }
 
-  Plan p{};
+  p = Plan{};
   p.B = h.B; p.J = h.J; p.W = h.W; p.r = h.r; p.rp = h.rp;
   p.ob_r = h.r; p.ob_rp = h.rp; p.ob_c0 = 0; p.ob_src0 = 0;  // the orth driver sets blocks
   p.gdt = h.gdt; p.edt = h.edt;
@@ -395,67 +426,105 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   p.mask_off = h.d_mask_off;
   p.err_word = h.d_err;
   p.debug_expire = (h.cfg.flags & PSGD_FLAG_DEBUG_EXPIRE_WAIT) ? 1 : 0;
+  p.mean_div = (float)h.W;
+  p.q_to_exchange = 0;
+  return PSGD_OK;
+}
 
+// The phases of one step. ex: 0 the whole step (psgd_step); 1 up to the rank's P sum
+// (psgd_step_p); 2 skip decision, orthonormalisation and the rank's Q sum (psgd_step_q);
+// 3 the new Q state, G^ and E (psgd_step_e).
+static psgd_status run_step(psgd_handle* ph, const psgd_step_args* a, Plan& p, void* stream, int ex,
+                            const int64_t* block_counts, int w_total) {
+  Handle& h = ph->h;
+  const size_t B = h.B, J = h.J, W = h.W;
+  const bool dev_scales = a->scales_device != nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
   cudaEvent_t* ev = nullptr;
-  if (h.prof_used < h.prof_max) ev = &h.prof_events[(size_t)h.prof_used++ * (PSGD_NUM_PHASES + 1)];
+  if (ex == 0 && h.prof_used < h.prof_max) ev = &h.prof_events[(size_t)h.prof_used++ * (PSGD_NUM_PHASES + 1)];
   int phase = 0;
   auto mark = [&]() { if (ev) cudaEventRecord(ev[phase++], s); };
-  mark();
-  if (dev_scales && (e = launch_inv_scale(h.B, a->scales_device, h.d_inv_dev, s)) != cudaSuccess)
-    return cuda_fail(e, "inv_scale");
-  if (dev_scales) ++h.launches;
-  if ((e = cudaMemsetAsync(a->counts, 0, 8 * B * W, s)) != cudaSuccess) return cuda_fail(e, "counts");
-  if ((e = cudaMemsetAsync(h.d_scal_all, 0, 4 * kScalWords * B * J, s)) != cudaSuccess) return cuda_fail(e, "scal");
-  // The fused path ingests the gradients and forms the P partial sums in one sweep; the
-  // debug outputs (mask bitmap, stop after ingest) use the separate ingest kernel.
-  const bool fused = h.tc && !(h.cfg.flags & (PSGD_FLAG_MASK | PSGD_FLAG_STOP_AFTER_INGEST));
-  if (fused) {
-    if ((e = launch_prep_q(h, p, s)) != cudaSuccess) return cuda_fail(e, "prep_q");
-    if ((e = launch_ingest_p(h, p, s)) != cudaSuccess) return cuda_fail(e, "ingest_p");
-    if ((e = launch_unc_count(h, p, s)) != cudaSuccess) return cuda_fail(e, "unc_count");
-  } else if ((e = launch_ingest(h, p, s)) != cudaSuccess) {
-    return cuda_fail(e, "ingest");
-  }
-  mark();
-  if ((e = launch_skip_and_unc(h, p, s)) != cudaSuccess) return cuda_fail(e, "skip");
-  mark();
-  if (h.cfg.flags & PSGD_FLAG_STOP_AFTER_INGEST) {
-    while (ev && phase <= PSGD_NUM_PHASES) mark();
-    return PSGD_OK;
-  }
-  if (fused) {
-    if (h.edt == DT_BF16 && (e = launch_rescale_tiny(h, p, s)) != cudaSuccess) return cuda_fail(e, "rescale");
-    if ((e = launch_preduce(h, p, s)) != cudaSuccess) return cuda_fail(e, "preduce");
-  } else if (h.tc) {
-    if ((e = launch_prep_q(h, p, s)) != cudaSuccess) return cuda_fail(e, "prep_q");
-    if ((e = launch_pgemm_tc(h, p, s)) != cudaSuccess) return cuda_fail(e, "pgemm_tc");
-    if (h.edt == DT_BF16 && (e = launch_rescale_tiny(h, p, s)) != cudaSuccess) return cuda_fail(e, "rescale");
-  } else {
-    if ((e = launch_qmax(h, p, s)) != cudaSuccess) return cuda_fail(e, "qmax");
-    if ((e = launch_pgemm_simt(h, p, s)) != cudaSuccess) return cuda_fail(e, "pgemm");
-  }
-  mark();
-  if (h.r <= kRankBlock) {
-    // Pass 0 as separate kernels; the later passes, which a warm-started P rarely needs,
-    // in one cooperative launch that leaves at once when none is needed.
-    if ((e = launch_orth_passes(h, p, 0, 0, s)) != cudaSuccess) return cuda_fail(e, "orth");
-    e = launch_orth_coop(h, p, false, false, 0, tc_pchunk_kb(), 1, s);
-    if (e == cudaErrorCooperativeLaunchTooLarge) {
-      cudaGetLastError();  // nothing was enqueued: separate kernels for the later passes
-      e = launch_orth_passes(h, p, 1, kMaxPasses - 1, s);
+
+  if (ex == 0 || ex == 1) {
+    if (ex == 1) {  // the skip decision waits for every rank's counts; P stays a plain sum
+      p.skip = h.d_noskip;
+      p.mean_div = 1.0f;
     }
-    if (e != cudaSuccess) return cuda_fail(e, "orth");
-  } else if ((e = launch_orth(h, p, s)) != cudaSuccess) {
-    return cuda_fail(e, "orth");
+    mark();
+    if (dev_scales && (e = launch_inv_scale(h.B, a->scales_device, h.d_inv_dev, s)) != cudaSuccess)
+      return cuda_fail(e, "inv_scale");
+    if (dev_scales) ++h.launches;
+    if ((e = cudaMemsetAsync(a->counts, 0, 8 * B * W, s)) != cudaSuccess) return cuda_fail(e, "counts");
+    if ((e = cudaMemsetAsync(h.d_scal_all, 0, 4 * kScalWords * B * J, s)) != cudaSuccess) return cuda_fail(e, "scal");
+    // The fused path ingests the gradients and forms the P partial sums in one sweep; the
+    // debug outputs (mask bitmap, stop after ingest) use the separate ingest kernel.
+    const bool fused = h.tc && !(h.cfg.flags & (PSGD_FLAG_MASK | PSGD_FLAG_STOP_AFTER_INGEST));
+    if (fused) {
+      if ((e = launch_prep_q(h, p, s)) != cudaSuccess) return cuda_fail(e, "prep_q");
+      if ((e = launch_ingest_p(h, p, s)) != cudaSuccess) return cuda_fail(e, "ingest_p");
+      if ((e = launch_unc_count(h, p, s)) != cudaSuccess) return cuda_fail(e, "unc_count");
+    } else if ((e = launch_ingest(h, p, s)) != cudaSuccess) {
+      return cuda_fail(e, "ingest");
+    }
+    mark();
+    if (ex == 0 && (e = launch_skip_and_unc(h, p, s)) != cudaSuccess) return cuda_fail(e, "skip");
+    mark();
+    if (h.cfg.flags & PSGD_FLAG_STOP_AFTER_INGEST) {
+      while (ev && phase <= PSGD_NUM_PHASES) mark();
+      return PSGD_OK;
+    }
+    if (fused) {
+      if (h.edt == DT_BF16 && (e = launch_rescale_tiny(h, p, s)) != cudaSuccess) return cuda_fail(e, "rescale");
+      if ((e = launch_preduce(h, p, s)) != cudaSuccess) return cuda_fail(e, "preduce");
+    } else if (h.tc) {
+      if ((e = launch_prep_q(h, p, s)) != cudaSuccess) return cuda_fail(e, "prep_q");
+      if ((e = launch_pgemm_tc(h, p, s)) != cudaSuccess) return cuda_fail(e, "pgemm_tc");
+      if (h.edt == DT_BF16 && (e = launch_rescale_tiny(h, p, s)) != cudaSuccess) return cuda_fail(e, "rescale");
+    } else {
+      if ((e = launch_qmax(h, p, s)) != cudaSuccess) return cuda_fail(e, "qmax");
+      if ((e = launch_pgemm_simt(h, p, s)) != cudaSuccess) return cuda_fail(e, "pgemm");
+    }
+    if (ex == 1) {
+      if ((e = launch_pack_p(h, p, s)) != cudaSuccess) return cuda_fail(e, "exchange P");
+      return PSGD_OK;
+    }
   }
-  mark();
-  if (h.tc) {
-    if ((e = launch_qgemm_tc(h, p, s, false)) != cudaSuccess) return cuda_fail(e, "qgemm_tc");
-  } else if ((e = launch_qgemm_simt(h, p, s)) != cudaSuccess) {
-    return cuda_fail(e, "qgemm");
+
+  if (ex == 0 || ex == 2) {
+    if (ex == 2) {  // the summed counts decide; the summed P divides by every rank's workers,
+                    // and the Q reduction writes this rank's sum to the exchange buffers
+      if ((e = launch_skip_global(h, p, block_counts, w_total, s)) != cudaSuccess) return cuda_fail(e, "skip");
+      if ((e = launch_unpack_p(h, p, w_total, s)) != cudaSuccess) return cuda_fail(e, "exchange P");
+      p.mean_div = 1.0f;
+      p.q_to_exchange = 1;
+    }
+    mark();
+    if (h.r <= kRankBlock) {
+      // Pass 0 as separate kernels; the later passes, which a warm-started P rarely needs,
+      // in one cooperative launch that leaves at once when none is needed.
+      if ((e = launch_orth_passes(h, p, 0, 0, s)) != cudaSuccess) return cuda_fail(e, "orth");
+      e = launch_orth_coop(h, p, false, false, 0, tc_pchunk_kb(), 1, s);
+      if (e == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();  // nothing was enqueued: separate kernels for the later passes
+        e = launch_orth_passes(h, p, 1, kMaxPasses - 1, s);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "orth");
+    } else if ((e = launch_orth(h, p, s)) != cudaSuccess) {
+      return cuda_fail(e, "orth");
+    }
+    mark();
+    if (h.tc) {
+      if ((e = launch_qgemm_tc(h, p, s, false)) != cudaSuccess) return cuda_fail(e, "qgemm_tc");
+    } else if ((e = launch_qgemm_simt(h, p, s)) != cudaSuccess) {
+      return cuda_fail(e, "qgemm");
+    }
+    mark();
+    if ((e = launch_qreduce(h, p, s)) != cudaSuccess) return cuda_fail(e, "qreduce");
+    if (ex == 2) return PSGD_OK;
   }
-  mark();
-  if ((e = launch_qreduce(h, p, s)) != cudaSuccess) return cuda_fail(e, "qreduce");
+
+  if (ex == 3 && (e = launch_unpack_q(h, p, w_total, s)) != cudaSuccess) return cuda_fail(e, "exchange Q");
   mark();
   if (h.tc) {
     if ((e = launch_decomp_tc(h, p, s)) != cudaSuccess) return cuda_fail(e, "decomp_tc");
@@ -464,6 +533,65 @@ psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
   }
   mark();
   return PSGD_OK;
+}
+
+psgd_status psgd_step(psgd_handle* ph, const psgd_step_args* a, void* stream) {
+  Plan p;
+  const psgd_status st = prepare_step(ph, a, stream, p);
+  if (st != PSGD_OK) return st;
+  return run_step(ph, a, p, stream, 0, nullptr, 0);
+}
+
+static psgd_status check_exchange(psgd_handle* ph, int w_total) {
+  if (!ph) return fail(PSGD_EINVAL, "handle is NULL");
+  const Handle& h = ph->h;
+  if (!(h.cfg.flags & PSGD_FLAG_EXCHANGE))
+    return fail(PSGD_EUNSUPPORTED, "the exchange calls need a handle made with PSGD_FLAG_EXCHANGE");
+  if (w_total < h.W) return fail(PSGD_EINVAL, "total_workers must be >= this handle's num_workers");
+  return PSGD_OK;
+}
+
+psgd_status psgd_step_p(psgd_handle* ph, const psgd_step_args* a, void* stream) {
+  psgd_status st = check_exchange(ph, ph ? ph->h.W : 0);
+  if (st != PSGD_OK) return st;
+  Plan p;
+  if ((st = prepare_step(ph, a, stream, p)) != PSGD_OK) return st;
+  return run_step(ph, a, p, stream, 1, nullptr, 0);
+}
+
+psgd_status psgd_step_q(psgd_handle* ph, const psgd_step_args* a, const int64_t* block_counts,
+                        int32_t total_workers, void* stream) {
+  psgd_status st = check_exchange(ph, total_workers);
+  if (st != PSGD_OK) return st;
+  if (!block_counts || (reinterpret_cast<uintptr_t>(block_counts) & 7u))
+    return fail(PSGD_EINVAL, "block_counts must be an 8-byte aligned device pointer");
+  Plan p;
+  if ((st = prepare_step(ph, a, stream, p)) != PSGD_OK) return st;
+  return run_step(ph, a, p, stream, 2, block_counts, total_workers);
+}
+
+psgd_status psgd_step_e(psgd_handle* ph, const psgd_step_args* a, int32_t total_workers, void* stream) {
+  psgd_status st = check_exchange(ph, total_workers);
+  if (st != PSGD_OK) return st;
+  Plan p;
+  if ((st = prepare_step(ph, a, stream, p)) != PSGD_OK) return st;
+  return run_step(ph, a, p, stream, 3, nullptr, total_workers);
+}
+
+int64_t* psgd_exchange_counts(psgd_handle* ph) { return ph ? ph->h.d_xcnt : nullptr; }
+
+float* psgd_exchange_p(psgd_handle* ph, int32_t b, int32_t j) {
+  if (!ph) return nullptr;
+  const Handle& h = ph->h;
+  if (b < 0 || b >= h.B || j < 0 || j >= h.J) return nullptr;
+  return h.meta[(size_t)b * h.J + j].xp;
+}
+
+float* psgd_exchange_q(psgd_handle* ph, int32_t b, int32_t j) {
+  if (!ph) return nullptr;
+  const Handle& h = ph->h;
+  if (b < 0 || b >= h.B || j < 0 || j >= h.J) return nullptr;
+  return h.meta[(size_t)b * h.J + j].xq;
 }
 
 static void destroy_profile(Handle& h) {

@@ -54,6 +54,8 @@ struct Handle {
   float* d_scal_all = nullptr;  // [B*J*kScalWords] scaling words, zeroed every step
   float* d_inv_dev = nullptr;   // [B] 1/s_b formed on the device (psgd_step_args.scales_device)
   GridBarrier* d_gbar = nullptr;  // the cooperative orthonormalisation kernel's barrier
+  uint8_t* d_noskip = nullptr;    // [B] zeros: the skip flags the exchange's first call runs with
+  int64_t* d_xcnt = nullptr;      // [B] exchange: this rank's nonfinite counts per block
   size_t maps_bytes = 0;        // TMA maps of the callers' G and E (tensor engine), after the table
   int max_mtiles = 0, max_S = 0, max_C = 0, max_ntiles64 = 0, max_mtiles64 = 0;
   int max_kchunks = 0, max_ntiles128 = 0;
@@ -101,6 +103,13 @@ cudaError_t launch_orth_coop(const Handle& h, const Plan& p, bool fused_preduce,
 // the cooperative kernel for the passes after it, or separate kernels for all passes.
 cudaError_t launch_orth_passes(const Handle& h, const Plan& p, int first_pass, int last_pass, cudaStream_t s);
 int orth_coop_grid();
+
+// Data-parallel exchange points (exchange.cu).
+cudaError_t launch_pack_p(const Handle& h, const Plan& p, cudaStream_t s);
+cudaError_t launch_skip_global(const Handle& h, const Plan& p, const int64_t* block_counts, int w_total,
+                               cudaStream_t s);
+cudaError_t launch_unpack_p(const Handle& h, const Plan& p, int w_total, cudaStream_t s);
+cudaError_t launch_unpack_q(const Handle& h, const Plan& p, int w_total, cudaStream_t s);
 cudaError_t launch_inv_scale(int B, const float* scale, float* inv, cudaStream_t s);
 
 }  // namespace psgd

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kCoopThreads, 1) k_orth_coop(Plan p, CoopArgs 
             acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
             acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
           }
-          const float fw = (float)p.W;
+          const float fw = p.mean_div;
           float4 o;
           o.x = __fdiv_rn(acc.x, fw); o.y = __fdiv_rn(acc.y, fw);
           o.z = __fdiv_rn(acc.z, fw); o.w = __fdiv_rn(acc.w, fw);

@@ -37,6 +37,8 @@ struct MatMeta {
   uint16_t* psplit;   // [2*rp][mpad] 16-bit: P^ (scaled) hi rows then lo rows
   uint16_t* pdec;     // [mpad][3*rp] 16-bit: [P^hi | P^lo | P^hi] rows (decompress A)
   uint16_t* qdec;     // [npad][3*rp] 16-bit: [Q hi | Q hi | Q lo] rows (decompress B)
+  float* xp;          // m x r fp32: exchange buffer of this rank's P sum (or NULL)
+  float* xq;          // n x r fp32: exchange buffer of this rank's Q sum (or NULL)
   float* scal;        // [8] words, zeroed every step: max|M|, max|P|, max|Q| (state),
                       // max|Q| (new), the exponent shift of a rescaled M scratch (int)
 };
@@ -87,6 +89,9 @@ struct Plan {
   int32_t ob_r, ob_rp, ob_c0, ob_src0;
   int32_t debug_expire;          // PSGD_FLAG_DEBUG_EXPIRE_WAIT: the decompression kernel's
                                  // MMA thread waits on a barrier nothing completes
+  float mean_div;                // divisor of the worker sums of P and Q: W, or 1 when the
+                                 // sums go to the exchange buffers (psgd_step_p / _q)
+  int32_t q_to_exchange;         // the Q reduction writes this rank's sum to MatMeta::xq
 };
 
 // Programmatic dependent launch. A kernel launched by launch_pdl may be scheduled while

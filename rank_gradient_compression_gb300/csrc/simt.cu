@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kT) k_pgemm(Plan p) {
     }
   }
   unsigned vmax = 0u;
-  const float fw = (float)p.W;
+  const float fw = p.mean_div;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t row = row0 + ty * 4 + i;
@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(256) k_qreduce(Plan p, float qscale) {
   const int g = warp & (kQredSplit - 1);
   const int64_t row = (int64_t)blockIdx.x * 2 + (warp >> 2);
   if ((int64_t)blockIdx.x * 2 >= mt.n) return;  // whole block past the end (block-uniform)
-  const float fw = (float)p.W;
-  float* q = p.tab.q[blockIdx.y];
+  const float fw = p.mean_div;
+  float* q = p.q_to_exchange ? mt.xq : p.tab.q[blockIdx.y];
   const int msh = reinterpret_cast<const int*>(mt.scal)[SC_MSHIFT];  // rescaled M: Q * 2^msh
   const size_t stride = (size_t)mt.n * p.rp;  // one slice of Qpart
   __shared__ float4 part[2][kQredSplit][32];
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(256) k_qreduce(Plan p, float qscale) {
     __syncthreads();
   }
   vmax = block_max_u32(vmax);
-  if (threadIdx.x == 0 && vmax) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 3, vmax);
+  if (threadIdx.x == 0 && vmax && !p.q_to_exchange) atomicMax(reinterpret_cast<unsigned*>(mt.scal) + 3, vmax);
 }
 
 template <typename TE> struct V4;

@@ -156,7 +156,7 @@ __global__ void k_preduce(Plan p, int pchunk_kb) {
       acc.x = __fadd_rn(acc.x, v.x); acc.y = __fadd_rn(acc.y, v.y);
       acc.z = __fadd_rn(acc.z, v.z); acc.w = __fadd_rn(acc.w, v.w);
     }
-    const float fw = (float)p.W;
+    const float fw = p.mean_div;
     float4 o;
     o.x = __fdiv_rn(acc.x, fw); o.y = __fdiv_rn(acc.y, fw);
     o.z = __fdiv_rn(acc.z, fw); o.w = __fdiv_rn(acc.w, fw);
@@ -238,6 +238,35 @@ __device__ __forceinline__ bool unit_off(const Plan& p, const MatMeta& mt, int o
   return only_shifted && reinterpret_cast<const int*>(mt.scal)[SC_MSHIFT] == 0;
 }
 
+// The sequence of (unit, k-block, worker) A stages of a CTA's units, skipping units that are
+// off; the Q GEMM's producer walks a copy of it kPrefetchStages ahead of its loads and
+// prefetches those boxes into L2.
+constexpr int kPrefetchStages = 3;
+struct AStageIter {
+  int u, u_end, u_step, kb, w;
+  bool valid;
+  __device__ void seek(const Plan& p, const Unit* units, int only_shifted);
+  __device__ void next(const Plan& p, const Unit* units, int only_shifted, int kps) {
+    if (++w < p.W) return;
+    w = 0;
+    kb += kps;
+    if (kb < units[u].kb1) return;
+    u += u_step;
+    seek(p, units, only_shifted);
+  }
+};
+
+__device__ void AStageIter::seek(const Plan& p, const Unit* units, int only_shifted) {
+  for (; u < u_end; u += u_step)
+    if (!unit_off(p, p.meta[units[u].t], only_shifted)) {
+      kb = units[u].kb0;
+      w = 0;
+      valid = true;
+      return;
+    }
+  valid = false;
+}
+
 // MN_A = false: P GEMM (A = M tile K-major, unit = row tile x k-chunk).
 // MN_A = true:  Q GEMM (A = M^T tile MN-major, unit = column tile x m-slice).
 // kps (Q GEMM): k-blocks per stage. With 2, an A stage is 128 rows of M (two 64 x 128-row
@@ -249,7 +278,7 @@ constexpr int kGemmEpiWarps = 8;   // two per TMEM lane quarter, each with half 
 template <bool MN_A, bool BF16>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
-       int a_stages, uint32_t b_stage, int only_shifted, int seg, int kps) {
+       int a_stages, uint32_t b_stage, int only_shifted, int seg, int kps, int contig) {
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -271,6 +300,11 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
   const uint32_t b_bytes = (uint32_t)N * BK * 2;  // one k-block's B tile
   const uint32_t b_tile = b_stage / (uint32_t)kps;  // its slot in a B stage (1 KB multiple)
   int* err = p.err_word;
+  // Units of this CTA: every gridDim.x-th one, or (contig) one contiguous range, so that
+  // consecutive units can share the rows of M and with them the B operand.
+  const int u_first = contig ? (int)((int64_t)blockIdx.x * nunits / gridDim.x) : (int)blockIdx.x;
+  const int u_end = contig ? (int)((int64_t)(blockIdx.x + 1) * nunits / gridDim.x) : nunits;
+  const int u_step = contig ? 1 : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < A_STAGES; ++i) { mbar_init(&sm.full_a[i], 1); mbar_init(&sm.empty_a[i], 1); }
@@ -294,8 +328,24 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t ia = 0, ib = 0;
+      int64_t b_tag[B_STAGES];  // (matrix, first k-block) a B stage holds, -1: none
+      for (int i = 0; i < B_STAGES; ++i) b_tag[i] = -1;
       bool ok = true;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      // L2 prefetch of the A boxes kPrefetchStages stages ahead (Q GEMM)
+      AStageIter pf{u_first, u_end, u_step, 0, 0, false};
+      auto prefetch_next = [&]() {
+        if (!pf.valid) return;
+        const Unit un = units[pf.u];
+        const CUtensorMap* mm = maps + (size_t)un.t * NMAPS + MAP_MQ;
+        tma_prefetch_3d(mm, un.tile * BM, pf.kb * BK, pf.w);
+        tma_prefetch_3d(mm, un.tile * BM + 64, pf.kb * BK, pf.w);
+        pf.next(p, units, only_shifted, kps);
+      };
+      if (MN_A) {
+        pf.seek(p, units, only_shifted);
+        for (int i = 0; i < kPrefetchStages; ++i) prefetch_next();
+      }
+      for (int u = u_first; u < u_end && ok; u += u_step) {
         const Unit un = units[u];
         const MatMeta& mt = p.meta[un.t];
         if (unit_off(p, mt, only_shifted)) continue;
@@ -306,11 +356,17 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
           const int sb = ib % B_STAGES;
           ok = mbar_wait(&sm.empty_b[sb], ((ib / B_STAGES) & 1) ^ 1, err);
           if (!ok) break;
-          mbar_arrive_expect_tx(&sm.full_b[sb], (uint32_t)nk * b_bytes);
-          for (int h = 0; h < nk; ++h)
-            for (int x = 0; x < NBOX; ++x)
-              tma_load_2d(S.b(sb, b_stage) + h * b_tile + x * (N / NBOX) * BK * 2, mb, (kb + h) * BK,
-                          x * (N / NBOX), &sm.full_b[sb]);
+          const int64_t tag = ((int64_t)un.t << 32) | ((int64_t)kb << 8) | nk;
+          if (b_tag[sb] == tag) {
+            mbar_arrive(&sm.full_b[sb]);  // the stage still holds these k-blocks' B tiles
+          } else {
+            b_tag[sb] = tag;
+            mbar_arrive_expect_tx(&sm.full_b[sb], (uint32_t)nk * b_bytes);
+            for (int h = 0; h < nk; ++h)
+              for (int x = 0; x < NBOX; ++x)
+                tma_load_2d(S.b(sb, b_stage) + h * b_tile + x * (N / NBOX) * BK * 2, mb, (kb + h) * BK,
+                            x * (N / NBOX), &sm.full_b[sb]);
+          }
           ++ib;
           for (int w = 0; w < p.W; ++w) {
             const int sa = ia % A_STAGES;
@@ -324,6 +380,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
             } else {
               tma_load_3d(S.a(sa), mm, un.tile * BM, kb * BK, w, &sm.full_a[sa]);
               tma_load_3d(S.a(sa) + a_bytes / 2, mm, un.tile * BM + 64, kb * BK, w, &sm.full_a[sa]);
+              prefetch_next();
             }
             ++ia;
           }
@@ -341,7 +398,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
       const uint32_t idesc = idesc_f16(BM, rp, BF16, MN_A, false);
       uint32_t ia = 0, ib = 0, ju = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      for (int u = u_first; u < u_end && ok; u += u_step) {
         const Unit un = units[u];
         if (unit_off(p, p.meta[un.t], only_shifted)) continue;
         const int nsteps = (un.kb1 - un.kb0) * p.W;
@@ -406,7 +463,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
     const int nch = rp / 16, ch0 = half ? (nch + 1) / 2 : 0, ch1 = half ? nch : (nch + 1) / 2;
     uint32_t ju = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+    for (int u = u_first; u < u_end && ok; u += u_step) {
       const Unit un = units[u];
       const MatMeta& mt = p.meta[un.t];
       if (unit_off(p, mt, only_shifted)) continue;
@@ -495,6 +552,7 @@ static_assert(128 % kIngRowsPerPass == 0, "ingest rows");
 // HBM markedly slower (measured on GB300: 4.4 against 6.1 TB/s for a pure TMA read of the
 // same bytes).
 constexpr int kMaxKps = 2;
+constexpr int kIngPrefetch = 1;  // G/E stages prefetched into L2 ahead of their loads
 __host__ __device__ constexpr int ge_bytes(int kps) { return 2 * kps * A_BYTES; }
 constexpr int kMaxGeStages = 4;
 struct IngBars {
@@ -601,6 +659,19 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
       const CUtensorMap* gem = static_cast<const CUtensorMap*>(p.tab.ge_maps);
       StageIter ti;
       ti.start(units, nunits, kps);
+      // L2 prefetch of the G/E boxes kIngPrefetch stages ahead of the loads
+      StageIter pf;
+      pf.start(units, nunits, kps);
+      auto prefetch_next = [&]() {
+        if (!pf.valid) return;
+        const size_t slot = (size_t)pf.un.t * p.W + pf.w;
+        for (int h = 0; h < pf.nk; ++h) {
+          tma_prefetch_2d(gem + 2 * slot, (pf.kb + h) * BK, pf.un.tile * BM);
+          tma_prefetch_2d(gem + 2 * slot + 1, (pf.kb + h) * BK, pf.un.tile * BM);
+        }
+        pf.next(units, nunits, p.W, kps);
+      };
+      for (int i = 0; i < kIngPrefetch; ++i) prefetch_next();
       uint32_t ig = 0;
       bool ok = true;
       while (ti.valid && ok) {
@@ -614,6 +685,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
           tma_load_2d(st + h * A_BYTES, gem + 2 * slot, (ti.kb + h) * BK, ti.un.tile * BM, &sm.full_ge[s]);
         for (int h = 0; h < ti.nk; ++h)  // then the E boxes
           tma_load_2d(st + (kps + h) * A_BYTES, gem + 2 * slot + 1, (ti.kb + h) * BK, ti.un.tile * BM, &sm.full_ge[s]);
+        prefetch_next();
         ++ig;
         ti.next(units, nunits, p.W, kps);
       }
@@ -851,6 +923,7 @@ constexpr int DEC_STAGES = 2;   // P^ / Q operand stages of the G^ MMA
 constexpr int DEC_MSTAGES = 4;  // M_w tile ring (E is formed in place and stored from it;
                                 // G^ goes out through the same ring, 64 fp32 columns a stage)
 constexpr int DEC_MSTAGE_BYTES = 2 * A_BYTES;
+constexpr int kDecPrefetch = 2;  // M tiles prefetched into L2 ahead of their loads
 constexpr int DEC_THREADS = 352;
 struct DecSmem {
   alignas(1024) uint8_t a[DEC_STAGES][A_BYTES];          // P^ split tiles, 128 x 64
@@ -995,6 +1068,18 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
         bulk_wait_read_all();
         return true;
       };
+      // L2 prefetch of the M tiles kDecPrefetch tiles ahead of their loads
+      int pf_u = blockIdx.x, pf_w = 0;
+      auto prefetch_next = [&]() {
+        while (pf_u < nunits && p.skip[p.meta[units[pf_u].t].b]) pf_u += gridDim.x;
+        if (pf_u >= nunits) return;
+        const Unit un = units[pf_u];
+        const CUtensorMap* mm = maps + (size_t)un.t * NMAPS + MAP_MP;
+        tma_prefetch_3d(mm, un.kb0 * DEC_NT, un.tile * BM, pf_w);
+        if ((int64_t)un.kb0 * DEC_NT + 64 < p.meta[un.t].n) tma_prefetch_3d(mm, un.kb0 * DEC_NT + 64, un.tile * BM, pf_w);
+        if (++pf_w == p.W) { pf_w = 0; pf_u += gridDim.x; }
+      };
+      for (int k = 0; k < kDecPrefetch; ++k) prefetch_next();
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const Unit un = units[u];
         const MatMeta& mt = p.meta[un.t];
@@ -1010,6 +1095,7 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
             mbar_arrive_expect_tx(&sm.mfull[s], (uint32_t)(1 + two) * A_BYTES);
             tma_load_3d(sm.mt[s], mm, col0, row0, w, &sm.mfull[s]);
             if (two) tma_load_3d(sm.mt[s] + A_BYTES, mm, col0 + 64, row0, w, &sm.mfull[s]);
+            prefetch_next();
             ++i;
           }
         }
@@ -1297,7 +1383,7 @@ cudaError_t launch_rescale_tiny(const Handle& h, const Plan& p, cudaStream_t s) 
   const uint32_t bst = gemm_b_stage(h.edt, p.rp);
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
-  launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 1, kGemmSegSteps, 1);
+  launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 1, kGemmSegSteps, 1, 0);
   h.launches += 1;
   return cudaGetLastError();
 }
@@ -1378,9 +1464,11 @@ cudaError_t tc_plan(Handle& h, char* ws_tc, cudaStream_t s) {
     for (int i = 0; i < mt.mtiles; ++i)
       for (int c = 0; c < mt.kchunks; ++c)
         pu.push_back(Unit{t, i, c * PCHUNK_KB, std::min(nkb, (c + 1) * PCHUNK_KB), c, 0});
+    // slice-major: the units of one slice of rows come back to back, and each CTA takes a
+    // contiguous range of them, so it keeps the slice's B tiles across column tiles
     const int mkb = (int)((m + 63) / 64), skb = QSLICE_ROWS / 64;
-    for (int i = 0; i < (int)((n + 127) / 128); ++i)
-      for (int s2 = 0; s2 < mt.S; ++s2)
+    for (int s2 = 0; s2 < mt.S; ++s2)
+      for (int i = 0; i < (int)((n + 127) / 128); ++i)
         qu.push_back(Unit{t, i, s2 * skb, std::min(mkb, (s2 + 1) * skb), s2, 0});
     for (int i = 0; i < mt.mtiles; ++i)
       for (int jn = 0; jn < (int)(npad / DEC_NT); ++jn) du.push_back(Unit{t, i, jn, jn + 1, 0, 0});
@@ -1388,10 +1476,11 @@ cudaError_t tc_plan(Handle& h, char* ws_tc, cudaStream_t s) {
   // largest units first, so the static round-robin ends with the short ones
   auto by_work = [](const Unit& a, const Unit& b) { return (a.kb1 - a.kb0) > (b.kb1 - b.kb0); };
   std::stable_sort(pu.begin(), pu.end(), by_work);
-  std::stable_sort(qu.begin(), qu.end(), by_work);
+
   tp->np = (int)pu.size(); tp->nq = (int)qu.size(); tp->nd = (int)du.size();
   tp->grid = num_sms();
-  cudaError_t e = cudaMemcpyAsync(tp->d_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice, s);
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(tp->d_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(tp->d_punits, pu.data(), sizeof(Unit) * pu.size(), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(tp->d_qunits, qu.data(), sizeof(Unit) * qu.size(), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(tp->d_dunits, du.data(), sizeof(Unit) * du.size(), cudaMemcpyHostToDevice, s);
@@ -1443,8 +1532,8 @@ cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const int ast = gemm_a_stages(bst);
   const size_t sm = gemm_smem(bst, ast);
   const int seg = kGemmSegSteps;
-  if (h.edt == DT_BF16) launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg, 1);
-  else launch_pdl(k_gemm<false, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg, 1);
+  if (h.edt == DT_BF16) launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg, 1, 0);
+  else launch_pdl(k_gemm<false, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg, 1, 0);
   int64_t maxe = 0;
   for (const MatMeta& mt : h.meta) maxe = std::max<int64_t>(maxe, mt.m * p.rp);
   launch_pdl(k_preduce, dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), dim3(256), 0, s, p, PCHUNK_KB);
@@ -1474,8 +1563,9 @@ cudaError_t launch_preduce(const Handle& h, const Plan& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-int tc_kpad(const Handle& h) { return static_cast<const TcPlan*>(h.tc_plan)->kp; }
 int tc_pchunk_kb() { return PCHUNK_KB; }
+
+int tc_kpad(const Handle& h) { return static_cast<const TcPlan*>(h.tc_plan)->kp; }
 
 cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s, bool psplit_done) {
   const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
@@ -1491,8 +1581,8 @@ cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s, bool
   const int ast = gemm_a_stages(bst, kps);
   const size_t sm = gemm_smem(bst, ast, kps);
   const int seg = kGemmSegSteps;
-  if (h.edt == DT_BF16) launch_pdl(k_gemm<true, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg, kps);
-  else launch_pdl(k_gemm<true, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg, kps);
+  if (h.edt == DT_BF16) launch_pdl(k_gemm<true, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg, kps, 1);
+  else launch_pdl(k_gemm<true, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_qunits, tp->nq, ast, bst, 0, seg, kps, 1);
   h.launches += 1;
   return cudaGetLastError();
 }

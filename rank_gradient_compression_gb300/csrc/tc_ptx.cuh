@@ -101,6 +101,18 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 }
 // Wait until every committed bulk store of this thread is complete.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Prefetch a box into L2 (no shared memory, no completion to wait for). Issued a few
+// stages ahead of the box's load, it keeps more bytes in flight than the stage ring holds.
+__device__ __forceinline__ void tma_prefetch_2d(const void* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d(const void* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int x, int y, int z,
                                             uint64_t* bar) {
   asm volatile(

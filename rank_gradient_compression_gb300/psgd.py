@@ -17,6 +17,7 @@ PSGD_F32, PSGD_F16, PSGD_BF16 = 0, 1, 2
 PSGD_OK, PSGD_EINVAL, PSGD_ECUDA, PSGD_EUNSUPPORTED, PSGD_ETIMEOUT = range(5)
 PSGD_FLAG_SIMT, PSGD_FLAG_MASK, PSGD_FLAG_STOP_AFTER_INGEST = 0x1, 0x2, 0x4
 PSGD_FLAG_DEBUG_EXPIRE_WAIT = 0x8
+PSGD_FLAG_EXCHANGE = 0x10
 
 DTYPE_CODE = {"f32": PSGD_F32, "f16": PSGD_F16, "bf16": PSGD_BF16}
 
@@ -26,7 +27,8 @@ EXPORTS = ("psgd_workspace_size", "psgd_mask_offset", "psgd_mask_words", "psgd_i
            "psgd_debug_m", "psgd_debug_phat", "psgd_engine", "psgd_profile_begin",
            "psgd_profile_end", "psgd_launch_count", "psgd_debug_orth",
            "psgd_orthonormalize_static", "psgd_scale_update", "psgd_clip_adam_workspace_size",
-           "psgd_clip_adam", "psgd_reduce_uncompressed")
+           "psgd_clip_adam", "psgd_reduce_uncompressed", "psgd_step_p", "psgd_step_q",
+           "psgd_step_e", "psgd_exchange_p", "psgd_exchange_q", "psgd_exchange_counts")
 PSGD_STATIC_MAX_ROWS, PSGD_STATIC_MAX_COLS = 16384, 128
 PSGD_MAX_ORTH_PASSES = 4
 PSGD_ADAM_MAX_TENSORS = 512
@@ -85,6 +87,18 @@ def _load():
     lib.psgd_init.argtypes = [POINTER(psgd_config), c_void_p, c_size_t, c_void_p, POINTER(c_void_p)]
     lib.psgd_step.restype = c_int32
     lib.psgd_step.argtypes = [c_void_p, POINTER(psgd_step_args), c_void_p]
+    for name in ("psgd_step_p",):
+        getattr(lib, name).restype = c_int32
+        getattr(lib, name).argtypes = [c_void_p, POINTER(psgd_step_args), c_void_p]
+    lib.psgd_step_q.restype = c_int32
+    lib.psgd_step_q.argtypes = [c_void_p, POINTER(psgd_step_args), c_void_p, c_int32, c_void_p]
+    lib.psgd_step_e.restype = c_int32
+    lib.psgd_step_e.argtypes = [c_void_p, POINTER(psgd_step_args), c_int32, c_void_p]
+    for name in ("psgd_exchange_p", "psgd_exchange_q"):
+        getattr(lib, name).restype = c_void_p
+        getattr(lib, name).argtypes = [c_void_p, c_int32, c_int32]
+    lib.psgd_exchange_counts.restype = c_void_p
+    lib.psgd_exchange_counts.argtypes = [c_void_p]
     lib.psgd_check.restype = c_int32
     lib.psgd_check.argtypes = [c_void_p, c_void_p]
     lib.psgd_finalize.restype = c_int32
@@ -160,6 +174,32 @@ def psgd_init(cfg, workspace_ptr: int, ws_bytes: int, stream: int) -> int:
 
 def psgd_step(handle: int, args: psgd_step_args, stream: int):
     _check(lib.psgd_step(c_void_p(handle), byref(args), c_void_p(stream)))
+
+
+def psgd_step_p(handle: int, args: psgd_step_args, stream: int):
+    _check(lib.psgd_step_p(c_void_p(handle), byref(args), c_void_p(stream)))
+
+
+def psgd_step_q(handle: int, args: psgd_step_args, block_counts_ptr: int, total_workers: int,
+                stream: int):
+    _check(lib.psgd_step_q(c_void_p(handle), byref(args), c_void_p(block_counts_ptr),
+                           int(total_workers), c_void_p(stream)))
+
+
+def psgd_step_e(handle: int, args: psgd_step_args, total_workers: int, stream: int):
+    _check(lib.psgd_step_e(c_void_p(handle), byref(args), int(total_workers), c_void_p(stream)))
+
+
+def psgd_exchange_p(handle: int, b: int, j: int) -> int:
+    return lib.psgd_exchange_p(c_void_p(handle), b, j) or 0
+
+
+def psgd_exchange_q(handle: int, b: int, j: int) -> int:
+    return lib.psgd_exchange_q(c_void_p(handle), b, j) or 0
+
+
+def psgd_exchange_counts(handle: int) -> int:
+    return lib.psgd_exchange_counts(c_void_p(handle)) or 0
 
 
 def psgd_check(handle: int, stream: int):
@@ -278,7 +318,7 @@ class PowerSGD:
         self.handle = psgd_init(self.cfg, self._ws_ptr, ws, stream)
         self.engine = psgd_engine(self.handle)
 
-    def step(self, grads, errs, q, scales, ghat, unc_in=None, unc_out=None, scales_device=None):
+    def _args(self, grads, errs, q, scales, ghat, unc_in=None, unc_out=None, scales_device=None):
         B, J, W = self.B, self.J, self.W
         g = _ptrs([grads[b][j][w] for b in range(B) for j in range(J) for w in range(W)])
         e = _ptrs([errs[b][j][w] for b in range(B) for j in range(J) for w in range(W)])
@@ -287,11 +327,51 @@ class PowerSGD:
         sc = (ctypes.c_float * B)(*[float(s) for s in scales]) if scales is not None else None
         ui = _ptrs([unc_in[b][w] for b in range(B) for w in range(W)]) if unc_in is not None else None
         uo = _ptrs([unc_out[b] for b in range(B)]) if unc_out is not None else None
-        args = psgd_step_args(g, e, qq, sc, gh, ui, uo, c_void_p(self.counts.data_ptr()),
+        return psgd_step_args(g, e, qq, sc, gh, ui, uo, c_void_p(self.counts.data_ptr()),
                               c_void_p(self.skip.data_ptr()),
                               c_void_p(self.mask.data_ptr() if self.mask is not None else 0),
                               c_void_p(scales_device.data_ptr() if scales_device is not None else 0))
-        psgd_step(self.handle, args, self.torch.cuda.current_stream(self.device).cuda_stream)
+
+    def _stream(self):
+        return self.torch.cuda.current_stream(self.device).cuda_stream
+
+    def step(self, grads, errs, q, scales, ghat, unc_in=None, unc_out=None, scales_device=None):
+        args = self._args(grads, errs, q, scales, ghat, unc_in, unc_out, scales_device)
+        psgd_step(self.handle, args, self._stream())
+
+    # Data-parallel exchange points (a handle made with PSGD_FLAG_EXCHANGE): step_p,
+    # all-reduce (sum) of exchange_p() and exchange_counts(), step_q, all-reduce of
+    # exchange_q(), step_e. The same arguments as step().
+    def step_p(self, grads, errs, q, scales, ghat, scales_device=None):
+        args = self._args(grads, errs, q, scales, ghat, scales_device=scales_device)
+        psgd_step_p(self.handle, args, self._stream())
+
+    def step_q(self, grads, errs, q, scales, ghat, block_counts, total_workers, scales_device=None):
+        args = self._args(grads, errs, q, scales, ghat, scales_device=scales_device)
+        psgd_step_q(self.handle, args, block_counts.data_ptr(), total_workers, self._stream())
+
+    def step_e(self, grads, errs, q, scales, ghat, total_workers, scales_device=None):
+        args = self._args(grads, errs, q, scales, ghat, scales_device=scales_device)
+        psgd_step_e(self.handle, args, total_workers, self._stream())
+
+    def _ws_view(self, ptr, count, dtype):
+        es = self.torch.empty((), dtype=dtype).element_size()
+        off = ptr - self.workspace.data_ptr()
+        return self.workspace[off:off + count * es].view(dtype)
+
+    def exchange_p(self):
+        """The P exchange buffers of every matrix, one flat fp32 view in (b, j) order."""
+        n = self.B * sum(m for m, _ in self.shapes) * self.r
+        return self._ws_view(psgd_exchange_p(self.handle, 0, 0), n, self.torch.float32)
+
+    def exchange_q(self):
+        """The Q exchange buffers of every matrix, one flat fp32 view in (b, j) order."""
+        n = self.B * sum(c for _, c in self.shapes) * self.r
+        return self._ws_view(psgd_exchange_q(self.handle, 0, 0), n, self.torch.float32)
+
+    def exchange_counts(self):
+        """This rank's per-block nonfinite counts (int64 [B]), written by step_p."""
+        return self._ws_view(psgd_exchange_counts(self.handle), self.B, self.torch.int64)
 
     def check(self):
         psgd_check(self.handle, self.torch.cuda.current_stream(self.device).cuda_stream)

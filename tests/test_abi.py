@@ -152,3 +152,25 @@ def test_reduce_uncompressed_argument_checks(psgd):
             psgd.psgd_reduce_uncompressed(**dict(ok, **kw))
         assert ex.value.status == psgd.PSGD_EINVAL
         assert msg in str(ex.value), (kw, str(ex.value))
+
+
+def test_exchange_flag_planning_and_null_handles(psgd):
+    """The data-parallel exchange calls: planning, rejections and NULL handles."""
+    shapes = [(256, 512), (128, 64)]
+    B, r = 3, 8
+    plain, _ = psgd.make_config(shapes, B, 2, r, "f16")
+    ex, _ = psgd.make_config(shapes, B, 2, r, "f16", flags=psgd.PSGD_FLAG_EXCHANGE)
+    extra = psgd.psgd_workspace_size(ex) - psgd.psgd_workspace_size(plain)
+    assert extra >= 4 * B * r * sum(m + n for m, n in shapes) + 8 * B
+    bad, _ = psgd.make_config(shapes, B, 2, r, "f16", unc_len=16, flags=psgd.PSGD_FLAG_EXCHANGE)
+    assert psgd.psgd_workspace_size(bad) == 0
+    assert "unc_len == 0" in psgd.lib.psgd_last_error().decode()
+    bad, _ = psgd.make_config(shapes, B, 2, r, "f16",
+                              flags=psgd.PSGD_FLAG_EXCHANGE | psgd.PSGD_FLAG_STOP_AFTER_INGEST)
+    assert psgd.psgd_workspace_size(bad) == 0
+    lib = psgd.lib
+    assert lib.psgd_step_p(None, None, None) == psgd.PSGD_EINVAL
+    assert lib.psgd_step_q(None, None, None, 4, None) == psgd.PSGD_EINVAL
+    assert lib.psgd_step_e(None, None, 4, None) == psgd.PSGD_EINVAL
+    assert psgd.psgd_exchange_p(0, 0, 0) == 0 and psgd.psgd_exchange_q(0, 0, 0) == 0
+    assert psgd.psgd_exchange_counts(0) == 0
