@@ -37,9 +37,12 @@
  *     PSGD_EUNSUPPORTED before any launch. CUDA launch/runtime errors return
  *     PSGD_ECUDA. psgd_last_error() returns a per-thread message for the last failure.
  *   - psgd_step is asynchronous on `stream` (a cudaStream_t, or NULL for the legacy
- *     default stream). It never synchronises the host, except when the pointer or
- *     scale tables differ from the previous call. Then it waits for that call's table
- *     upload to finish before it reuses the staging buffer.
+ *     default stream). The handle keeps the last 4 distinct pointer/scale tables (with
+ *     the TMA descriptors of their G and E buffers) on the device, so buffer sets used
+ *     in turn are encoded and uploaded once. A table that is none of those replaces the
+ *     least recently used one; the host then waits only if that slot's own upload, 4
+ *     tables ago, has not finished. Calls on one handle must be ordered on the device
+ *     (one stream, or streams joined by events): a table is overwritten in stream order.
  */
 #ifndef PSGD_H_
 #define PSGD_H_

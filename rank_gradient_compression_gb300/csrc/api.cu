@@ -44,7 +44,7 @@ struct Layout {
   size_t inv_dev = 0, gbar = 0, noskip = 0, xcnt = 0;
   std::vector<size_t> mscr, P, Xa, Xb, Phat, ostate, Qpart, Gpart, Rinv, xp, xq;
   size_t tc = 0;
-  size_t table_bytes = 0, maps_bytes = 0;
+  size_t table_bytes = 0, maps_bytes = 0, table_stride = 0;
   int64_t nseg = 0;
 };
 
@@ -96,7 +96,8 @@ Layout plan_layout(const psgd_config* c) {
   L.table_bytes = 8 * ((size_t)2 * B * J * W + 2 * (size_t)B * J + (size_t)B * W + B) + 4 * (size_t)B;
   L.table_bytes = (L.table_bytes + 127) / 128 * 128;
   L.maps_bytes = tc_ge_maps_bytes(c);
-  L.table = take(L.table_bytes + L.maps_bytes);
+  L.table_stride = up256(L.table_bytes + L.maps_bytes);
+  L.table = take(Handle::kTableSlots * L.table_stride);
   L.err = take(16);
   L.scal = take(4 * kScalWords * (size_t)B * J);
   L.inv_dev = take(4 * (size_t)B);
@@ -235,6 +236,7 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
   h.d_segs = reinterpret_cast<IngestSeg*>(h.ws + L.segs);
   h.d_table = h.ws + L.table;
   h.table_bytes = L.table_bytes;
+  h.table_stride = L.table_stride;
   h.maps_bytes = h.tc ? L.maps_bytes : 0;
   h.d_err = reinterpret_cast<int*>(h.ws + L.err);
   h.d_scal_all = reinterpret_cast<float*>(h.ws + L.scal);
@@ -319,24 +321,18 @@ psgd_status psgd_init(const psgd_config* cfg, void* workspace, size_t ws_bytes, 
   if (e == cudaSuccess) e = cudaMemsetAsync(h.d_err, 0, 16, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(h.d_noskip, 0, (size_t)h.B, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&h.h_stage), h.table_bytes + h.maps_bytes, cudaHostAllocDefault);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.upload_ev, cudaEventDisableTiming);
+  if (e == cudaSuccess)
+    e = cudaHostAlloc(reinterpret_cast<void**>(&h.h_stage), Handle::kTableSlots * h.table_stride, cudaHostAllocDefault);
+  for (int k = 0; k < Handle::kTableSlots && e == cudaSuccess; ++k)
+    e = cudaEventCreateWithFlags(&h.slot_ev[k], cudaEventDisableTiming);
   if (e != cudaSuccess) {
+    for (int k = 0; k < Handle::kTableSlots; ++k)
+      if (h.slot_ev[k]) cudaEventDestroy(h.slot_ev[k]);
     if (h.h_stage) cudaFreeHost(h.h_stage);
     tc_free(h);
     delete ph;
     return cuda_fail(e, "psgd_init");
   }
-  const size_t B = h.B, J = h.J, W = h.W;
-  char* base = h.d_table;
-  h.tab.g = reinterpret_cast<const void* const*>(base);
-  h.tab.e = reinterpret_cast<void* const*>(base + 8 * B * J * W);
-  h.tab.q = reinterpret_cast<float* const*>(base + 16 * B * J * W);
-  h.tab.ghat = reinterpret_cast<float* const*>(base + 16 * B * J * W + 8 * B * J);
-  h.tab.unc_in = reinterpret_cast<const float* const*>(base + 16 * B * J * W + 16 * B * J);
-  h.tab.unc_out = reinterpret_cast<float* const*>(base + 16 * B * J * W + 16 * B * J + 8 * B * W);
-  h.tab.inv_scale = reinterpret_cast<const float*>(base + 16 * B * J * W + 16 * B * J + 8 * B * W + 8 * B);
-  h.tab.ge_maps = h.maps_bytes ? base + h.table_bytes : nullptr;
   *out = ph;
   return PSGD_OK;
 }
@@ -399,17 +395,29 @@ static psgd_status prepare_step(psgd_handle* ph, const psgd_step_args* a, void* 
     const float inv = dev_scales ? 0.0f : (float)(1.0 / (double)a->scales[b]);
     std::memcpy(o + 4 * b, &inv, 4);
   }
-  if (!h.have_table || tab != h.last_table) {
-    if (h.have_table && (e = cudaEventSynchronize(h.upload_ev)) != cudaSuccess) return cuda_fail(e, "table event");
-    std::memcpy(h.h_stage, tab.data(), h.table_bytes);
-    if (h.maps_bytes && !tc_encode_ge_maps(h, a->grads, a->errs, a->ghat, h.h_stage + h.table_bytes))
+  int slot = -1;
+  for (int k = 0; k < Handle::kTableSlots && slot < 0; ++k)
+    if (h.slot_used[k] && h.slot_key[k] == tab) slot = k;
+  if (slot < 0) {  // a new table: the least recently used slot takes it
+    slot = 0;
+    for (int k = 1; k < Handle::kTableSlots; ++k)
+      if (h.slot_used[k] < h.slot_used[slot]) slot = k;
+    char* stage = h.h_stage + (size_t)slot * h.table_stride;
+    // The slot's staging buffer may still feed its previous upload (stream order keeps the
+    // device copy from overwriting a table that an earlier step still reads).
+    if (h.slot_used[slot] && (e = cudaEventSynchronize(h.slot_ev[slot])) != cudaSuccess)
+      return cuda_fail(e, "table event");
+    std::memcpy(stage, tab.data(), h.table_bytes);
+    if (h.maps_bytes && !tc_encode_ge_maps(h, a->grads, a->errs, a->ghat, stage + h.table_bytes))
       return fail(PSGD_ECUDA, "cuTensorMapEncodeTiled failed for a gradient or error buffer");
-    if ((e = cudaMemcpyAsync(h.d_table, h.h_stage, h.table_bytes + h.maps_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    if ((e = cudaMemcpyAsync(h.d_table + (size_t)slot * h.table_stride, stage, h.table_bytes + h.maps_bytes,
+                             cudaMemcpyHostToDevice, s)) != cudaSuccess)
       return cuda_fail(e, "table upload");
-    if ((e = cudaEventRecord(h.upload_ev, s)) != cudaSuccess) return cuda_fail(e, "table event");
-    h.last_table.swap(tab);
-    h.have_table = true;
+    if ((e = cudaEventRecord(h.slot_ev[slot], s)) != cudaSuccess) return cuda_fail(e, "table event");
+    h.slot_key[slot].swap(tab);
+    ++h.table_uploads;
   }
+  h.slot_used[slot] = ++h.table_clock;
 
   p = Plan{};
   p.B = h.B; p.J = h.J; p.W = h.W; p.r = h.r; p.rp = h.rp;
@@ -418,7 +426,17 @@ static psgd_status prepare_step(psgd_handle* ph, const psgd_step_args* a, void* 
   p.unc_len = h.cfg.unc_len;
   p.meta = h.d_meta;
   p.threshold = h.d_threshold;
-  p.tab = h.tab;
+  {
+    const char* base = h.d_table + (size_t)slot * h.table_stride;
+    p.tab.g = reinterpret_cast<const void* const*>(base);
+    p.tab.e = reinterpret_cast<void* const*>(base + 8 * B * J * W);
+    p.tab.q = reinterpret_cast<float* const*>(base + 16 * B * J * W);
+    p.tab.ghat = reinterpret_cast<float* const*>(base + 16 * B * J * W + 8 * B * J);
+    p.tab.unc_in = reinterpret_cast<const float* const*>(base + 16 * B * J * W + 16 * B * J);
+    p.tab.unc_out = reinterpret_cast<float* const*>(base + 16 * B * J * W + 16 * B * J + 8 * B * W);
+    p.tab.inv_scale = reinterpret_cast<const float*>(base + 16 * B * J * W + 16 * B * J + 8 * B * W + 8 * B);
+    p.tab.ge_maps = h.maps_bytes ? base + h.table_bytes : nullptr;
+  }
   if (dev_scales) p.tab.inv_scale = h.d_inv_dev;  // formed below, before the ingest
   p.counts = a->counts;
   p.skip = a->skip;
@@ -656,7 +674,8 @@ psgd_status psgd_check(psgd_handle* ph, void* stream) {
 psgd_status psgd_finalize(psgd_handle* ph) {
   if (!ph) return PSGD_OK;
   Handle& h = ph->h;
-  if (h.upload_ev) { cudaEventSynchronize(h.upload_ev); cudaEventDestroy(h.upload_ev); }
+  for (int k = 0; k < Handle::kTableSlots; ++k)
+    if (h.slot_ev[k]) { cudaEventSynchronize(h.slot_ev[k]); cudaEventDestroy(h.slot_ev[k]); }
   if (h.h_stage) cudaFreeHost(h.h_stage);
   destroy_profile(h);
   tc_free(h);

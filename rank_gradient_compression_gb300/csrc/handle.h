@@ -41,14 +41,19 @@ struct Handle {
   int64_t ingest_ctas = 0;
   int64_t unc_cta_start = 0;  // first CTA of the gains/biases segments
 
-  // per-step pointer table
+  // Per-step pointer tables (and the TMA maps of G and E), cached in kTableSlots device
+  // slots keyed by their host bytes, so that buffer sets used in turn are encoded and
+  // uploaded once. Slot k: device bytes at d_table + k * table_stride, pinned staging at
+  // h_stage + k * table_stride, upload event, key, last use.
+  static constexpr int kTableSlots = 4;
   char* d_table = nullptr;
-  size_t table_bytes = 0;
-  char* h_stage = nullptr;  // pinned
-  std::vector<char> last_table;
-  cudaEvent_t upload_ev = nullptr;
-  bool have_table = false;
-  StepTable tab{};
+  size_t table_bytes = 0, table_stride = 0;
+  char* h_stage = nullptr;  // pinned, kTableSlots * table_stride
+  std::vector<char> slot_key[kTableSlots];
+  cudaEvent_t slot_ev[kTableSlots] = {};
+  int64_t slot_used[kTableSlots] = {};  // step counter at last use; 0: empty
+  int64_t table_clock = 0;
+  int64_t table_uploads = 0;            // uploads so far (a test reads it)
 
   int* d_err = nullptr;
   float* d_scal_all = nullptr;  // [B*J*kScalWords] scaling words, zeroed every step

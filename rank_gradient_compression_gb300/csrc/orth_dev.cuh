@@ -76,8 +76,20 @@ __device__ __forceinline__ void gram_block_rows(const float (*Xs)[128], int bi, 
   }
 }
 
+// The whole 8 x 8 block, as two 16-byte stores per row when the pitch allows (rp is a
+// multiple of 16 in the step). Entries past r or below the diagonal are sums like the
+// others and are never read; rows and columns stay below rp (8 ceil(r / 8) <= rp).
 __device__ __forceinline__ void gram_block_store(float* out, const float (&acc)[8][8], int bi,
                                                  int bj, int r, int rp) {
+  if ((rp & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0 && bj * 8 + 8 <= rp && bi * 8 + 8 <= rp) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float* row = out + (size_t)(bi * 8 + i) * rp + bj * 8;
+      *reinterpret_cast<float4*>(row) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4*>(row + 4) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int ii = bi * 8 + i;
@@ -234,195 +246,171 @@ __device__ void gsum_item(const Plan& p, const MatMeta& mt, int blk, float (*par
 }
 
 // ---------------------------------------------------------------- Cholesky + R^-1
-// One CTA of kCholWarps warps per matrix. The Gram matrix lives in registers: warp w owns
-// the 8-row panel [8w, 8w + 8), and lane l holds columns l, l + 32, l + 64, l + 96 of
-// those rows. r <= 128, so every row has an owner.
+// One CTA of kCholWarps warps per matrix; r <= 128. The Gram matrix G sits in shared
+// memory as A (both triangles), next to Z = I.
 //
-// Factorisation G = R^T R (right-looking, by panels): the owner warp factors its panel
-// with shuffles only and writes the panel's 8 rows of R to shared memory; after one
-// block barrier every later warp subtracts the rank-8 update from its rows. Pivot k is
-// dead when it is <= dead_tol * diag0[k] (or not finite): row k of R becomes e_k and
-// column k takes no part in later updates.
-//
-// R^-1 in the same sweep: elimination on [G | I] turns the identity into L^-1 = R^-T with
-// L = R^T. Each warp also holds its rows of Z (initially I) in registers; the owner warp
-// scales its Z rows by 1/r_kk and updates them with the same multipliers as its G rows,
-// publishes them next to the R rows, and the later warps subtract the same multiples
-// from their Z rows. R^-1 = Z^T. One block barrier per 8 rows in all.
+// Factorisation G = R^T R, right-looking by panels of 8 pivots, two block barriers per
+// panel:
+//  1. Each of the 128 threads of warps 0..3 factors the panel's 8 x 8 diagonal block in
+//     its registers (all alike: no shuffle and no barrier on the chain of the 8 pivots).
+//     Pivot k is dead when it is <= dead_tol * diag0[k] (or not finite): row k of R
+//     becomes e_k and column k takes no part in later updates.
+//  2. The same threads solve for the panel's rows, one column each: R[k0+t][j] for j right
+//     of the block (row t loses R[k0+s][k0+t] times the finished row s < t, then is
+//     scaled by 1 / r_tt), and the panel's rows of Z with the same multipliers.
+//     Elimination on [G | I] turns I into L^-1 = R^-T (L = R^T), so R^-1 = Z^T.
+//  3. Every warp subtracts the rank-8 update from the rows below the panel, one row per
+//     warp at a time. Lane q owns the column quad [4q, 4q + 4) of [Z | A]: Z left of the
+//     panel's end (Z is lower triangular), A from there on (upper triangle only). It
+//     keeps the panel's 8 entries of its quad in registers for the whole panel.
 constexpr int kCholWarps = 16;
 constexpr int kCholThreads = kCholWarps * 32;
 constexpr int kPanel = 8;
-static_assert(kCholWarps * kPanel >= kRankBlock, "every row needs an owner warp");
-constexpr int kRsLd = kRankBlock + 1;  // row stride of R in shared memory
+constexpr int kCLd = kRankBlock + 4;  // row pitch of A and Z in shared memory (16-byte rows)
+static_assert(kRankBlock == 128 && kCholThreads >= kRankBlock, "one column per solver thread");
 
 struct CholSmem {
-  float R[kRankBlock * kRsLd];           // rows of R as they are finished
-  float X[2][kPanel * kRsLd];          // published rows of Z = R^-T (ping-pong by panel)
-  float diag0[kRankBlock];               // diagonal of the unshifted Gram matrix
-  float ratio[kRankBlock];               // pivot / diag0 (0 for dead pivots)
+  float A[kRankBlock * kCLd];  // G, rows turning into R
+  float Z[kRankBlock * kCLd];  // I, rows turning into Z = R^-T
+  float diag0[kRankBlock];     // diagonal of the unshifted Gram matrix
+  float ratio[kRankBlock];     // pivot / diag0 (0 for dead pivots)
   int dead[kRankBlock];
-  float trace, maxr, minr, minratio;    // block-wide scalars of one factorisation
+  float trace, maxr, minr, minratio;  // block-wide scalars of one factorisation
   int ndead;
 };
 
-// Warp w holds rows i in [8w, 8w + 8) of G (becoming R) in a[t][q] and of Z = R^-T in
-// z[t][q], column j = lane + 32 q. One code body for every warp, with the loops that
-// only address shared memory kept rolled: a per-warp specialisation of the register
-// arrays would be smaller in arithmetic but overflows the instruction cache.
-__device__ __forceinline__ float sel4(const float (&v)[4], int q) {  // q warp-uniform
-  return q == 0 ? v[0] : q == 1 ? v[1] : q == 2 ? v[2] : v[3];
-}
-
-__device__ __forceinline__ void load_gram_rows(const MatMeta& mt, int r, int rp,
-                                               float (&a)[kPanel][4], float shift, CholSmem& S,
-                                               bool record) {
+// A = G + shift I and Z = I on the leading r x r block, zeros elsewhere. The Gram sum holds
+// the upper triangle; each thread mirrors the entries it loads.
+__device__ __forceinline__ void chol_load(const MatMeta& mt, int r, int rp, float shift, CholSmem& S,
+                                          bool record) {
   const float* src = mt.Gpart + (size_t)mt.C * rp * rp;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int t = 0; t < kPanel; ++t) {  // all loads first (upper triangle)
-    const int i = warp * kPanel + t;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int j = lane + 32 * q;
-      a[t][q] = (i < r && j < r && j >= i) ? __ldcg(src + (size_t)i * rp + j) : 0.f;
+  for (int idx = threadIdx.x; idx < kRankBlock * kRankBlock; idx += kCholThreads) {
+    const int i = idx >> 7, j = idx & 127;
+    S.Z[i * kCLd + j] = (i == j && i < r) ? 1.f : 0.f;
+    if (j >= i) {
+      float g = j < r ? __ldcg(src + (size_t)i * rp + j) : 0.f;
+      if (i == j && i < r) {
+        if (record) S.diag0[i] = g;
+        g += shift;
+      }
+      S.A[i * kCLd + j] = g;
+      S.A[j * kCLd + i] = g;
     }
   }
-  const int qw = warp >> 2;  // the diagonal of row i sits in group i / 32 = warp / 4
+}
+
+// Steps 1 and 2 for the panel at k0 (kb <= 8 pivots); threads 0..127, column c = thread.
+__device__ __forceinline__ void chol_panel_solve(int k0, int kb, int r, float dead_tol, CholSmem& S) {
+  float D[kPanel][kPanel];
+#pragma unroll
+  for (int s = 0; s < kPanel; ++s)
+#pragma unroll
+    for (int t = 0; t < kPanel; ++t) D[s][t] = (t >= s && t < kb) ? S.A[(k0 + s) * kCLd + k0 + t] : 0.f;
+  float inv[kPanel];
+  bool dead[kPanel];
 #pragma unroll
   for (int t = 0; t < kPanel; ++t) {
-    const int i = warp * kPanel + t;
-    if (i < r && lane == (i & 31)) {
+    inv[t] = 1.f;
+    dead[t] = true;
+    if (t < kb) {
+      const float d = D[t][t];
+      const float d0 = S.diag0[k0 + t];
+      const bool bad = !(d > dead_tol * d0) || !isfinite(d) || !(d0 > 0.f);
+      const float iv = bad ? 1.f : rsqrtf(d);
+      inv[t] = iv;
+      dead[t] = bad;
+      D[t][t] = bad ? 1.f : d * iv;  // r_kk
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (q == qw) {
-          if (record) S.diag0[i] = a[t][q];
-          a[t][q] += shift;
-        }
+      for (int u = t + 1; u < kPanel; ++u) D[t][u] = bad ? 0.f : D[t][u] * iv;  // R[k0+t][k0+u]
+#pragma unroll
+      for (int u = t + 1; u < kPanel; ++u)
+#pragma unroll
+        for (int v = u; v < kPanel; ++v) D[u][v] = fmaf(-D[t][u], D[t][v], D[u][v]);
+      if (threadIdx.x == 0) {
+        S.dead[k0 + t] = bad;
+        S.ratio[k0 + t] = bad ? 0.f : __fdividef(d, d0);  // statistics only
+      }
     }
+  }
+  const int c = threadIdx.x;
+  if (c < k0 + kPanel && c < r) {  // the panel's rows of Z (lower triangular: columns <= k0 + 7)
+    float x[kPanel];
+#pragma unroll
+    for (int t = 0; t < kPanel; ++t) x[t] = t < kb ? S.Z[(k0 + t) * kCLd + c] : 0.f;
+#pragma unroll
+    for (int t = 0; t < kPanel; ++t) {
+#pragma unroll
+      for (int s2 = 0; s2 < t; ++s2) x[t] = fmaf(-D[s2][t], x[s2], x[t]);
+      x[t] *= inv[t];
+    }
+#pragma unroll
+    for (int t = 0; t < kPanel; ++t)
+      if (t < kb) S.Z[(k0 + t) * kCLd + c] = x[t];
+  }
+  if (c >= k0 && c < r) {  // the panel's rows of R
+    float x[kPanel];
+    if (c < k0 + kPanel) {  // inside the diagonal block: the factor itself
+      const int cu = c - k0;
+#pragma unroll
+      for (int t = 0; t < kPanel; ++t) {
+        float v = 0.f;
+#pragma unroll
+        for (int u = 0; u < kPanel; ++u)
+          if (u == cu && u >= t) v = D[t][u];
+        x[t] = v;
+      }
+    } else {  // right of it: forward substitution with the block's R
+#pragma unroll
+      for (int t = 0; t < kPanel; ++t) x[t] = t < kb ? S.A[(k0 + t) * kCLd + c] : 0.f;
+#pragma unroll
+      for (int t = 0; t < kPanel; ++t) {
+#pragma unroll
+        for (int s2 = 0; s2 < t; ++s2) x[t] = fmaf(-D[s2][t], x[s2], x[t]);
+        x[t] = dead[t] ? 0.f : x[t] * inv[t];
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kPanel; ++t)
+      if (t < kb) S.A[(k0 + t) * kCLd + c] = x[t];
   }
 }
 
-__device__ __forceinline__ void identity_rows(float (&z)[kPanel][4]) {
+// Step 3 for the panel at k0: rows i >= k0 + 8 of A (upper triangle) and Z lose
+// sum_t R[k0+t][i] times the panel's row t.
+__device__ __forceinline__ void chol_trailing_update(int k0, int kb, int r, CholSmem& S) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kend = k0 + kPanel, c0 = 4 * lane;
+  if (kend >= r || c0 >= r) return;
+  const bool zq = c0 < kend;
+  float* M = zq ? S.Z : S.A;
+  float4 pv[kPanel];
 #pragma unroll
   for (int t = 0; t < kPanel; ++t)
+    pv[t] = t < kb ? *reinterpret_cast<const float4*>(&M[(k0 + t) * kCLd + c0]) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = kend + warp; i < r; i += kCholWarps) {
+    if (!zq && c0 + 3 < i) continue;  // wholly below the diagonal of A
+    float4 v = *reinterpret_cast<const float4*>(&M[i * kCLd + c0]);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) z[t][q] = (warp * kPanel + t == lane + 32 * q) ? 1.f : 0.f;
+    for (int t = 0; t < kPanel; ++t) {
+      const float cf = S.A[(k0 + t) * kCLd + i];  // R[k0+t][i] (0 past kb: pv is 0 there too)
+      v.x = fmaf(-cf, pv[t].x, v.x);
+      v.y = fmaf(-cf, pv[t].y, v.y);
+      v.z = fmaf(-cf, pv[t].z, v.z);
+      v.w = fmaf(-cf, pv[t].w, v.w);
+    }
+    *reinterpret_cast<float4*>(&M[i * kCLd + c0]) = v;
+  }
 }
 
-// Factor the registers' panels in place (a: rows of G -> R; z: rows of I -> Z = R^-T) and
-// fill S.R, S.dead, S.ratio.
-__device__ void cholesky_panels(float (&a)[kPanel][4], float (&z)[kPanel][4], int r,
-                                float dead_tol, CholSmem& S) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ void chol_factor(int r, float dead_tol, CholSmem& S) {
   const int npan = (r + kPanel - 1) / kPanel;
   for (int pn = 0; pn < npan; ++pn) {
-    const int k0 = pn * kPanel;
-    const int qg = pn >> 2;  // column group of this panel's pivots
-    float* Zp = S.X[pn & 1];
-    if (warp == pn) {  // the owner
-      // The panel's 8 x 8 diagonal block reaches every lane in one round of shuffles
-      // (upper triangle; columns k0.. sit in group qg at lanes l0..l0+7), and every lane
-      // factors it in registers: no shuffle lies on the chain of the 8 pivots.
-      const int nk = min(kPanel, r - k0);
-      const int l0 = k0 & 31;
-      float D[kPanel][kPanel];
-#pragma unroll
-      for (int s = 0; s < kPanel; ++s) {
-        const float v = sel4(a[s], qg);
-#pragma unroll
-        for (int t = s; t < kPanel; ++t) D[s][t] = __shfl_sync(0xffffffffu, v, l0 + t);
-      }
-      float inv[kPanel];
-      bool dead[kPanel];
-#pragma unroll
-      for (int t = 0; t < kPanel; ++t) {
-        inv[t] = 1.f;
-        dead[t] = true;
-        if (t < nk) {
-          const float d = D[t][t];
-          const float d0 = S.diag0[k0 + t];
-          const bool bad = !(d > dead_tol * d0) || !isfinite(d) || !(d0 > 0.f);
-          const float iv = bad ? 1.f : rsqrtf(d);
-          inv[t] = iv;
-          dead[t] = bad;
-          D[t][t] = bad ? 1.f : d * iv;  // r_kk
-#pragma unroll
-          for (int u = t + 1; u < kPanel; ++u) D[t][u] = bad ? 0.f : D[t][u] * iv;  // R[t][u]
-#pragma unroll
-          for (int u = t + 1; u < kPanel; ++u)
-#pragma unroll
-            for (int v = u; v < kPanel; ++v) D[u][v] = fmaf(-D[t][u], D[t][v], D[u][v]);
-          if (lane == 0) {
-            S.dead[k0 + t] = bad;
-            S.ratio[k0 + t] = bad ? 0.f : __fdividef(d, d0);  // statistics only
-          }
-        }
-      }
-      // The panel's rows of R and Z by forward substitution with the block's R: row t
-      // loses R[s][t] times the finished row s (s < t), then is scaled by 1 / r_tt. These
-      // are the right-looking panel updates, in the same order.
-#pragma unroll
-      for (int t = 0; t < kPanel; ++t) {
-        if (t < nk) {
-          const int k = k0 + t;
-#pragma unroll
-          for (int s2 = 0; s2 < t; ++s2) {
-            const float c = D[s2][t];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              a[t][q] = fmaf(-c, a[s2][q], a[t][q]);
-              z[t][q] = fmaf(-c, z[s2][q], z[t][q]);
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int j = lane + 32 * q;
-            a[t][q] = j < k ? 0.f : (j == k ? D[t][t] : (dead[t] ? 0.f : a[t][q] * inv[t]));
-            z[t][q] *= inv[t];
-          }
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kPanel; ++t)
-        if (k0 + t < r) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            S.R[(k0 + t) * kRsLd + lane + 32 * q] = a[t][q];
-            Zp[t * kRsLd + lane + 32 * q] = z[t][q];
-          }
-        }
-    }
+    const int k0 = pn * kPanel, kb = min(kPanel, r - k0);
+    if (threadIdx.x < kRankBlock) chol_panel_solve(k0, kb, r, dead_tol, S);
     __syncthreads();
-    if (warp > pn && warp * kPanel < r) {  // warps whose rows all lie past r have nothing to update
-      const int kend = min(kPanel, r - k0);
-      const int i0 = warp * kPanel;
-      // Only columns j >= i0 of G's rows matter (upper triangle), and Z = R^-T's rows are 0
-      // past column i0 + 7 (lower triangle, from identity rows). Both limits fall in column
-      // group qa = i0 / 32, so G's groups below qa and Z's groups above it are left as
-      // they are: 5 of the 8 groups are updated.
-      const int qa = i0 >> 5;
-#pragma unroll 1
-      for (int pp = 0; pp < kend; ++pp) {
-        const float* Rk = S.R + (k0 + pp) * kRsLd;
-        const float* Zk = Zp + pp * kRsLd;
-        float rj[4], zj[4], c[kPanel];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          rj[q] = q >= qa ? Rk[lane + 32 * q] : 0.f;
-          zj[q] = q <= qa ? Zk[lane + 32 * q] : 0.f;
-        }
-#pragma unroll
-        for (int t = 0; t < kPanel; ++t) c[t] = Rk[i0 + t];
-#pragma unroll
-        for (int t = 0; t < kPanel; ++t) {  // rows i >= r hold zeros and stay unused
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (q >= qa) a[t][q] = fmaf(-c[t], rj[q], a[t][q]);
-            if (q <= qa) z[t][q] = fmaf(-c[t], zj[q], z[t][q]);
-          }
-        }
-      }
+    if (k0 + kPanel < r) {
+      chol_trailing_update(k0, kb, r, S);
+      __syncthreads();
     }
   }
 }
@@ -437,9 +425,7 @@ __device__ void chol_matrix(const Plan& p, const MatMeta& mt, int pass, CholSmem
   int* st = mt.ostate + pass * 4;
   const int src = pass == 0 ? 0 : ld_int(mt.ostate + (pass - 1) * 4 + 1);
 
-  float a[kPanel][4], z[kPanel][4];
-  identity_rows(z);
-  load_gram_rows(mt, r, rp, a, 0.f, S, true);
+  chol_load(mt, r, rp, 0.f, S, true);
   __syncthreads();
   if (warp == 0) {  // trace: fixed-order warp reduction
     float t = 0.f;
@@ -453,25 +439,19 @@ __device__ void chol_matrix(const Plan& p, const MatMeta& mt, int pass, CholSmem
   bool shifted = false;
   if (!(trace > 0.f) || !isfinite(trace)) {
     for (int k = threadIdx.x; k < r; k += blockDim.x) { S.dead[k] = 1; S.ratio[k] = 0.f; }
-    for (int idx = threadIdx.x; idx < r * kRsLd; idx += blockDim.x) {
-      const int i = idx / kRsLd, j = idx - i * kRsLd;
-      S.R[idx] = (i == j) ? 1.f : 0.f;
-    }
     __syncthreads();
   } else {
-    cholesky_panels(a, z, r, last ? 0x1p-40f : 0x1p-16f, S);
-    __syncthreads();
+    chol_factor(r, last ? 0x1p-40f : 0x1p-16f, S);
     int nd = 0;
     for (int k = lane; k < r; k += 32) nd += S.dead[k];
     nd = __reduce_add_sync(0xffffffffu, nd);  // every warp computes the same count
     if (nd > 0 && !last) {
       shifted = true;
       const float shift = 0x1p-20f * sqrtf((float)mt.m) * trace;
-      load_gram_rows(mt, r, rp, a, shift, S, false);
-      identity_rows(z);
+      __syncthreads();  // every warp has read the dead flags
+      chol_load(mt, r, rp, shift, S, false);
       __syncthreads();
-      cholesky_panels(a, z, r, 0x1p-40f, S);
-      __syncthreads();
+      chol_factor(r, 0x1p-40f, S);
     }
   }
   // statistics of the factor: warp 0 reduces over the pivots
@@ -480,7 +460,7 @@ __device__ void chol_matrix(const Plan& p, const MatMeta& mt, int pass, CholSmem
     int nd = 0;
     for (int k = lane; k < r; k += 32) {
       if (S.dead[k]) { ++nd; continue; }
-      const float d = S.R[k * kRsLd + k];
+      const float d = S.A[k * kCLd + k];
       mx = fmaxf(mx, d); mn = fminf(mn, d); mr = fminf(mr, S.ratio[k]);
     }
 #pragma unroll
@@ -492,35 +472,29 @@ __device__ void chol_matrix(const Plan& p, const MatMeta& mt, int pass, CholSmem
     nd = __reduce_add_sync(0xffffffffu, nd);
     if (lane == 0) { S.maxr = mx; S.minr = mn; S.minratio = mr; S.ndead = nd; }
   }
-  // R^-1 = Z^T to global, dead columns zeroed: this warp's Z rows j = 8 warp + t are R^-1's
-  // columns j, so each thread holds 8 consecutive entries of R^-1 rows i = lane + 32 q,
-  // written as two 16-byte stores when the pitch and the base allow.
+  // R^-1 = Z^T to global, dead columns zeroed: R^-1[i][j] = Z[j][i] for j >= i, 0 below
+  // the diagonal; r x r entries, four consecutive columns per thread.
   float* Ri = mt.Rinv;
-  const int j0 = warp * kPanel;
-  if (j0 < r) {
-    bool live[kPanel];
+  const bool vec = (rp & 3) == 0 && (reinterpret_cast<uintptr_t>(Ri) & 15) == 0;
+  const int nq = (r + 3) / 4;
+  for (int idx = threadIdx.x; idx < r * nq; idx += blockDim.x) {
+    const int i = idx / nq, j0 = 4 * (idx - i * nq);
+    float v[4];
 #pragma unroll
-    for (int t = 0; t < kPanel; ++t) live[t] = j0 + t < r && S.dead[j0 + t] == 0;
-    const bool vec = j0 + kPanel <= r && (rp & 3) == 0 &&
-                     (reinterpret_cast<uintptr_t>(Ri) & 15) == 0;
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      v[u] = (j < r && j >= i && S.dead[j] == 0) ? S.Z[j * kCLd + i] : 0.f;
+    }
+    float* row = Ri + (size_t)i * rp + j0;
+    if (vec && j0 + 4 <= rp) {
+      *reinterpret_cast<float4*>(row) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int i = lane + 32 * q;
-      if (i >= r) continue;
-      float v[kPanel];
-#pragma unroll
-      for (int t = 0; t < kPanel; ++t) v[t] = (i <= j0 + t && live[t]) ? z[t][q] : 0.f;
-      float* row = Ri + (size_t)i * rp + j0;
-      if (vec) {
-        *reinterpret_cast<float4*>(row) = make_float4(v[0], v[1], v[2], v[3]);
-        *reinterpret_cast<float4*>(row + 4) = make_float4(v[4], v[5], v[6], v[7]);
-      } else {
-#pragma unroll
-        for (int t = 0; t < kPanel; ++t)
-          if (j0 + t < r) row[t] = v[t];
-      }
+      for (int u = 0; u < 4; ++u)
+        if (j0 + u < r) row[u] = v[u];
     }
   }
+  __syncthreads();  // the statistics of warp 0
   if (threadIdx.x == 0) {
     const bool nearly_orth = !shifted && S.ndead == 0 && S.minratio >= 0.5f &&
                              S.maxr <= 2.f * S.minr;

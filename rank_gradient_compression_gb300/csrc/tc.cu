@@ -394,60 +394,70 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The issue loop between two MMAs is kept to a few integer adds: the descriptors of a
+    // stage are its base descriptor plus constant offsets (in 16-byte units), ring slots and
+    // segment ends are counters. Each tcgen05.mma waits until the tensor pipe takes it, so
+    // the work between two of them adds to every MMA's time.
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(BM, rp, BF16, MN_A, false);
-      uint32_t ia = 0, ib = 0, ju = 0;
+      const uint64_t a_base = MN_A ? smem_desc(smem_u32(S.a(0)), a_bytes / 2, 1024) : smem_desc(smem_u32(S.a(0)), 16, 1024);
+      const uint64_t b_base = smem_desc(smem_u32(S.b(0, b_stage)), 16, 1024);
+      const uint32_t a_stage16 = a_bytes >> 4, b_stage16 = b_stage >> 4, b_tile16 = b_tile >> 4;
+      const uint32_t term16 = (uint32_t)rp * 8;  // rp rows of 128 bytes
+      uint32_t sa = 0, pa = 0, sb = 0, pb = 0, ju = 0;
       bool ok = true;
       for (int u = u_first; u < u_end && ok; u += u_step) {
         const Unit un = units[u];
         if (unit_off(p, p.meta[un.t], only_shifted)) continue;
-        const int nsteps = (un.kb1 - un.kb0) * p.W;
-        int step = 0, acc = 0;
+        int steps_left = (un.kb1 - un.kb0) * p.W, seg_left = 0, acc = 0;
         uint32_t d_tmem = tmem_base, accum = 0;
         for (int kb = un.kb0; kb < un.kb1 && ok; kb += kps) {
           const int nk = min(kps, un.kb1 - kb);
-          const int sb = ib % B_STAGES;
-          ok = mbar_wait(&sm.full_b[sb], (ib / B_STAGES) & 1, err);
+          ok = mbar_wait(&sm.full_b[sb], pb, err);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t b_addr = smem_u32(S.b(sb, b_stage));
+          const uint64_t bd = b_base + (uint64_t)(sb * b_stage16);
           for (int w = 0; w < p.W && ok; ++w) {
-            const int sa = ia % A_STAGES;
-            ok = mbar_wait(&sm.full_a[sa], (ia / A_STAGES) & 1, err);
+            ok = mbar_wait(&sm.full_a[sa], pa, err);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(S.a(sa));
-            for (int h = 0; h < nk; ++h) {  // one step per k-block of the stage
-              if (step % seg == 0) {  // open an accumulator segment
-                acc = (int)(ju % NACC);
-                ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
-                if (!ok) break;
-                tc_fence_after();
-                d_tmem = tmem_base + (uint32_t)acc * kAccCols;
-                accum = 0;
-              }
+            const uint64_t ad = a_base + (uint64_t)(sa * a_stage16);
 #pragma unroll
-              for (int k = 0; k < BK / 16; ++k) {
-                // MN-major A: 64 x (64 kps)-row boxes, k-block h at h * 64 rows of 128 bytes
-                const uint64_t adesc = MN_A ? smem_desc(a_addr + h * 8192 + k * 2048, a_bytes / 2, 1024)
-                                            : smem_desc(a_addr + k * 32, 16, 1024);
-#pragma unroll
-                for (int tm = 0; tm < TERMS; ++tm) {  // B rows [tm rp, (tm + 1) rp): term tm
-                  umma_f16(d_tmem, adesc, smem_desc(b_addr + h * b_tile + tm * rp * 128 + k * 32, 16, 1024),
-                           idesc, accum);
-                  accum = 1;
+            for (int h = 0; h < 2; ++h) {  // one step per k-block of the stage
+              if (h < nk && ok) {
+                if (seg_left == 0) {  // open an accumulator segment
+                  acc = (int)(ju % NACC);
+                  ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
+                  if (!ok) break;
+                  tc_fence_after();
+                  d_tmem = tmem_base + (uint32_t)acc * kAccCols;
+                  accum = 0;
+                  seg_left = seg;
                 }
-              }
-              if (++step % seg == 0 || step == nsteps) {  // close the segment
-                umma_commit(&sm.acc_full[acc]);
-                ++ju;
+                const uint64_t bdh = bd + (uint64_t)(h * b_tile16);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                  // MN-major A: 64 x (64 kps)-row boxes, k-block h at h * 64 rows of 128 bytes
+                  const uint64_t adk = ad + (uint64_t)(MN_A ? (h * 8192 + k * 2048) >> 4 : (k * 32) >> 4);
+#pragma unroll
+                  for (int tm = 0; tm < TERMS; ++tm) {  // B rows [tm rp, (tm + 1) rp): term tm
+                    umma_f16(d_tmem, adk, bdh + (uint64_t)(tm * term16 + k * 2), idesc, accum);
+                    accum = 1;
+                  }
+                }
+                --steps_left;
+                if (--seg_left == 0 || steps_left == 0) {  // close the segment
+                  umma_commit(&sm.acc_full[acc]);
+                  ++ju;
+                  seg_left = 0;
+                }
               }
             }
             umma_commit(&sm.empty_a[sa]);
-            ++ia;
+            if (++sa == (uint32_t)A_STAGES) { sa = 0; pa ^= 1; }
           }
           umma_commit(&sm.empty_b[sb]);
-          ++ib;
+          if (++sb == (uint32_t)B_STAGES) { sb = 0; pb ^= 1; }
         }
       }
       umma_commit(&sm.done);
@@ -694,52 +704,54 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Between two MMAs only integer adds (descriptor = stage base + constant offset), as in
+    // the separate GEMM kernel.
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(BM, rp, BF16, false, false);
-      uint32_t ia = 0, ib = 0, ju = 0;
+      const uint64_t a_base = smem_desc(smem_u32(a0), 16, 1024), b_base = smem_desc(smem_u32(b0), 16, 1024);
+      const uint32_t b_stage16 = b_stage >> 4, term16 = (uint32_t)rp * 8;
+      uint32_t sa = 0, pa = 0, sb = 0, pb = 0, ju = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
         const Unit un = units[u];
-        const int nsteps = (un.kb1 - un.kb0) * p.W;
-        int step = 0, acc = 0;
+        int steps_left = (un.kb1 - un.kb0) * p.W, seg_left = 0, acc = 0;
         uint32_t d_tmem = tmem_base, accum = 0;
         for (int w = 0; w < p.W && ok; ++w) {
           for (int kb = un.kb0; kb < un.kb1 && ok; ++kb) {
-            const int sb = ib % B_STAGES;
-            ok = mbar_wait(&sm.full_b[sb], (ib / B_STAGES) & 1, err);
+            ok = mbar_wait(&sm.full_b[sb], pb, err);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t b_addr = smem_u32(b0 + (size_t)sb * b_stage);
-            if (step % seg == 0) {  // open an accumulator segment
+            const uint64_t bd = b_base + (uint64_t)(sb * b_stage16);
+            if (seg_left == 0) {  // open an accumulator segment
               acc = (int)(ju % NACC);
               ok = mbar_wait(&sm.acc_empty[acc], ((ju / NACC) & 1) ^ 1, err);
               if (!ok) break;
               tc_fence_after();
               d_tmem = tmem_base + (uint32_t)acc * kAccCols;
               accum = 0;
+              seg_left = seg;
             }
-            const int sa = ia % a_stages;
-            ok = mbar_wait(&sm.full_a[sa], (ia / a_stages) & 1, err);
+            ok = mbar_wait(&sm.full_a[sa], pa, err);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(a0 + (size_t)sa * A_BYTES);
+            const uint64_t ad = a_base + (uint64_t)(sa * (A_BYTES >> 4));
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              const uint64_t adesc = smem_desc(a_addr + k * 32, 16, 1024);
 #pragma unroll
               for (int tm = 0; tm < TERMS; ++tm) {  // B rows [tm rp, (tm + 1) rp): term tm of Q
-                umma_f16(d_tmem, adesc, smem_desc(b_addr + tm * rp * 128 + k * 32, 16, 1024), idesc,
-                         accum);
+                umma_f16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(tm * term16 + k * 2), idesc, accum);
                 accum = 1;
               }
             }
             umma_commit(&sm.empty_a[sa]);
             umma_commit(&sm.empty_b[sb]);
-            ++ia;
-            ++ib;
-            if (++step % seg == 0 || step == nsteps) {  // close the segment
+            if (++sa == (uint32_t)a_stages) { sa = 0; pa ^= 1; }
+            if (++sb == (uint32_t)B_STAGES) { sb = 0; pb ^= 1; }
+            --steps_left;
+            if (--seg_left == 0 || steps_left == 0) {  // close the segment
               umma_commit(&sm.acc_full[acc]);
               ++ju;
+              seg_left = 0;
             }
           }
         }
