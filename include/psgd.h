@@ -120,7 +120,8 @@ typedef struct {
   uint32_t* mask_bits;          /* device, only with PSGD_FLAG_MASK (else ignored): one
                                    bit per matrix entry, LSB-first in 32-bit words,
                                    row-major; matrix (b,j,w) starts at word
-                                   psgd_mask_offset(cfg, b, j, w) */
+                                   psgd_mask_offset(cfg, b, j, w). Bits past a matrix's
+                                   last entry in its last word are unspecified. */
   const float* scales_device;   /* [B] device, or NULL: s_b read on the device (the state
                                    psgd_scale_update keeps), so no host round trip sits
                                    between steps. Each s_b must be > 0; it may be below 1

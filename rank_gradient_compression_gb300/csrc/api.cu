@@ -475,9 +475,10 @@ static psgd_status run_step(psgd_handle* ph, const psgd_step_args* a, Plan& p, v
     if (dev_scales) ++h.launches;
     if ((e = cudaMemsetAsync(a->counts, 0, 8 * B * W, s)) != cudaSuccess) return cuda_fail(e, "counts");
     if ((e = cudaMemsetAsync(h.d_scal_all, 0, 4 * kScalWords * B * J, s)) != cudaSuccess) return cuda_fail(e, "scal");
-    // The fused path ingests the gradients and forms the P partial sums in one sweep; the
-    // debug outputs (mask bitmap, stop after ingest) use the separate ingest kernel.
-    const bool fused = h.tc && !(h.cfg.flags & (PSGD_FLAG_MASK | PSGD_FLAG_STOP_AFTER_INGEST));
+    // The fused path ingests the gradients, writes the mask bitmap when asked, and forms
+    // the P partial sums in one sweep; stopping after the ingest (debug) uses the separate
+    // ingest kernel.
+    const bool fused = h.tc && !(h.cfg.flags & PSGD_FLAG_STOP_AFTER_INGEST);
     if (fused) {
       if ((e = launch_prep_q(h, p, s)) != cudaSuccess) return cuda_fail(e, "prep_q");
       if ((e = launch_ingest_p(h, p, s)) != cudaSuccess) return cuda_fail(e, "ingest_p");

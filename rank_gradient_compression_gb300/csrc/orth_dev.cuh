@@ -56,6 +56,13 @@ __device__ __forceinline__ void block_coords(int b, int nb, int& bi, int& bj) {
   bj = i + rem;
 }
 
+// Column c of a row of the Gram staging tile sits at gram_slot(c): the first halves (4
+// columns) of the 8-column blocks side by side, then the second halves. A warp's threads
+// read the halves of up to 14 different blocks of one row, 16 bytes each, and in this
+// order those are consecutive 16-byte words (no bank conflict); in plain column order
+// every fourth block would share banks.
+__device__ __forceinline__ int gram_slot(int c) { return ((c >> 2) & 1) * 64 + (c >> 3) * 4 + (c & 3); }
+
 // acc += rows [q0, q0 + 32) of Xs restricted to columns 8 bi.. x columns 8 bj.., row by
 // row in order.
 __device__ __forceinline__ void gram_block_rows(const float (*Xs)[128], int bi, int bj, int q0,
@@ -63,10 +70,10 @@ __device__ __forceinline__ void gram_block_rows(const float (*Xs)[128], int bi, 
 #pragma unroll 4
   for (int q = q0; q < q0 + 32; ++q) {
     float a[8], b[8];
-    const float4 a0 = *reinterpret_cast<const float4*>(&Xs[q][bi * 8]);
-    const float4 a1 = *reinterpret_cast<const float4*>(&Xs[q][bi * 8 + 4]);
-    const float4 b0 = *reinterpret_cast<const float4*>(&Xs[q][bj * 8]);
-    const float4 b1 = *reinterpret_cast<const float4*>(&Xs[q][bj * 8 + 4]);
+    const float4 a0 = *reinterpret_cast<const float4*>(&Xs[q][bi * 4]);
+    const float4 a1 = *reinterpret_cast<const float4*>(&Xs[q][64 + bi * 4]);
+    const float4 b0 = *reinterpret_cast<const float4*>(&Xs[q][bj * 4]);
+    const float4 b1 = *reinterpret_cast<const float4*>(&Xs[q][64 + bj * 4]);
     a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w; a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
     b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w; b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
 #pragma unroll
@@ -178,7 +185,7 @@ __device__ void gram_chunk(const Plan& p, const MatMeta& mt, int pass, int chunk
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int f = tid + kT * u, rr = f >> 5, c = (f & 31) * 4;
-      *reinterpret_cast<float4*>(&Xs[rr][c]) =
+      *reinterpret_cast<float4*>(&Xs[rr][gram_slot(c)]) =
           make_float4(c < r ? v[u].x * sc : 0.f, c + 1 < r ? v[u].y * sc : 0.f,
                       c + 2 < r ? v[u].z * sc : 0.f, c + 3 < r ? v[u].w * sc : 0.f);
     }
@@ -192,7 +199,7 @@ __device__ void gram_chunk(const Plan& p, const MatMeta& mt, int pass, int chunk
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const int f = tid + kT * u;
-      Xs[f >> 7][f & 127] = v[u] * sc;
+      Xs[f >> 7][gram_slot(f & 127)] = v[u] * sc;
     }
   }
   bar.sync();
@@ -249,20 +256,24 @@ __device__ void gsum_item(const Plan& p, const MatMeta& mt, int blk, float (*par
 // One CTA of kCholWarps warps per matrix; r <= 128. The Gram matrix G sits in shared
 // memory as A (both triangles), next to Z = I.
 //
-// Factorisation G = R^T R, right-looking by panels of 8 pivots, two block barriers per
-// panel:
-//  1. Each of the 128 threads of warps 0..3 factors the panel's 8 x 8 diagonal block in
-//     its registers (all alike: no shuffle and no barrier on the chain of the 8 pivots).
-//     Pivot k is dead when it is <= dead_tol * diag0[k] (or not finite): row k of R
-//     becomes e_k and column k takes no part in later updates.
+// Factorisation G = R^T R, right-looking by panels of 8 pivots:
+//  1. Each of the 128 threads of warps 0..3 (the solver) factors the panel's 8 x 8 diagonal
+//     block in its registers (all alike: no shuffle and no barrier on the chain of the 8
+//     pivots). Pivot k is dead when it is <= dead_tol * diag0[k] (or not finite): row k of
+//     R becomes e_k and column k takes no part in later updates.
 //  2. The same threads solve for the panel's rows, one column each: R[k0+t][j] for j right
 //     of the block (row t loses R[k0+s][k0+t] times the finished row s < t, then is
 //     scaled by 1 / r_tt), and the panel's rows of Z with the same multipliers.
-//     Elimination on [G | I] turns I into L^-1 = R^-T (L = R^T), so R^-1 = Z^T.
-//  3. Every warp subtracts the rank-8 update from the rows below the panel, one row per
-//     warp at a time. Lane q owns the column quad [4q, 4q + 4) of [Z | A]: Z left of the
-//     panel's end (Z is lower triangular), A from there on (upper triangle only). It
-//     keeps the panel's 8 entries of its quad in registers for the whole panel.
+//     Elimination on [G | I] turns I into L^-1 = R^-T (L = R^T), so R^-1 = Z^T. Each
+//     column's 8 entries of R also go to RT[j] (the panel rows, transposed), so that a
+//     row's 8 multipliers below are two 16-byte loads.
+//  3. Warps 4..15 subtract the rank-8 update from the rows below the panel, one row per
+//     warp at a time: lane q owns the column quad [4q, 4q + 4) of [Z | A] (Z left of the
+//     panel's end, A from there on, its upper triangle only) and keeps the panel's 8
+//     entries of its quad in registers.
+// One-panel lookahead: the update warps do the next panel's 8 rows first and signal the
+// solver (named barrier 4: 384 arrivals, 128 waiting), which factors and solves the next
+// panel while they update the remaining rows. One block barrier per panel.
 constexpr int kCholWarps = 16;
 constexpr int kCholThreads = kCholWarps * 32;
 constexpr int kPanel = 8;
@@ -272,6 +283,7 @@ static_assert(kRankBlock == 128 && kCholThreads >= kRankBlock, "one column per s
 struct CholSmem {
   float A[kRankBlock * kCLd];  // G, rows turning into R
   float Z[kRankBlock * kCLd];  // I, rows turning into Z = R^-T
+  float RT[2][kRankBlock][kPanel];  // panel p's rows of R, transposed, in RT[p % 2]: RT[.][j][t] = R[k0+t][j]
   float diag0[kRankBlock];     // diagonal of the unshifted Gram matrix
   float ratio[kRankBlock];     // pivot / diag0 (0 for dead pivots)
   int dead[kRankBlock];
@@ -280,15 +292,25 @@ struct CholSmem {
 };
 
 // A = G + shift I and Z = I on the leading r x r block, zeros elsewhere. The Gram sum holds
-// the upper triangle; each thread mirrors the entries it loads.
+// the upper triangle; each thread mirrors the entries it loads. All of a thread's loads are
+// issued before its first shared-memory store (a store between two loads through a plain
+// pointer would make each load wait for the one before it).
 __device__ __forceinline__ void chol_load(const MatMeta& mt, int r, int rp, float shift, CholSmem& S,
                                           bool record) {
   const float* src = mt.Gpart + (size_t)mt.C * rp * rp;
-  for (int idx = threadIdx.x; idx < kRankBlock * kRankBlock; idx += kCholThreads) {
-    const int i = idx >> 7, j = idx & 127;
+  constexpr int kPer = kRankBlock * kRankBlock / kCholThreads;  // 32 entries per thread
+  float v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int idx = (int)threadIdx.x + kCholThreads * u, i = idx >> 7, j = idx & 127;
+    v[u] = (j >= i && j < r) ? __ldcg(src + (size_t)i * rp + j) : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int idx = (int)threadIdx.x + kCholThreads * u, i = idx >> 7, j = idx & 127;
     S.Z[i * kCLd + j] = (i == j && i < r) ? 1.f : 0.f;
     if (j >= i) {
-      float g = j < r ? __ldcg(src + (size_t)i * rp + j) : 0.f;
+      float g = v[u];
       if (i == j && i < r) {
         if (record) S.diag0[i] = g;
         g += shift;
@@ -303,9 +325,13 @@ __device__ __forceinline__ void chol_load(const MatMeta& mt, int r, int rp, floa
 __device__ __forceinline__ void chol_panel_solve(int k0, int kb, int r, float dead_tol, CholSmem& S) {
   float D[kPanel][kPanel];
 #pragma unroll
-  for (int s = 0; s < kPanel; ++s)
+  for (int s = 0; s < kPanel; ++s) {  // row s of the block: two 16-byte loads (k0 % 8 == 0)
+    const float4 lo = *reinterpret_cast<const float4*>(&S.A[(k0 + s) * kCLd + k0]);
+    const float4 hi = *reinterpret_cast<const float4*>(&S.A[(k0 + s) * kCLd + k0 + 4]);
+    const float row[kPanel] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-    for (int t = 0; t < kPanel; ++t) D[s][t] = (t >= s && t < kb) ? S.A[(k0 + s) * kCLd + k0 + t] : 0.f;
+    for (int t = 0; t < kPanel; ++t) D[s][t] = (t >= s && t < kb) ? row[t] : 0.f;
+  }
   float inv[kPanel];
   bool dead[kPanel];
 #pragma unroll
@@ -326,13 +352,18 @@ __device__ __forceinline__ void chol_panel_solve(int k0, int kb, int r, float de
       for (int u = t + 1; u < kPanel; ++u)
 #pragma unroll
         for (int v = u; v < kPanel; ++v) D[u][v] = fmaf(-D[t][u], D[t][v], D[u][v]);
-      if (threadIdx.x == 0) {
-        S.dead[k0 + t] = bad;
-        S.ratio[k0 + t] = bad ? 0.f : __fdividef(d, d0);  // statistics only
-      }
     }
   }
   const int c = threadIdx.x;
+  if (c == 0) {  // the pivot records
+#pragma unroll
+    for (int t = 0; t < kPanel; ++t) {
+      if (t < kb) {
+        S.dead[k0 + t] = dead[t];
+        S.ratio[k0 + t] = dead[t] ? 0.f : __fdividef(D[t][t] * D[t][t], S.diag0[k0 + t]);  // statistics only
+      }
+    }
+  }
   if (c < k0 + kPanel && c < r) {  // the panel's rows of Z (lower triangular: columns <= k0 + 7)
     float x[kPanel];
 #pragma unroll
@@ -347,71 +378,87 @@ __device__ __forceinline__ void chol_panel_solve(int k0, int kb, int r, float de
     for (int t = 0; t < kPanel; ++t)
       if (t < kb) S.Z[(k0 + t) * kCLd + c] = x[t];
   }
-  if (c >= k0 && c < r) {  // the panel's rows of R
+  // The panel's rows of R from column k0 on, by forward substitution with the block's R.
+  // Inside the block (c < k0 + 8) this repeats the factor's own FMAs in its order, so row
+  // t <= c - k0 gets the block's value bit for bit (the diagonal: d / sqrt(d) as above);
+  // rows below the block's diagonal get values that nothing reads.
+  if (c >= k0 && c < r) {
     float x[kPanel];
-    if (c < k0 + kPanel) {  // inside the diagonal block: the factor itself
-      const int cu = c - k0;
 #pragma unroll
-      for (int t = 0; t < kPanel; ++t) {
-        float v = 0.f;
+    for (int t = 0; t < kPanel; ++t) x[t] = t < kb ? S.A[(k0 + t) * kCLd + c] : 0.f;
 #pragma unroll
-        for (int u = 0; u < kPanel; ++u)
-          if (u == cu && u >= t) v = D[t][u];
-        x[t] = v;
-      }
-    } else {  // right of it: forward substitution with the block's R
+    for (int t = 0; t < kPanel; ++t) {
 #pragma unroll
-      for (int t = 0; t < kPanel; ++t) x[t] = t < kb ? S.A[(k0 + t) * kCLd + c] : 0.f;
-#pragma unroll
-      for (int t = 0; t < kPanel; ++t) {
-#pragma unroll
-        for (int s2 = 0; s2 < t; ++s2) x[t] = fmaf(-D[s2][t], x[s2], x[t]);
-        x[t] = dead[t] ? 0.f : x[t] * inv[t];
-      }
+      for (int s2 = 0; s2 < t; ++s2) x[t] = fmaf(-D[s2][t], x[s2], x[t]);
+      x[t] = (dead[t] && c != k0 + t) ? 0.f : (dead[t] ? 1.f : x[t] * inv[t]);
     }
 #pragma unroll
     for (int t = 0; t < kPanel; ++t)
       if (t < kb) S.A[(k0 + t) * kCLd + c] = x[t];
+    float* rt = S.RT[(k0 / kPanel) & 1][c];  // the update of this panel reads it while the next
+    *reinterpret_cast<float4*>(rt) = make_float4(x[0], x[1], x[2], x[3]);  // panel's solve writes
+    *reinterpret_cast<float4*>(rt + 4) = make_float4(x[4], x[5], x[6], x[7]);  // the other buffer
   }
 }
 
-// Step 3 for the panel at k0: rows i >= k0 + 8 of A (upper triangle) and Z lose
-// sum_t R[k0+t][i] times the panel's row t.
-__device__ __forceinline__ void chol_trailing_update(int k0, int kb, int r, CholSmem& S) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kend = k0 + kPanel, c0 = 4 * lane;
-  if (kend >= r || c0 >= r) return;
-  const bool zq = c0 < kend;
-  float* M = zq ? S.Z : S.A;
-  float4 pv[kPanel];
+// Step 3 for the full panel at k0 (8 pivots) on rows [i0, i1): A (upper triangle) and Z
+// lose sum_t R[k0+t][i] times the panel's row t. The calling group of nw warps (w = this
+// warp's index in it) takes rows i0 + w, i0 + w + nw, ... pv: the lane's quad of the
+// panel's rows, loaded by chol_panel_quad.
+__device__ __forceinline__ void chol_panel_quad(int k0, int r, CholSmem& S, float4 (&pv)[kPanel]) {
+  const int c0 = 4 * (threadIdx.x & 31);
+  const float* M = c0 < k0 + kPanel ? S.Z : S.A;
 #pragma unroll
   for (int t = 0; t < kPanel; ++t)
-    pv[t] = t < kb ? *reinterpret_cast<const float4*>(&M[(k0 + t) * kCLd + c0]) : make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = kend + warp; i < r; i += kCholWarps) {
+    pv[t] = c0 < r ? *reinterpret_cast<const float4*>(&M[(k0 + t) * kCLd + c0]) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__device__ __forceinline__ void chol_update_rows(int k0, int r, int i0, int i1, int w, int nw,
+                                                 const float4 (&pv)[kPanel], CholSmem& S) {
+  const int c0 = 4 * (threadIdx.x & 31);
+  if (i0 >= i1 || c0 >= r) return;
+  const bool zq = c0 < k0 + kPanel;
+  float* M = zq ? S.Z : S.A;
+  for (int i = i0 + w; i < i1; i += nw) {
     if (!zq && c0 + 3 < i) continue;  // wholly below the diagonal of A
+    const float* rt = S.RT[(k0 / kPanel) & 1][i];
+    const float4 cf0 = *reinterpret_cast<const float4*>(rt);  // R[k0 .. k0+3][i]
+    const float4 cf1 = *reinterpret_cast<const float4*>(rt + 4);
+    const float cf[kPanel] = {cf0.x, cf0.y, cf0.z, cf0.w, cf1.x, cf1.y, cf1.z, cf1.w};
     float4 v = *reinterpret_cast<const float4*>(&M[i * kCLd + c0]);
 #pragma unroll
     for (int t = 0; t < kPanel; ++t) {
-      const float cf = S.A[(k0 + t) * kCLd + i];  // R[k0+t][i] (0 past kb: pv is 0 there too)
-      v.x = fmaf(-cf, pv[t].x, v.x);
-      v.y = fmaf(-cf, pv[t].y, v.y);
-      v.z = fmaf(-cf, pv[t].z, v.z);
-      v.w = fmaf(-cf, pv[t].w, v.w);
+      v.x = fmaf(-cf[t], pv[t].x, v.x);
+      v.y = fmaf(-cf[t], pv[t].y, v.y);
+      v.z = fmaf(-cf[t], pv[t].z, v.z);
+      v.w = fmaf(-cf[t], pv[t].w, v.w);
     }
     *reinterpret_cast<float4*>(&M[i * kCLd + c0]) = v;
   }
 }
 
+__device__ __forceinline__ void next_rows_ready_arrive() { asm volatile("bar.arrive 4, 512;" ::: "memory"); }
+__device__ __forceinline__ void next_rows_ready_wait() { asm volatile("bar.sync 4, 512;" ::: "memory"); }
+
 __device__ void chol_factor(int r, float dead_tol, CholSmem& S) {
+  const int warp = threadIdx.x >> 5;
   const int npan = (r + kPanel - 1) / kPanel;
-  for (int pn = 0; pn < npan; ++pn) {
-    const int k0 = pn * kPanel, kb = min(kPanel, r - k0);
-    if (threadIdx.x < kRankBlock) chol_panel_solve(k0, kb, r, dead_tol, S);
-    __syncthreads();
-    if (k0 + kPanel < r) {
-      chol_trailing_update(k0, kb, r, S);
-      __syncthreads();
+  if (threadIdx.x < kRankBlock) chol_panel_solve(0, min(kPanel, r), r, dead_tol, S);
+  __syncthreads();
+  for (int pn = 0; pn + 1 < npan; ++pn) {
+    const int k0 = pn * kPanel, nxt = k0 + kPanel;
+    const int nkb = min(kPanel, r - nxt);
+    if (warp < 4) {
+      next_rows_ready_wait();
+      chol_panel_solve(nxt, nkb, r, dead_tol, S);
+    } else {
+      float4 pv[kPanel];
+      chol_panel_quad(k0, r, S, pv);
+      chol_update_rows(k0, r, nxt, nxt + nkb, warp - 4, kCholWarps - 4, pv, S);
+      next_rows_ready_arrive();
+      chol_update_rows(k0, r, nxt + kPanel, r, warp - 4, kCholWarps - 4, pv, S);
     }
+    __syncthreads();
   }
 }
 
@@ -540,7 +587,8 @@ __device__ void apply_tile(const Plan& p, const MatMeta& mt, int pass, int tile,
   // A warp owns a 16-column strip (tx = column block of 8, ty = group of 4 rows), so the
   // chunks of R^-1 below its strip (rows k > its last column: zero) are skipped whole.
   const int tx = tid >> 4, ty = tid & 15;
-  const int warp_last_col = (tid >> 5) * 16 + 15;
+  // a strip wholly right of column r - 1 has no output: it skips every chunk
+  const int warp_last_col = (tid >> 5) * 16 >= r ? -1 : (tid >> 5) * 16 + 15;
   float acc[4][8], lo[4][8];  // lo: compensation terms (kAcc only)
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -653,7 +701,7 @@ __device__ void apply_tile(const Plan& p, const MatMeta& mt, int pass, int tile,
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int c = tx * 8 + j;
-      Ys[rr][c] = (live_row && c < r) ? acc[i][j] : 0.f;
+      Ys[rr][gram_slot(c)] = (live_row && c < r) ? acc[i][j] : 0.f;
     }
   }
   bar.sync();

@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(256) k_qdec(Plan p, int kp) {
 // Shared memory, carved at run time: a_stages A tiles (16 KB each), B_STAGES B tiles of
 // b_stage bytes (1 KB multiples), then the barriers and the TMEM address slot.
 constexpr int kMaxAStages = 12;
-constexpr int kGemmAccs = 4;  // TMEM accumulators of the separate GEMMs
+constexpr int kGemmAccs = 2;  // TMEM accumulators of the separate GEMMs (256 columns each)
 struct GemmBars {
   uint64_t full_a[kMaxAStages], empty_a[kMaxAStages];
   uint64_t full_b[B_STAGES], empty_b[B_STAGES];
@@ -290,12 +290,15 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int TERMS = BF16 ? 3 : 2;
   const int rp = p.rp, N = TERMS * rp;          // B rows: the split terms, rp rows each
-  // The split terms go along K into one accumulator of rp <= 128 columns, so four
-  // accumulators fit in TMEM's 512 columns: the MMA can run three segments ahead of the
-  // epilogue's drain.
+  // One MMA of N = 2 rp multiplies the A tile by the first two split terms side by side
+  // (B rows [0, 2 rp)), so the tensor core reads each A tile once per K step instead of
+  // once per term: below N = 256 an MMA's time is set by the shared-memory bytes it reads.
+  // Accumulator columns [0, rp) hold term 0's products, [rp, 2 rp) term 1's; the third
+  // term of bf16 goes onto term 0's columns. The epilogue adds the two halves. Two
+  // accumulators of 256 columns fit in TMEM: the MMA can run a segment ahead of the drain.
   constexpr int NACC = kGemmAccs;
-  constexpr uint32_t kAccCols = 128;
-  static_assert(NACC * kAccCols <= 512 && kAccCols >= kRankBlock, "accumulators fit in TMEM");
+  constexpr uint32_t kAccCols = 256;
+  static_assert(NACC * kAccCols <= 512 && kAccCols >= 2 * kRankBlock, "accumulators fit in TMEM");
   const int NBOX = N <= 256 ? 1 : 2;            // TMA boxes per B tile (<= 256 rows each)
   const uint32_t b_bytes = (uint32_t)N * BK * 2;  // one k-block's B tile
   const uint32_t b_tile = b_stage / (uint32_t)kps;  // its slot in a B stage (1 KB multiple)
@@ -328,8 +331,8 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t ia = 0, ib = 0;
-      int64_t b_tag[B_STAGES];  // (matrix, first k-block) a B stage holds, -1: none
-      for (int i = 0; i < B_STAGES; ++i) b_tag[i] = -1;
+      static_assert(B_STAGES == 2, "two B tags");
+      int64_t b_tag0 = -1, b_tag1 = -1;  // (matrix, first k-block) each B stage holds, -1: none
       bool ok = true;
       // L2 prefetch of the A boxes kPrefetchStages stages ahead (Q GEMM)
       AStageIter pf{u_first, u_end, u_step, 0, 0, false};
@@ -357,10 +360,10 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
           ok = mbar_wait(&sm.empty_b[sb], ((ib / B_STAGES) & 1) ^ 1, err);
           if (!ok) break;
           const int64_t tag = ((int64_t)un.t << 32) | ((int64_t)kb << 8) | nk;
-          if (b_tag[sb] == tag) {
+          if ((sb ? b_tag1 : b_tag0) == tag) {
             mbar_arrive(&sm.full_b[sb]);  // the stage still holds these k-blocks' B tiles
           } else {
-            b_tag[sb] = tag;
+            if (sb) b_tag1 = tag; else b_tag0 = tag;
             mbar_arrive_expect_tx(&sm.full_b[sb], (uint32_t)nk * b_bytes);
             for (int h = 0; h < nk; ++h)
               for (int x = 0; x < NBOX; ++x)
@@ -399,7 +402,7 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
     // segment ends are counters. Each tcgen05.mma waits until the tensor pipe takes it, so
     // the work between two of them adds to every MMA's time.
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(BM, rp, BF16, MN_A, false);
+      const uint32_t idesc2 = idesc_f16(BM, 2 * rp, BF16, MN_A, false), idesc1 = idesc_f16(BM, rp, BF16, MN_A, false);
       const uint64_t a_base = MN_A ? smem_desc(smem_u32(S.a(0)), a_bytes / 2, 1024) : smem_desc(smem_u32(S.a(0)), 16, 1024);
       const uint64_t b_base = smem_desc(smem_u32(S.b(0, b_stage)), 16, 1024);
       const uint32_t a_stage16 = a_bytes >> 4, b_stage16 = b_stage >> 4, b_tile16 = b_tile >> 4;
@@ -439,11 +442,10 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
                 for (int k = 0; k < BK / 16; ++k) {
                   // MN-major A: 64 x (64 kps)-row boxes, k-block h at h * 64 rows of 128 bytes
                   const uint64_t adk = ad + (uint64_t)(MN_A ? (h * 8192 + k * 2048) >> 4 : (k * 32) >> 4);
-#pragma unroll
-                  for (int tm = 0; tm < TERMS; ++tm) {  // B rows [tm rp, (tm + 1) rp): term tm
-                    umma_f16(d_tmem, adk, bdh + (uint64_t)(tm * term16 + k * 2), idesc, accum);
-                    accum = 1;
-                  }
+                  // B rows [0, 2 rp): terms 0 and 1; rows [2 rp, 3 rp): term 2 (bf16)
+                  umma_f16(d_tmem, adk, bdh + (uint64_t)(k * 2), idesc2, accum);
+                  if (TERMS == 3) umma_f16(d_tmem, adk, bdh + (uint64_t)(2 * term16 + k * 2), idesc1, 1u);
+                  accum = 1;
                 }
                 --steps_left;
                 if (--seg_left == 0 || steps_left == 0) {  // close the segment
@@ -488,16 +490,15 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
         tc_fence_after();
         const uint32_t t_row = tmem_base + (uint32_t)acc * kAccCols + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
-        for (int cc = 0; cc < kRankBlock / 32; cc += 2) {  // chunks in pairs, one wait a pair
+        for (int cc = 0; cc < kRankBlock / 32; ++cc) {  // a chunk's two term columns, one wait
           if (ch0 + cc < ch1) {
             const int c = (ch0 + cc) * 16;
-            const bool pair = ch0 + cc + 1 < ch1;
             float t0[16], t1[16];
-            tmem_ld16x2(t_row + c, t_row + (pair ? c + 16 : c), t0, t1);
+            tmem_ld16x2(t_row + c, t_row + rp + c, t0, t1);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              run[cc * 16 + i] = sg == 0 ? t0[i] : __fadd_rn(run[cc * 16 + i], t0[i]);
-              if (pair) run[cc * 16 + 16 + i] = sg == 0 ? t1[i] : __fadd_rn(run[cc * 16 + 16 + i], t1[i]);
+              const float v = __fadd_rn(t0[i], t1[i]);
+              run[cc * 16 + i] = sg == 0 ? v : __fadd_rn(run[cc * 16 + i], v);
             }
           }
         }
@@ -599,7 +600,7 @@ struct StageIter {
   }
 };
 
-template <typename TE>
+template <typename TE, bool kMask>
 __global__ void __launch_bounds__(kIngThreads, 1)
 k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ units, int nunits,
            int a_stages, int ge_stages, int kps, uint32_t b_stage, int seg) {
@@ -833,6 +834,9 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
                            inv_s >= 0x1p-24f;
       const __half2 inv2 = __float2half2_rn(inv_s);
       TE* mo = static_cast<TE*>(mt.mscr) + (size_t)ti.w * mt.m * mt.n;
+      // nonfinite mask (PSGD_FLAG_MASK): n is a multiple of 8, so a thread's 8 entries are
+      // one byte of the row-major, LSB-first bitmap
+      uint8_t* mbits = kMask ? reinterpret_cast<uint8_t*>(p.mask + p.mask_off[(size_t)ti.un.t * p.W + ti.w]) : nullptr;
       int cnt = 0;
       unsigned mmax = 0u;
       for (int h = 0; h < ti.nk && ok; ++h) {  // the stage's k-blocks, one A tile each
@@ -855,6 +859,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
             const TE* gx = reinterpret_cast<const TE*>(&gv);
             const TE* ex = reinterpret_cast<const TE*>(&ev);
             TE* mx = reinterpret_cast<TE*>(&mv);
+            uint32_t mbyte = 0u;
             if (h2_path) {
               const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, ew[4] = {ev.x, ev.y, ev.z, ev.w};
               uint32_t mw[4];
@@ -864,6 +869,7 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
                 const uint32_t bad = ((xe & 0xFFFFu) == 0x7C00u ? 0x0000FFFFu : 0u) |
                                      ((xe >> 16) == 0x7C00u ? 0xFFFF0000u : 0u);
                 cnt += __popc(bad) >> 4;
+                if (kMask) mbyte |= ((bad & 1u) | ((bad >> 15) & 2u)) << (2 * i);
                 __half2 gh, eh;
                 memcpy(&gh, &gw[i], 4);
                 memcpy(&eh, &ew[i], 4);
@@ -879,11 +885,13 @@ k_ingest_p(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict_
                 const float x = to_f(gx[i]) * inv_s;
                 const bool bad = !isfinite(x);
                 cnt += bad;
+                if (kMask) mbyte |= (uint32_t)bad << i;
                 mx[i] = add_to<TE>(bad ? 0.0f : x, to_f(ex[i]));
                 if (BF16) mmax = max(mmax, __float_as_uint(fabsf(to_f(mx[i]))));
               }
             }
             __stcg(reinterpret_cast<uint4*>(mo + row * mt.n + col), mv);
+            if (kMask) mbits[(row * mt.n + col) >> 3] = (uint8_t)mbyte;
           }
           *reinterpret_cast<uint4*>(tile + rl * 128 + ((cq ^ (rl & 7)) << 4)) = mv;
         }
@@ -1207,12 +1215,15 @@ k_decomp_tc(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict
       if (!ok) break;
       // G^: half g of the tile (this warp's 64 columns when half == g) goes into a stage in
       // the 128-byte-swizzled layout of two 32-column fp32 boxes, which the TMA warp stores.
-      // The other half's warps only arrive.
+      // The other half's warps only arrive, but they too wait for the stage first: the TMA
+      // warp marks it full only after the stage's previous use is done, and an arrival
+      // before that would count toward the previous use (whose store would then start
+      // while a slower warp is still writing its tile).
       for (int g = 0; g < 2; ++g) {
         const int s = (int)(i % DEC_MSTAGES);
+        ok = mbar_wait(&sm.mfull[s], (i / DEC_MSTAGES) & 1, err);
+        if (!ok) break;
         if (half == g) {
-          ok = mbar_wait(&sm.mfull[s], (i / DEC_MSTAGES) & 1, err);
-          if (!ok) break;
           uint8_t* st = sm.mt[s] + row_in_tile * 128;
 #pragma unroll
           for (int b = 0; b < 2; ++b)
@@ -1505,8 +1516,10 @@ cudaError_t tc_plan(Handle& h, char* ws_tc, cudaStream_t s) {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_ingest_p<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_ingest_p<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_ingest_p<__half, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_ingest_p<__nv_bfloat16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_ingest_p<__half, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_ingest_p<__nv_bfloat16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, gs);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_decomp_tc<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, ds);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k_decomp_tc<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, ds);
   return e;
@@ -1561,8 +1574,15 @@ cudaError_t launch_ingest_p(const Handle& h, const Plan& p, cudaStream_t s) {
   size_t sm;
   ingest_stages(h.edt, bst, &ast, &gst, &kps, &sm);
   const int seg = kIngSegSteps;
-  if (h.edt == DT_BF16) k_ingest_p<__nv_bfloat16><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, kps, bst, seg);
-  else k_ingest_p<__half><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, kps, bst, seg);
+  // the mask bitmap (a debug output) has its own instantiation: the ingest warps' issue rate
+  // sets this kernel's pace, and the bit assembly would slow every step
+  if (h.edt == DT_BF16) {
+    if (p.mask) k_ingest_p<__nv_bfloat16, true><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, kps, bst, seg);
+    else k_ingest_p<__nv_bfloat16, false><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, kps, bst, seg);
+  } else {
+    if (p.mask) k_ingest_p<__half, true><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, kps, bst, seg);
+    else k_ingest_p<__half, false><<<grid, kIngThreads, sm, s>>>(p, tp->d_maps, tp->d_punits, tp->np, ast, gst, kps, bst, seg);
+  }
   h.launches += 1;
   return cudaGetLastError();
 }

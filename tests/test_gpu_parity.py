@@ -64,12 +64,13 @@ def test_ingest_every_bit_pattern(dtype, scale):
 def test_fused_ingest_every_bit_pattern(dtype, scale):
     """The production path (the fused ingest + P GEMM kernel, a full step): every 16-bit
     pattern once per worker as a gradient entry, under random finite error-buffer values
-    below 2^10. M and the nonfinite counts must equal the oracle's bit for bit."""
+    below 2^10. M, the nonfinite mask bitmap and the counts must equal the oracle's bit
+    for bit."""
     psgd = _psgd()
     tdt = synth.TORCH_DTYPE[dtype]
     rng = np.random.default_rng(13)
     W, m, n, r = 2, 256, 256, 16
-    ps = psgd.PowerSGD([(m, n)], 1, W, r, dtype)
+    ps = psgd.PowerSGD([(m, n)], 1, W, r, dtype, flags=psgd.PSGD_FLAG_MASK)
     assert ps.engine == "tcgen05"
     grads, errs, gin, ein = [], [], [], []
     top = 0x6400 if dtype == "f16" else 0x4480  # |E| < 2^10
@@ -93,6 +94,10 @@ def test_fused_ingest_every_bit_pattern(dtype, scale):
         same = (got_m == want_m) | (np.isnan(got_m) & np.isnan(want_m))
         assert same.all(), f"worker {w}: {int((~same).sum())} M entries differ"
         assert counts[w] == int(mask.sum())
+        off = psgd.psgd_mask_offset(ps.cfg, 0, 0, w)
+        words = ps.mask[off:off + m * n // 32].cpu().numpy().astype(np.uint32)
+        got_mask = np.unpackbits(words.view(np.uint8), bitorder="little").astype(bool)
+        assert np.array_equal(got_mask, mask.reshape(-1)), f"worker {w}: mask bits differ"
 
 
 def test_ingest_fp32_specials():
