@@ -323,7 +323,12 @@ __device__ __forceinline__ void chol_load(const MatMeta& mt, int r, int rp, floa
 
 // Steps 1 and 2 for the panel at k0 (kb <= 8 pivots); threads 0..127, column c = thread.
 __device__ __forceinline__ void chol_panel_solve(int k0, int kb, int r, float dead_tol, CholSmem& S) {
-  float D[kPanel][kPanel];
+  float D[kPanel][kPanel], d0[kPanel];
+  {  // the block's original diagonal, off the pivot chain
+    const float4 lo = *reinterpret_cast<const float4*>(&S.diag0[k0]);
+    const float4 hi = *reinterpret_cast<const float4*>(&S.diag0[k0 + 4]);
+    d0[0] = lo.x; d0[1] = lo.y; d0[2] = lo.z; d0[3] = lo.w; d0[4] = hi.x; d0[5] = hi.y; d0[6] = hi.z; d0[7] = hi.w;
+  }
 #pragma unroll
   for (int s = 0; s < kPanel; ++s) {  // row s of the block: two 16-byte loads (k0 % 8 == 0)
     const float4 lo = *reinterpret_cast<const float4*>(&S.A[(k0 + s) * kCLd + k0]);
@@ -340,8 +345,7 @@ __device__ __forceinline__ void chol_panel_solve(int k0, int kb, int r, float de
     dead[t] = true;
     if (t < kb) {
       const float d = D[t][t];
-      const float d0 = S.diag0[k0 + t];
-      const bool bad = !(d > dead_tol * d0) || !isfinite(d) || !(d0 > 0.f);
+      const bool bad = !(d > dead_tol * d0[t]) || !isfinite(d) || !(d0[t] > 0.f);
       const float iv = bad ? 1.f : rsqrtf(d);
       inv[t] = iv;
       dead[t] = bad;
@@ -360,7 +364,7 @@ __device__ __forceinline__ void chol_panel_solve(int k0, int kb, int r, float de
     for (int t = 0; t < kPanel; ++t) {
       if (t < kb) {
         S.dead[k0 + t] = dead[t];
-        S.ratio[k0 + t] = dead[t] ? 0.f : __fdividef(D[t][t] * D[t][t], S.diag0[k0 + t]);  // statistics only
+        S.ratio[k0 + t] = dead[t] ? 0.f : __fdividef(D[t][t] * D[t][t], d0[t]);  // statistics only
       }
     }
   }

@@ -118,6 +118,26 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Flattened grids over the B*J matrices. Every block has the same J shapes, so matrix j of
+// block 0 gives the item count of matrix j of every block: item i of the launch is item k
+// of matrix t = b*J + j. A grid of B * sum_j count(j) blocks has no idle blocks, where a
+// (max count, B*J) grid would launch, for every smaller matrix, blocks that leave at once.
+template <typename F>
+__device__ __forceinline__ void flat_item(const Plan& p, int64_t i, F count, int& t, int64_t& k) {
+  int64_t per = 0;
+  for (int j = 0; j < p.J; ++j) per += count(p.meta[j]);
+  const int64_t b = i / per;
+  int64_t rem = i - b * per;
+  int j = 0;
+  for (; j < p.J - 1; ++j) {
+    const int64_t c = count(p.meta[j]);
+    if (rem < c) break;
+    rem -= c;
+  }
+  t = (int)b * p.J + j;
+  k = rem;
+}
+
 // Barrier policies of device code that a group of threads runs: the whole CTA
 // (__syncthreads), or one 256-thread half of a 512-thread CTA (named barrier 1 or 2).
 struct CtaBar {

@@ -201,18 +201,20 @@ __global__ void __launch_bounds__(kT) k_qgemm(Plan p) {
 // its loads in flight together), and the four sums are added in the order g = 0, 1, 2, 3,
 // a fixed order whatever the run. Lane l takes 4 consecutive columns per 128-column
 // chunk of the row (one 16-byte load per slice; rp is a multiple of 16).
-// grid = (ceil(max n / 2), B*J), 256 threads: rows 2 blockIdx.x and 2 blockIdx.x + 1.
+// Flattened grid (flat_item): B * sum_j ceil(n_j / 2) blocks of 256 threads, two rows each.
 constexpr int kQredSplit = 4;
 __global__ void __launch_bounds__(256) k_qreduce(Plan p, float qscale) {
   pdl_wait();
-  const MatMeta& mt = p.meta[blockIdx.y];
+  int t;
+  int64_t item;
+  flat_item(p, blockIdx.x, [](const MatMeta& m) { return (m.n + 1) / 2; }, t, item);
+  const MatMeta& mt = p.meta[t];
   if (p.skip[mt.b]) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = warp & (kQredSplit - 1);
-  const int64_t row = (int64_t)blockIdx.x * 2 + (warp >> 2);
-  if ((int64_t)blockIdx.x * 2 >= mt.n) return;  // whole block past the end (block-uniform)
+  const int64_t row = item * 2 + (warp >> 2);
   const float fw = p.mean_div;
-  float* q = p.q_to_exchange ? mt.xq : p.tab.q[blockIdx.y];
+  float* q = p.q_to_exchange ? mt.xq : p.tab.q[t];
   const int msh = reinterpret_cast<const int*>(mt.scal)[SC_MSHIFT];  // rescaled M: Q * 2^msh
   const size_t stride = (size_t)mt.n * p.rp;  // one slice of Qpart
   __shared__ float4 part[2][kQredSplit][32];
@@ -361,10 +363,9 @@ cudaError_t launch_qgemm_simt(const Handle& h, const Plan& p, cudaStream_t s) {
 }
 
 cudaError_t launch_qreduce(const Handle& h, const Plan& p, cudaStream_t s) {
-  int64_t max_n = 0;
-  for (const MatMeta& mt : h.meta) max_n = std::max<int64_t>(max_n, mt.n);
-  dim3 grid((unsigned)((max_n + 1) / 2), p.B * p.J);
-  launch_pdl(k_qreduce, dim3(grid), dim3(256), 0, s, p, h.tc ? 0x1p-14f : 1.0f);
+  int64_t per = 0;
+  for (int j = 0; j < h.J; ++j) per += (h.meta[j].n + 1) / 2;
+  launch_pdl(k_qreduce, dim3((unsigned)(per * p.B)), dim3(256), 0, s, p, h.tc ? 0x1p-14f : 1.0f);
   h.launches += 1;
   return cudaGetLastError();
 }

@@ -59,29 +59,31 @@ __device__ void psplit_rows(const Plan& p, const MatMeta& mt, int kp, int blk, f
   const int64_t left = mt.m - row0;
   const int nrows = left <= 0 ? 0 : (left < 32 ? (int)left : 32);
   const float* src = mt.Phat + row0 * rp;
-  {  // stage the rows * 2^14 (exact): every load of a thread before its stores
-    constexpr int kPer = 32 * kRankBlock / 256;
-    const int count = nrows * rp;
-    float v[kPer];
+  {  // stage the rows * 2^14 (exact), warp w rows w, w + 8, ..., lane 16 bytes of a row:
+     // every load of a thread before its stores (rp is a multiple of 16, P^ 16-byte aligned)
+    float4 v[4];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = tid + u * 256;
-      v[u] = i < count ? __ldcg(src + i) : 0.f;
+    for (int u = 0; u < 4; ++u) {
+      const int rr = (tid >> 5) + 8 * u, c = (tid & 31) * 4;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (rr < nrows && c < rp) v[u] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)rr * rp + c));
     }
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = tid + u * 256;
-      if (i < 32 * rp) {
-        const int rr = i / rp, c = i - rr * rp;
-        xs[rr][c] = (i < count && c < r) ? v[u] * 16384.0f : 0.f;
+    for (int u = 0; u < 4; ++u) {
+      const int rr = (tid >> 5) + 8 * u, c = (tid & 31) * 4;
+      if (c < rp) {
+        xs[rr][c] = c < r ? v[u].x * 16384.0f : 0.f;
+        xs[rr][c + 1] = c + 1 < r ? v[u].y * 16384.0f : 0.f;
+        xs[rr][c + 2] = c + 2 < r ? v[u].z * 16384.0f : 0.f;
+        xs[rr][c + 3] = c + 3 < r ? v[u].w * 16384.0f : 0.f;
       }
     }
   }
   bar.sync();
-  // pdec rows: [hi | lo | hi], kp / 8 groups of 8 columns per segment
-  const int gpr = kp / 8;
+  // pdec rows: [hi | lo | hi], kp / 8 groups of 8 columns per segment (kp / 8 is 8 or 16)
+  const int gpr = kp / 8, lg = __ffs(gpr) - 1;
   for (int it = tid; it < 32 * gpr; it += 256) {
-    const int rr = it / gpr, c0 = (it - rr * gpr) * 8;
+    const int rr = it >> lg, c0 = (it & (gpr - 1)) * 8;
     __align__(16) uint16_t hh[8], hl[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) split2<__half>(c0 + i < rp ? xs[rr][c0 + i] : 0.f, hh[i], hl[i]);

@@ -137,14 +137,16 @@ __global__ void __launch_bounds__(256) k_qsplit(Plan p) {
 // P = (sum_c Ppart[c]) / W in chunk order, plus max|P| -> scal[1]. P keeps the power-of-
 // two scale 2^e of the split Q: P^ does not depend on it, and removing it would push P
 // below fp32's range when both M and Q are tiny (deep blocks of the stack, M ~ Q ~ 2^-80).
-// grid = (ceil(m*rp / 256), B*J).
+// Flattened grid (flat_item): B * sum_j ceil(m_j rp / 1024) blocks of 256 threads.
 __global__ void k_preduce(Plan p, int pchunk_kb) {
   pdl_wait();
-  const MatMeta& mt = p.meta[blockIdx.y];
+  int t;
+  int64_t item;
+  flat_item(p, blockIdx.x, [&](const MatMeta& m) { return (m.m * p.rp + 1023) / 1024; }, t, item);
+  const MatMeta& mt = p.meta[t];
   if (p.skip[mt.b]) return;
   const int rp = p.rp;
-  if ((int64_t)blockIdx.x * blockDim.x * 4 >= mt.m * p.rp) return;  // whole block past the end
-  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  const int64_t i = (item * blockDim.x + threadIdx.x) * 4;
   const int64_t mpad = (mt.m + 127) / 128 * 128;
   unsigned mx = 0u;
   if (i < mt.m * rp) {
@@ -169,14 +171,17 @@ __global__ void k_preduce(Plan p, int pchunk_kb) {
 }
 
 // From P^ (m x rp fp32): the Q GEMM's split operand and the decompression's A operand,
-// 32 rows of P^ per CTA (psplit_rows). grid = (mpad / 32, B*J).
+// 32 rows of P^ per CTA (psplit_rows). Flattened grid: B * sum_j mpad_j / 32 blocks.
 template <typename T>
 __global__ void __launch_bounds__(256) k_psplit(Plan p, int kp) {
   pdl_wait();
-  const MatMeta& mt = p.meta[blockIdx.y];
+  int t;
+  int64_t item;
+  flat_item(p, blockIdx.x, [](const MatMeta& m) { return (m.m + 127) / 128 * 4; }, t, item);
+  const MatMeta& mt = p.meta[t];
   if (p.skip[mt.b]) return;
   __shared__ float xs[32][kRankBlock + 1];
-  psplit_rows<T>(p, mt, kp, blockIdx.x, xs, threadIdx.x, CtaBar{});
+  psplit_rows<T>(p, mt, kp, (int)item, xs, threadIdx.x, CtaBar{});
 }
 
 // qdec[npad][3 kp] = [hi | hi | lo] of the new Q * 2^e in fp16 (e from max|Q|, scal[3]).
@@ -1559,9 +1564,9 @@ cudaError_t launch_pgemm_tc(const Handle& h, const Plan& p, cudaStream_t s) {
   const int seg = kGemmSegSteps;
   if (h.edt == DT_BF16) launch_pdl(k_gemm<false, true>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg, 1, 0);
   else launch_pdl(k_gemm<false, false>, dim3(grid), dim3(kGemmThreads), sm, s, p, tp->d_maps, tp->d_punits, tp->np, ast, bst, 0, seg, 1, 0);
-  int64_t maxe = 0;
-  for (const MatMeta& mt : h.meta) maxe = std::max<int64_t>(maxe, mt.m * p.rp);
-  launch_pdl(k_preduce, dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), dim3(256), 0, s, p, PCHUNK_KB);
+  int64_t per = 0;
+  for (int j = 0; j < h.J; ++j) per += (h.meta[j].m * p.rp + 1023) / 1024;
+  launch_pdl(k_preduce, dim3((unsigned)(per * p.B)), dim3(256), 0, s, p, PCHUNK_KB);
   h.launches += 2;
   return cudaGetLastError();
 }
@@ -1588,9 +1593,9 @@ cudaError_t launch_ingest_p(const Handle& h, const Plan& p, cudaStream_t s) {
 }
 
 cudaError_t launch_preduce(const Handle& h, const Plan& p, cudaStream_t s) {
-  int64_t maxe = 0;
-  for (const MatMeta& mt : h.meta) maxe = std::max<int64_t>(maxe, mt.m * p.rp);
-  launch_pdl(k_preduce, dim3((unsigned)((maxe / 4 + 255) / 256), p.B * p.J), dim3(256), 0, s, p, PCHUNK_KB);
+  int64_t per = 0;
+  for (int j = 0; j < h.J; ++j) per += (h.meta[j].m * p.rp + 1023) / 1024;
+  launch_pdl(k_preduce, dim3((unsigned)(per * p.B)), dim3(256), 0, s, p, PCHUNK_KB);
   h.launches += 1;
   return cudaGetLastError();
 }
@@ -1602,7 +1607,9 @@ int tc_kpad(const Handle& h) { return static_cast<const TcPlan*>(h.tc_plan)->kp;
 cudaError_t launch_qgemm_tc(const Handle& h, const Plan& p, cudaStream_t s, bool psplit_done) {
   const TcPlan* tp = static_cast<const TcPlan*>(h.tc_plan);
   if (!psplit_done) {
-    dim3 g((unsigned)h.max_mtiles * 4, p.B * p.J);
+    int64_t per = 0;
+    for (int j = 0; j < h.J; ++j) per += (h.meta[j].m + 127) / 128 * 4;
+    dim3 g((unsigned)(per * p.B));
     if (h.edt == DT_BF16) launch_pdl(k_psplit<__nv_bfloat16>, dim3(g), dim3(256), 0, s, p, tp->kp);
     else launch_pdl(k_psplit<__half>, dim3(g), dim3(256), 0, s, p, tp->kp);
     h.launches += 1;
