@@ -60,7 +60,7 @@ typedef enum {
   PSGD_OK = 0,
   PSGD_EINVAL = 1,        /* bad argument: null pointer, bad shape, misalignment, ... */
   PSGD_ECUDA = 2,         /* a CUDA runtime or launch error */
-  PSGD_EUNSUPPORTED = 3,  /* valid but not supported by this build (e.g. dtype mix) */
+  PSGD_EUNSUPPORTED = 3,  /* valid but not supported by this library (e.g. dtype mix) */
   PSGD_ETIMEOUT = 4       /* a bounded device-side wait expired (see psgd_check) */
 } psgd_status;
 

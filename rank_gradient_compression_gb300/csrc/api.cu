@@ -58,10 +58,10 @@ psgd_status validate_config(const psgd_config* c) {
   if (!valid_dtype(c->grad_dtype) || !valid_dtype(c->err_dtype))
     return fail(PSGD_EINVAL, "unknown dtype");
   if (c->grad_dtype != c->err_dtype)
-    return fail(PSGD_EUNSUPPORTED, "grad_dtype and err_dtype must be equal in this build");
+    return fail(PSGD_EUNSUPPORTED, "grad_dtype and err_dtype must be equal");
   if (c->rank < 1) return fail(PSGD_EINVAL, "rank must be >= 1");
   if (c->rank > kMaxRank)
-    return fail(PSGD_EUNSUPPORTED, "rank above 1024 is not supported by this build");
+    return fail(PSGD_EUNSUPPORTED, "rank above 1024 is not supported");
   if (c->unc_len < 0) return fail(PSGD_EINVAL, "unc_len must be >= 0");
   if ((c->flags & PSGD_FLAG_EXCHANGE) && c->unc_len != 0)
     return fail(PSGD_EUNSUPPORTED, "PSGD_FLAG_EXCHANGE needs unc_len == 0 (reduce gains/biases separately)");

@@ -46,7 +46,7 @@ struct MatMeta {
 constexpr int kMaxPasses = 4;  // CholeskyQR passes at most (shifted ones included)
 constexpr int kRankBlock = 128;  // widest column block the orthonormalisation factors at once,
                                  // and the largest r of the tensor-core engine
-constexpr int kMaxRank = 1024;   // largest r of this build (the FFMA engine above kRankBlock)
+constexpr int kMaxRank = 1024;   // largest r supported (the FFMA engine above kRankBlock)
 constexpr int64_t kGramRows = 64;  // rows per partial sum of the Gram matrix X^T X
 
 // Per-step device pointer tables (uploaded when they change).

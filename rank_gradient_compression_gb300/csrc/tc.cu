@@ -335,6 +335,8 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      // M (A) is streamed once; the split B tiles are re-read by every column tile of a slice
+      const uint64_t pol_stream = l2_evict_first(), pol_keep = l2_evict_last();
       uint32_t ia = 0, ib = 0;
       static_assert(B_STAGES == 2, "two B tags");
       int64_t b_tag0 = -1, b_tag1 = -1;  // (matrix, first k-block) each B stage holds, -1: none
@@ -372,8 +374,8 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
             mbar_arrive_expect_tx(&sm.full_b[sb], (uint32_t)nk * b_bytes);
             for (int h = 0; h < nk; ++h)
               for (int x = 0; x < NBOX; ++x)
-                tma_load_2d(S.b(sb, b_stage) + h * b_tile + x * (N / NBOX) * BK * 2, mb, (kb + h) * BK,
-                            x * (N / NBOX), &sm.full_b[sb]);
+                tma_load_2d_hint(S.b(sb, b_stage) + h * b_tile + x * (N / NBOX) * BK * 2, mb, (kb + h) * BK,
+                                 x * (N / NBOX), &sm.full_b[sb], pol_keep);
           }
           ++ib;
           for (int w = 0; w < p.W; ++w) {
@@ -386,8 +388,8 @@ k_gemm(Plan p, const CUtensorMap* __restrict__ maps, const Unit* __restrict__ un
             if (!MN_A) {
               tma_load_3d(S.a(sa), mm, kb * BK, un.tile * BM, w, &sm.full_a[sa]);
             } else {
-              tma_load_3d(S.a(sa), mm, un.tile * BM, kb * BK, w, &sm.full_a[sa]);
-              tma_load_3d(S.a(sa) + a_bytes / 2, mm, un.tile * BM + 64, kb * BK, w, &sm.full_a[sa]);
+              tma_load_3d_hint(S.a(sa), mm, un.tile * BM, kb * BK, w, &sm.full_a[sa], pol_stream);
+              tma_load_3d_hint(S.a(sa) + a_bytes / 2, mm, un.tile * BM + 64, kb * BK, w, &sm.full_a[sa], pol_stream);
               prefetch_next();
             }
             ++ia;
