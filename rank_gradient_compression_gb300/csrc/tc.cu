@@ -6,18 +6,18 @@
 //
 // M is exact in its 16-bit type. The fp32 operand (Q or P^) is scaled by a power of two
 // and split into 16-bit terms: x*2^e = hi + lo for fp16 (~22 significant bits), and
-// hi + mid + lo for bf16 (~24). The terms sit side by side as the N dimension of the
-// MMA (N = terms * rp, issued as <= 256-wide pieces), so one pass over M produces every
-// partial product in TMEM, and the epilogue adds them. A plain 16-bit product would
-// keep 11 (fp16) or 8 (bf16) bits. The decompression
+// hi + mid + lo for bf16 (~24). One pass over M multiplies it by every term: the fused P
+// GEMM issues one MMA per term into the same accumulator columns, and the Q GEMM one MMA
+// of width 2 rp for the first two terms side by side (the epilogue adds the two column
+// ranges). A plain 16-bit product would keep 11 (fp16) or 8 (bf16) bits. The decompression
 // ("32-bit products for the decompressed gradient", "Zero-Shot Text-to-Image Generation -
 // 中文验证版", §证据) uses three products of fp16 splits, so a dropped lo*lo term costs
 // ~2^-22.
 //
 // Persistent kernels, one CTA per SM. Warp 0 issues TMA loads into a ring of
 // shared-memory stages. Warp 1 owns TMEM and issues tcgen05.mma from one thread. Four
-// (P/Q GEMM) or eight (G^) epilogue warps drain the accumulators, which are double
-// buffered in TMEM so the next unit's MMAs overlap the epilogue. Every mbarrier wait is
+// (fused P GEMM) or eight (Q GEMM, G^) epilogue warps drain the accumulators, which are
+// double buffered in TMEM so the next segment's MMAs overlap the epilogue. Every mbarrier wait is
 // bounded. On expiry the kernel records DEVERR_TIMEOUT, waits (bounded) for its own
 // TMA loads, releases TMEM and returns.
 #include <cuda.h>
@@ -48,12 +48,15 @@ constexpr int PCHUNK_KB = 4;           // P GEMM: k-blocks of 64 columns per uni
 // accumulator per chained MMA, and those losses add up (they do not cancel like
 // round-to-nearest errors). So an accumulator chains a bounded number of MMAs: after each
 // segment of (k-block, worker) steps the epilogue adds the accumulator into a running sum
-// with round-to-nearest fp32 adds. In both GEMM kernels each K step issues one MMA per
-// split term of the fp32 operand into the same accumulator of rp columns, so a step
-// chains 8 (fp16) or 12 (bf16) MMAs: a Q GEMM segment of 16 steps chains 128 (fp16), a
-// fused P GEMM segment of 4 steps 32. The separate GEMMs keep the running sum in
-// registers and rotate four accumulators; the fused ingest kernel keeps it in TMEM next
-// to two accumulators. P's segments are shorter than Q's: errors in P are amplified by
+// with round-to-nearest fp32 adds. The fused ingest kernel issues one MMA per split term of
+// Q into the same accumulator of rp columns, so a (k-block, worker) step chains 8 (fp16)
+// or 12 (bf16) MMAs and a segment of 4 steps 32; it keeps the running sum in TMEM next to
+// two accumulators. The separate GEMM kernel multiplies the first two split terms in one
+// MMA of width 2 rp (term 0's products in columns [0, rp), term 1's in [rp, 2 rp); bf16's
+// third term goes onto term 0's columns), so a step chains 4 (fp16) or 8 (bf16) MMAs per
+// column and a segment of 16 steps 64 (fp16); the epilogue adds the two column ranges and
+// keeps the running sum in registers, with two accumulators in TMEM. P's segments are
+// shorter than Q's: errors in P are amplified by
 // cond(P) in the span of P^ (up to ~2e4 for a decaying spectrum at r = 112), errors in
 // Q reach G^ and E directly.
 constexpr int kGemmSegSteps = 16;
