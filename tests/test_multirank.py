@@ -226,3 +226,57 @@ def test_allreduce_step_matches_one_process_over_all_workers():
                     # E is f16-rounded on both sides: the fp64 sums differ in order only,
                     # so an entry may round the other way at most once in a long while
                     assert np.mean(got_e != want_e) < 1e-3
+
+
+_UNEVEN = (1, 2, 3)  # workers held by each of three ranks
+
+
+def _uneven_worker(rank, world, port, out):
+    import numpy as np
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        W_all = sum(_UNEVEN)
+        grads, errs, q = _exchange_inputs(_EX_B, W_all, _EX_SHAPES, _EX_R, 11)
+        lo = sum(_UNEVEN[:rank])
+        mine = slice(lo, lo + _UNEVEN[rank])
+        g = [[grads[b][j][mine] for j in range(len(_EX_SHAPES))] for b in range(_EX_B)]
+        e = [[errs[b][j][mine] for j in range(len(_EX_SHAPES))] for b in range(_EX_B)]
+        ghat = [[np.zeros((m, n)) for (m, n) in _EX_SHAPES] for _ in range(_EX_B)]
+        frac = 5.0 / (W_all * (24 * 16 + 16 * 32))  # threshold 5 over all six workers
+        eng = _OracleEngine(_EX_SHAPES, _EX_B, _UNEVEN[rank], _EX_R, frac, "f16")
+        w_total = pd.total_workers(_UNEVEN[rank])
+        pd.allreduce_step(eng, g, e, q, [1.0] * _EX_B, ghat, w_total)
+        out[rank] = (w_total, eng.skip, [[x.tolist() for x in row] for row in ghat])
+    finally:
+        dist.destroy_process_group()
+
+
+def test_allreduce_step_with_uneven_workers_per_rank():
+    """Three gloo ranks holding 1, 2 and 3 workers: the total worker count is summed, the
+    factors divided by it, and every rank ends with the oracle's G-hat over all six workers
+    and the same skip decisions (block 1's nonfinite entries sit on the last worker only)."""
+    import numpy as np
+    from oracle import powersgd as o
+    world = len(_UNEVEN)
+    port = _free_port()
+    with mp.Manager() as man:
+        out = man.dict()
+        mp.spawn(_uneven_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    W_all = sum(_UNEVEN)
+    assert all(res[k][0] == W_all for k in range(world))
+    grads, errs, q = _exchange_inputs(_EX_B, W_all, _EX_SHAPES, _EX_R, 11)
+    frac = 5.0 / (W_all * (24 * 16 + 16 * 32))
+    for b in range(_EX_B):
+        st = o.BlockState(e=[list(errs[b][j]) for j in range(len(_EX_SHAPES))],
+                          q=[q[b][j].copy() for j in range(len(_EX_SHAPES))])
+        want = o.block_step(grads[b], st, 1.0, "f16", skip_fraction=frac)
+        for k in range(world):
+            assert res[k][1][b] == want.skip
+            for j in range(len(_EX_SHAPES)):
+                gh = np.array(res[k][2][b][j])
+                assert np.linalg.norm(gh - want.g_hat[j]) <= 1e-12 * max(1.0, np.linalg.norm(want.g_hat[j]))
+    assert res[0][1] == [False, True, False]
